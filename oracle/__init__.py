@@ -1,0 +1,167 @@
+"""CPU oracle for im2win convolution -- test infrastructure only.
+
+Plain fp64 C (``oracle.c``) behind ctypes. Only ``tests/``, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import this
+package; the product library never does, and shares no code with it.
+
+Each wrapper names the passage of the method it follows:
+
+* ``conv_direct`` / ``conv_points`` -- direct convolution, the left column of
+  Fig. 1 of "Enabling Memory-efficient Im2win Convolution with Multi-precision
+  Support on GPU CUDA and Tensor Cores" (valid convolution, Table I shapes).
+* ``im2win`` -- the im2win transformation, Abstract of "Im2win: Memory
+  Efficient Convolution On SIMD Architectures" and Fig. 1 middle column.
+* ``conv_im2win`` -- convolution as dot products over window segments (same).
+* ``conv_im2col`` -- im2col + GEMM, Fig. 1 right column.
+
+Inputs are numpy arrays; floating inputs are widened to float64 exactly before
+the call (the caller has already rounded them to the dtype under test).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_I64 = ctypes.c_int64
+_PD = ctypes.POINTER(ctypes.c_double)
+_PI = ctypes.POINTER(ctypes.c_int64)
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (OpenMP when the compiler has it)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:3] + ["-fopenmp"] + base[3:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            shp = [_I64] * 9
+            lib.oracle_conv_direct.argtypes = [_PD, _PD, _PD, _PD] + shp
+            lib.oracle_conv_points.argtypes = [_PD, _PD, _PI, _I64, _PD, _PD] + shp
+            lib.oracle_conv_im2win.argtypes = [_PD, _PD, _PD] + shp
+            lib.oracle_conv_im2col.argtypes = [_PD, _PD, _PD] + shp
+            lib.oracle_im2win.argtypes = [ctypes.c_void_p, ctypes.c_void_p] + [_I64] * 6
+            for f in (lib.oracle_conv_direct, lib.oracle_conv_points, lib.oracle_conv_im2win,
+                      lib.oracle_conv_im2col, lib.oracle_im2win):
+                f.restype = ctypes.c_int
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loops use (1 without OpenMP)."""
+    return int(_load().oracle_num_threads())
+
+
+def out_shape(x_shape, w_shape, stride):
+    n, ci, hi, wi = x_shape
+    co, ci2, hf, wf = w_shape
+    if ci != ci2:
+        raise ValueError("channel mismatch")
+    sh, sw = stride
+    return (n, co, (hi - hf) // sh + 1, (wi - wf) // sw + 1)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _dp(a):
+    return a.ctypes.data_as(_PD)
+
+
+def _args(x, w, stride):
+    n, ci, hi, wi = x.shape
+    co, _, hf, wf = w.shape
+    return [n, ci, hi, wi, co, hf, wf, stride[0], stride[1]]
+
+
+def conv_direct(x, w, stride=(1, 1)):
+    """Direct convolution in fp64; returns (out, S) with S = sum |x||w| per output."""
+    x, w = _f64(x), _f64(w)
+    shp = out_shape(x.shape, w.shape, stride)
+    out = np.empty(shp, np.float64)
+    scale = np.empty(shp, np.float64)
+    rc = _load().oracle_conv_direct(_dp(x), _dp(w), _dp(out), _dp(scale), *_args(x, w, stride))
+    if rc:
+        raise ValueError("oracle_conv_direct: bad shape")
+    return out, scale
+
+
+def conv_points(x, w, idx, stride=(1, 1)):
+    """Direct-sum outputs at coordinates idx[t] = (n, co, ho, wo); returns (vals, S)."""
+    x, w = _f64(x), _f64(w)
+    idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64).reshape(-1, 4))
+    out = np.empty(len(idx), np.float64)
+    scale = np.empty(len(idx), np.float64)
+    rc = _load().oracle_conv_points(_dp(x), _dp(w), idx.ctypes.data_as(_PI), len(idx),
+                                    _dp(out), _dp(scale), *_args(x, w, stride))
+    if rc:
+        raise ValueError("oracle_conv_points: bad shape or index")
+    return out, scale
+
+
+def im2win(x, H_f, s_h):
+    """Window tensor win[n][ci][ho][w*H_f + r] = x[n][ci][ho*s_h + r][w], same dtype, byte copy."""
+    x = np.ascontiguousarray(x)
+    n, ci, hi, wi = x.shape
+    ho = (hi - H_f) // s_h + 1
+    win = np.empty((n, ci, ho, wi * H_f), dtype=x.dtype)
+    rc = _load().oracle_im2win(x.ctypes.data, win.ctypes.data, x.dtype.itemsize,
+                               n, ci, hi, wi, H_f, s_h)
+    if rc:
+        raise ValueError("oracle_im2win: bad shape")
+    return win
+
+
+def conv_im2win(x, w, stride=(1, 1)):
+    """Convolution through the fp64 window tensor and the re-laid filter."""
+    x, w = _f64(x), _f64(w)
+    win = im2win(x, w.shape[2], stride[0])
+    out = np.empty(out_shape(x.shape, w.shape, stride), np.float64)
+    rc = _load().oracle_conv_im2win(_dp(win), _dp(w), _dp(out), *_args(x, w, stride))
+    if rc:
+        raise ValueError("oracle_conv_im2win: bad shape")
+    return out
+
+
+def conv_im2col(x, w, stride=(1, 1)):
+    """Brute-force im2col + GEMM convolution in fp64 (small inputs)."""
+    x, w = _f64(x), _f64(w)
+    out = np.empty(out_shape(x.shape, w.shape, stride), np.float64)
+    rc = _load().oracle_conv_im2col(_dp(x), _dp(w), _dp(out), *_args(x, w, stride))
+    if rc:
+        raise ValueError("oracle_conv_im2col: bad shape")
+    return out
+
+
+def workspace_elems(x_shape, w_shape, stride):
+    """Element counts (input, window tensor, im2col matrix) for one problem."""
+    n, ci, hi, wi = x_shape
+    _, _, hf, wf = w_shape
+    _, _, ho, wo = out_shape(x_shape, w_shape, stride)
+    return n * ci * hi * wi, n * ci * ho * wi * hf, n * ci * hf * wf * ho * wo
