@@ -1,0 +1,140 @@
+/*
+ * im2win.h -- C ABI of the GB300 (sm_103a) im2win convolution library.
+ *
+ * The method is the im2win convolution of
+ *   [SIMD] "Im2win: Memory Efficient Convolution On SIMD Architectures" (Abstract), and
+ *   [GPU]  "Enabling Memory-efficient Im2win Convolution with Multi-precision Support
+ *           on GPU CUDA and Tensor Cores" (Abstract, Fig. 1, Tables I and II).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Shapes: N images, C_i input channels of H_i x W_i, C_o filters of C_i x H_f x W_f,
+ *    strides s_h, s_w; "valid" convolution with no padding or dilation, so
+ *    H_o = (H_i - H_f)/s_h + 1 and W_o = (W_i - W_f)/s_w + 1 (floor), which every
+ *    layer of [GPU] Table I satisfies. All sizes are int64_t and must be >= 1
+ *    (N may be 0: the call then does nothing), with H_f <= H_i and W_f <= W_i.
+ *  - Layouts are dense and row-major: x[N][C_i][H_i][W_i] (NCHW),
+ *    filt[C_o][C_i][H_f][W_f], out[N][C_o][H_o][W_o], and the window tensor
+ *    win[N][C_i][H_o][W_i*H_f].
+ *  - dtype is one of im2win_dtype. x, filt, win and out all have that dtype.
+ *    F16/BF16 convolutions multiply on the tensor cores with fp32 accumulation and
+ *    round the result to the input dtype (round-to-nearest-even); F32
+ *    convolutions run on the CUDA cores in fp32.
+ *  - Every pointer argument except `bytes` is a DEVICE pointer on the current
+ *    CUDA device, allocated and owned by the caller; the library never allocates,
+ *    frees or synchronises (except im2win_device_status, which synchronises the
+ *    given stream). Pointers must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    All work is enqueued asynchronously on it; calls on different streams that
+ *    share a workspace race.
+ *  - Return value: an im2win_status. Argument errors are reported before any work
+ *    is enqueued. IM2WIN_ERR_CUDA means a launch failed (cudaGetLastError).
+ *    Kernels that wait on in-kernel barriers give up after a bounded time and
+ *    record IM2WIN_ERR_TIMEOUT in the workspace's status word, which
+ *    im2win_device_status reads back.
+ */
+#ifndef IM2WIN_H
+#define IM2WIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    IM2WIN_F32 = 0,
+    IM2WIN_F16 = 1,
+    IM2WIN_BF16 = 2
+} im2win_dtype;
+
+typedef enum {
+    IM2WIN_OK = 0,
+    IM2WIN_ERR_INVALID_ARG = 1, /* bad shape, null pointer, unknown dtype or op */
+    IM2WIN_ERR_UNSUPPORTED = 2, /* well-formed but outside what the kernels handle */
+    IM2WIN_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+    IM2WIN_ERR_WORKSPACE = 4,   /* ws is NULL or ws_bytes is below the required size */
+    IM2WIN_ERR_CUDA = 5,        /* a CUDA call or kernel launch failed */
+    IM2WIN_ERR_TIMEOUT = 6      /* an in-kernel barrier wait gave up (device status only) */
+} im2win_status;
+
+/* Which call a workspace size is asked for. */
+typedef enum {
+    IM2WIN_OP_TRANSFORM = 0,  /* bytes of the window tensor `win` that im2win_transform writes */
+    IM2WIN_OP_CONV = 1,       /* workspace of im2win_conv (status block + re-laid filter) */
+    IM2WIN_OP_CONV_FUSED = 2  /* workspace of im2win_conv_fused (status block + re-laid filter) */
+} im2win_op;
+
+/*
+ * Bytes needed for `op` on this problem, written to *bytes (a HOST pointer).
+ * Pure host arithmetic: no device call. For IM2WIN_OP_TRANSFORM this is
+ * N*C_i*H_o*W_i*H_f*esz, the size of the window tensor ([SIMD] Abstract: one row of
+ * W_i*H_f unique elements per channel and output row). For the two convolutions it
+ * is a 256-byte status block plus the filter re-laid for the kernel that runs, each
+ * part rounded up to 256 bytes; the fused convolution needs no window tensor.
+ * Errors: INVALID_ARG for a bad shape, dtype or op, or bytes == NULL.
+ */
+im2win_status im2win_workspace_size(int op, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i,
+                                    int64_t C_o, int64_t H_f, int64_t W_f, int64_t s_h,
+                                    int64_t s_w, int dtype, size_t *bytes);
+
+/*
+ * The im2win transformation ([SIMD] Abstract; [GPU] Fig. 1, middle column):
+ *   win[n][ci][ho][w*H_f + r] = x[n][ci][ho*s_h + r][w]   for w < W_i, r < H_f,
+ * i.e. the H_f input rows under output row ho are flattened column by column into
+ * one contiguous window row; all W_i columns are kept. A bit-exact copy of
+ * esz-byte elements. Reads x (N*C_i*H_i*W_i elements), writes exactly
+ * N*C_i*H_o*W_i*H_f elements at win; C_o, W_f and s_w are validated but do not
+ * change the result. x and win must not overlap.
+ */
+im2win_status im2win_transform(const void *x, void *win, int64_t N, int64_t C_i, int64_t H_i,
+                               int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f,
+                               int64_t s_h, int64_t s_w, int dtype, void *stream);
+
+/*
+ * Convolution over a window tensor ([GPU] Abstract: full precision on CUDA cores,
+ * half precision on tensor cores; [SIMD] Abstract):
+ *   out[n][co][ho][wo] = sum_ci sum_{k < W_f*H_f} win[n][ci][ho][wo*s_w*H_f + k] * filt'[co][ci][k],
+ *   filt'[co][ci][j*H_f + r] = filt[co][ci][r][j],
+ * which equals the direct valid cross-correlation of x with filt. `win` is the
+ * output of im2win_transform for the same shape. The filter is re-laid into `ws`
+ * on every call (ws_bytes >= im2win_workspace_size(IM2WIN_OP_CONV, ...)).
+ * Errors: INVALID_ARG, MISALIGNED, WORKSPACE, UNSUPPORTED (shape beyond the
+ * kernels' index range), CUDA.
+ */
+im2win_status im2win_conv(const void *win, const void *filt, void *out, void *ws,
+                          size_t ws_bytes, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i,
+                          int64_t C_o, int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w,
+                          int dtype, void *stream);
+
+/*
+ * Fused im2win convolution: the same result as im2win_transform followed by
+ * im2win_conv, computed straight from the NCHW input. The kernel stages, in
+ * shared memory only, the unique input elements of the windows of the output
+ * tile it computes, so the window tensor is never written to device memory;
+ * the workspace holds only the re-laid filter and the status block
+ * (ws_bytes >= im2win_workspace_size(IM2WIN_OP_CONV_FUSED, ...)).
+ * Errors as for im2win_conv.
+ */
+im2win_status im2win_conv_fused(const void *x, const void *filt, void *out, void *ws,
+                                size_t ws_bytes, int64_t N, int64_t C_i, int64_t H_i,
+                                int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f,
+                                int64_t s_h, int64_t s_w, int dtype, void *stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char *im2win_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads the status word that the last convolution
+ * enqueued with workspace `ws` left in it: IM2WIN_OK, or IM2WIN_ERR_TIMEOUT if
+ * one of its in-kernel waits gave up. ws_bytes must cover the 256-byte status
+ * block. Returns IM2WIN_ERR_CUDA if the synchronisation or the copy fails.
+ */
+im2win_status im2win_device_status(const void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IM2WIN_H */

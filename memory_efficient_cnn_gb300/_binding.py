@@ -1,0 +1,202 @@
+"""ctypes binding of libim2win.so: argument marshalling only.
+
+The functions named like the C entry points take torch tensors (device memory
+owned by torch) and pass their data pointers, the shape arguments and the
+current CUDA stream to the library; every step of the computation runs in the
+library's kernels. There is no CPU path: if the library is missing, or the
+tensors are not CUDA tensors, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
+OP_TRANSFORM, OP_CONV, OP_CONV_FUSED = 0, 1, 2
+F32, F16, BF16 = 0, 1, 2
+_DTYPE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+
+EXPORTS = ("im2win_workspace_size", "im2win_transform", "im2win_conv", "im2win_conv_fused",
+           "im2win_status_string", "im2win_device_status")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Im2winError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libim2win.so (built in-tree by build.build()); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with memory_efficient_cnn_gb300.build.build() "
+                    "(nvcc, sm_103a); there is no fallback implementation")
+            L = ctypes.CDLL(path)
+            i64, vp, sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+            shp = [i64] * 9
+            L.im2win_workspace_size.argtypes = [ctypes.c_int] + shp + [ctypes.c_int, ctypes.POINTER(sz)]
+            L.im2win_transform.argtypes = [vp, vp] + shp + [ctypes.c_int, vp]
+            L.im2win_conv.argtypes = [vp, vp, vp, vp, sz] + shp + [ctypes.c_int, vp]
+            L.im2win_conv_fused.argtypes = [vp, vp, vp, vp, sz] + shp + [ctypes.c_int, vp]
+            L.im2win_status_string.argtypes = [ctypes.c_int]
+            L.im2win_status_string.restype = ctypes.c_char_p
+            L.im2win_device_status.argtypes = [vp, sz, vp]
+            for f in ("im2win_workspace_size", "im2win_transform", "im2win_conv",
+                      "im2win_conv_fused", "im2win_device_status"):
+                getattr(L, f).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().im2win_status_string(int(status)).decode()
+
+
+im2win_status_string = status_string
+
+
+def _check(fn, status):
+    if status != OK:
+        raise Im2winError(fn, status)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPE[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}; use float32, float16 or bfloat16") from None
+
+
+def _cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("im2win tensors must be CUDA tensors (no CPU implementation exists)")
+        if not t.is_contiguous():
+            raise ValueError("im2win tensors must be contiguous")
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def out_hw(H_i, W_i, H_f, W_f, s_h, s_w):
+    """Valid-convolution output extent (no padding)."""
+    return (H_i - H_f) // s_h + 1, (W_i - W_f) // s_w + 1
+
+
+def im2win_workspace_size(op: int, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, dtype: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("im2win_workspace_size",
+           lib().im2win_workspace_size(op, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, dtype,
+                                       ctypes.byref(out)))
+    return out.value
+
+
+def im2win_transform(x: torch.Tensor, win: torch.Tensor, C_o, H_f, W_f, s_h, s_w) -> None:
+    _cuda(x, win)
+    N, C_i, H_i, W_i = x.shape
+    if win.dtype != x.dtype:
+        raise TypeError("win must have the dtype of x")
+    need = im2win_workspace_size(OP_TRANSFORM, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
+                                 _dtype_code(x))
+    if win.numel() * win.element_size() < need:
+        raise ValueError("win is smaller than the window tensor")
+    _check("im2win_transform",
+           lib().im2win_transform(x.data_ptr(), win.data_ptr(), N, C_i, H_i, W_i, C_o, H_f, W_f,
+                                  s_h, s_w, _dtype_code(x), _stream(x)))
+
+
+def im2win_conv(win: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w) -> None:
+    _cuda(win, filt, out, ws)
+    if not (win.dtype == filt.dtype == out.dtype):
+        raise TypeError("win, filt and out must share a dtype")
+    _check("im2win_conv",
+           lib().im2win_conv(win.data_ptr(), filt.data_ptr(), out.data_ptr(), ws.data_ptr(),
+                             ws.numel() * ws.element_size(), N, C_i, H_i, W_i, C_o, H_f, W_f,
+                             s_h, s_w, _dtype_code(win), _stream(win)))
+
+
+def im2win_conv_fused(x: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                      s_h, s_w) -> None:
+    _cuda(x, filt, out, ws)
+    if not (x.dtype == filt.dtype == out.dtype):
+        raise TypeError("x, filt and out must share a dtype")
+    N, C_i, H_i, W_i = x.shape
+    C_o, _, H_f, W_f = filt.shape
+    _check("im2win_conv_fused",
+           lib().im2win_conv_fused(x.data_ptr(), filt.data_ptr(), out.data_ptr(), ws.data_ptr(),
+                                   ws.numel() * ws.element_size(), N, C_i, H_i, W_i, C_o, H_f,
+                                   W_f, s_h, s_w, _dtype_code(x), _stream(x)))
+
+
+def im2win_device_status(ws: torch.Tensor) -> int:
+    """Synchronise the current stream and return the status word of `ws`."""
+    _cuda(ws)
+    return lib().im2win_device_status(ws.data_ptr(), ws.numel() * ws.element_size(), _stream(ws))
+
+
+# ---------------------------------------------------------------- conveniences
+def workspace(op: int, x_shape, w_shape, stride, dtype: torch.dtype, device) -> torch.Tensor:
+    """Allocate (through torch) the workspace `op` needs."""
+    N, C_i, H_i, W_i = x_shape
+    C_o, _, H_f, W_f = w_shape
+    b = im2win_workspace_size(op, N, C_i, H_i, W_i, C_o, H_f, W_f, stride[0], stride[1],
+                              _DTYPE[dtype])
+    return torch.empty(max(b, 16), dtype=torch.uint8, device=device)
+
+
+def transform(x: torch.Tensor, H_f: int, s_h: int = 1) -> torch.Tensor:
+    """Window tensor win[N][C_i][H_o][W_i*H_f] of x."""
+    N, C_i, H_i, W_i = x.shape
+    H_o = (H_i - H_f) // s_h + 1
+    win = torch.empty((N, C_i, H_o, W_i * H_f), dtype=x.dtype, device=x.device)
+    im2win_transform(x, win, 1, H_f, 1, s_h, 1)
+    return win
+
+
+def conv(win: torch.Tensor, filt: torch.Tensor, stride=(1, 1), ws: torch.Tensor | None = None,
+         out: torch.Tensor | None = None) -> torch.Tensor:
+    """Convolution from a window tensor produced by transform()."""
+    N, C_i, H_o, L = win.shape
+    C_o, _, H_f, W_f = filt.shape
+    W_i = L // H_f
+    H_i = (H_o - 1) * stride[0] + H_f
+    _, W_o = out_hw(H_i, W_i, H_f, W_f, *stride)
+    if ws is None:
+        ws = workspace(OP_CONV, (N, C_i, H_i, W_i), filt.shape, stride, win.dtype, win.device)
+    if out is None:
+        out = torch.empty((N, C_o, H_o, W_o), dtype=win.dtype, device=win.device)
+    im2win_conv(win, filt, out, ws, N, C_i, H_i, W_i, C_o, H_f, W_f, stride[0], stride[1])
+    return out
+
+
+def conv_fused(x: torch.Tensor, filt: torch.Tensor, stride=(1, 1), ws: torch.Tensor | None = None,
+               out: torch.Tensor | None = None) -> torch.Tensor:
+    """Fused im2win convolution straight from the NCHW input."""
+    N, C_i, H_i, W_i = x.shape
+    C_o, _, H_f, W_f = filt.shape
+    H_o, W_o = out_hw(H_i, W_i, H_f, W_f, *stride)
+    if ws is None:
+        ws = workspace(OP_CONV_FUSED, x.shape, filt.shape, stride, x.dtype, x.device)
+    if out is None:
+        out = torch.empty((N, C_o, H_o, W_o), dtype=x.dtype, device=x.device)
+    im2win_conv_fused(x, filt, out, ws, stride[0], stride[1])
+    return out

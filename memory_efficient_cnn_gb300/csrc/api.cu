@@ -1,0 +1,142 @@
+// C ABI of the im2win library: argument validation, workspace sizing and
+// dispatch to the kernels. No allocation, no synchronisation (except
+// im2win_device_status), no CPU fallback: every result is computed on the GPU.
+#include <cstdint>
+#include <cstring>
+
+#include "im2win_internal.cuh"
+
+using namespace im2win;
+
+namespace {
+
+im2win_status make_shape(Shape &s, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i, int64_t C_o,
+                         int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w) {
+    if (N < 0 || C_i <= 0 || H_i <= 0 || W_i <= 0 || C_o <= 0 || H_f <= 0 || W_f <= 0 ||
+        s_h <= 0 || s_w <= 0 || H_f > H_i || W_f > W_i)
+        return IM2WIN_ERR_INVALID_ARG;
+    // keep every element count far from int64 overflow
+    const int64_t lim = int64_t(1) << 40;
+    if (N > lim || C_i > lim || H_i > lim || W_i > lim || C_o > lim ||
+        N * C_i > lim || H_i * W_i > lim || C_o * C_i > lim || H_f * W_f > lim)
+        return IM2WIN_ERR_UNSUPPORTED;
+    s.N = N; s.C_i = C_i; s.H_i = H_i; s.W_i = W_i; s.C_o = C_o;
+    s.H_f = H_f; s.W_f = W_f; s.s_h = s_h; s.s_w = s_w;
+    s.H_o = (H_i - H_f) / s_h + 1;
+    s.W_o = (W_i - W_f) / s_w + 1;
+    return IM2WIN_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t window_bytes(const Shape &s, int esz) {
+    return (size_t)(s.N * s.C_i * s.H_o * s.W_i * s.H_f) * (size_t)esz;
+}
+
+size_t conv_ws_bytes(const Shape &s, int dtype, bool fused) {
+    const size_t f = dtype == IM2WIN_F32 ? conv_f32_filter_bytes(s) : conv_tc_filter_bytes(s, fused);
+    return kStatusBytes + round_up(f, 256);
+}
+
+im2win_status conv_common(const void *src, const void *filt, void *out, void *ws, size_t ws_bytes,
+                          int64_t N, int64_t C_i, int64_t H_i, int64_t W_i, int64_t C_o,
+                          int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w, int dtype,
+                          void *stream, bool fused) {
+    Shape s;
+    im2win_status st = make_shape(s, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w);
+    if (st != IM2WIN_OK) return st;
+    if (elem_size(dtype) == 0) return IM2WIN_ERR_INVALID_ARG;
+    if (s.N == 0) return IM2WIN_OK;  // empty batch: nothing to read or write
+    if (!src || !filt || !out) return IM2WIN_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(filt) || !aligned16(out)) return IM2WIN_ERR_MISALIGNED;
+    if (!ws || ws_bytes < conv_ws_bytes(s, dtype, fused)) return IM2WIN_ERR_WORKSPACE;
+    if (!aligned16(ws)) return IM2WIN_ERR_MISALIGNED;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (dtype == IM2WIN_F32) {
+        if (!conv_f32_supported(s, fused)) return IM2WIN_ERR_UNSUPPORTED;
+        e = launch_conv_f32(src, filt, out, ws, s, fused, cs);
+    } else {
+        if (!conv_tc_supported(s, fused)) return IM2WIN_ERR_UNSUPPORTED;
+        e = launch_conv_tc(src, filt, out, ws, s, fused, dtype == IM2WIN_BF16, cs);
+    }
+    return e == cudaSuccess ? IM2WIN_OK : IM2WIN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+im2win_status im2win_workspace_size(int op, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i,
+                                    int64_t C_o, int64_t H_f, int64_t W_f, int64_t s_h,
+                                    int64_t s_w, int dtype, size_t *bytes) {
+    if (!bytes) return IM2WIN_ERR_INVALID_ARG;
+    Shape s;
+    im2win_status st = make_shape(s, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w);
+    if (st != IM2WIN_OK) return st;
+    const int esz = elem_size(dtype);
+    if (esz == 0) return IM2WIN_ERR_INVALID_ARG;
+    switch (op) {
+        case IM2WIN_OP_TRANSFORM: *bytes = window_bytes(s, esz); return IM2WIN_OK;
+        case IM2WIN_OP_CONV: *bytes = conv_ws_bytes(s, dtype, false); return IM2WIN_OK;
+        case IM2WIN_OP_CONV_FUSED: *bytes = conv_ws_bytes(s, dtype, true); return IM2WIN_OK;
+        default: return IM2WIN_ERR_INVALID_ARG;
+    }
+}
+
+im2win_status im2win_transform(const void *x, void *win, int64_t N, int64_t C_i, int64_t H_i,
+                               int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f,
+                               int64_t s_h, int64_t s_w, int dtype, void *stream) {
+    Shape s;
+    im2win_status st = make_shape(s, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w);
+    if (st != IM2WIN_OK) return st;
+    const int esz = elem_size(dtype);
+    if (esz == 0) return IM2WIN_ERR_INVALID_ARG;
+    if (s.N == 0) return IM2WIN_OK;  // empty batch: nothing to read or write
+    if (!x || !win) return IM2WIN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(win)) return IM2WIN_ERR_MISALIGNED;
+    if (!transform_supported(s, esz)) return IM2WIN_ERR_UNSUPPORTED;
+    cudaError_t e = launch_transform(x, win, s, esz, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? IM2WIN_OK : IM2WIN_ERR_CUDA;
+}
+
+im2win_status im2win_conv(const void *win, const void *filt, void *out, void *ws,
+                          size_t ws_bytes, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i,
+                          int64_t C_o, int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w,
+                          int dtype, void *stream) {
+    return conv_common(win, filt, out, ws, ws_bytes, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
+                       dtype, stream, false);
+}
+
+im2win_status im2win_conv_fused(const void *x, const void *filt, void *out, void *ws,
+                                size_t ws_bytes, int64_t N, int64_t C_i, int64_t H_i,
+                                int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f,
+                                int64_t s_h, int64_t s_w, int dtype, void *stream) {
+    return conv_common(x, filt, out, ws, ws_bytes, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
+                       dtype, stream, true);
+}
+
+const char *im2win_status_string(int status) {
+    switch (status) {
+        case IM2WIN_OK: return "ok";
+        case IM2WIN_ERR_INVALID_ARG: return "invalid argument";
+        case IM2WIN_ERR_UNSUPPORTED: return "unsupported shape";
+        case IM2WIN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case IM2WIN_ERR_WORKSPACE: return "workspace missing or too small";
+        case IM2WIN_ERR_CUDA: return "CUDA error";
+        case IM2WIN_ERR_TIMEOUT: return "in-kernel wait timed out";
+        default: return "unknown status";
+    }
+}
+
+im2win_status im2win_device_status(const void *ws, size_t ws_bytes, void *stream) {
+    if (!ws || ws_bytes < kStatusBytes) return IM2WIN_ERR_WORKSPACE;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return IM2WIN_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return IM2WIN_ERR_CUDA;
+    return word == 0 ? IM2WIN_OK : static_cast<im2win_status>(word);
+}
+
+}  // extern "C"

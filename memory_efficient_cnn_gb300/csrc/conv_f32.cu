@@ -1,0 +1,251 @@
+// fp32 im2win convolution on the CUDA cores (sm_103a).
+//
+// "Enabling Memory-efficient Im2win Convolution with Multi-precision Support
+// on GPU CUDA and Tensor Cores", Abstract (full precision on CUDA cores):
+//   out[n][co][ho][wo] = sum_ci sum_{k < W_f*H_f} win[n][ci][ho][wo*s_w*H_f + k] * filt'[co][ci][k]
+//   filt'[co][ci][j*H_f + r] = filt[co][ci][r][j]
+// Seen as a product of the filter matrix filt' (C_o x K, K = C_i*W_f*H_f,
+// row-major) with a matrix whose column for output pixel p = (ho, wo) is the
+// concatenation over ci of that pixel's contiguous window segments.
+//
+// Kernel: a CTA computes TM output channels x 128 pixels of one image.
+// The K dimension is walked in chunks of 16; each chunk's window segments
+// (16 x 128) and filter slice (16 x TM) are staged in shared memory, double
+// buffered through registers, and every thread accumulates an 8 x 4
+// (channels x pixels) register tile with FFMA. Warps are 4 channel-groups x
+// 8 pixel-groups so that the shared-memory operand reads are broadcasts.
+// The fused variant (FROM_X) gathers the same matrix straight from the NCHW
+// input (x[n][ci][ho*s_h + r][wo*s_w + j] for k = j*H_f + r) and never
+// materialises the window tensor.
+#include <algorithm>
+
+#include "im2win_internal.cuh"
+
+namespace im2win {
+namespace {
+
+constexpr int TP = 128;  // pixels per CTA
+constexpr int KC = 16;   // K per stage
+
+struct F32Params {
+    const float *src;    // window tensor or NCHW input
+    const float *filt;   // filt' [C_o][K]
+    float *out;
+    uint32_t *status;
+    int C_i, C_o, H_o, W_o, H_i, W_i, H_f, s_h, s_w;
+    int P;               // H_o * W_o
+    int K;               // C_i * W_f * H_f
+    int KK;              // W_f * H_f
+    int pos_tiles;       // ceil(P / TP)
+    int L;               // W_i * H_f
+    int S;               // s_w * H_f
+    int64_t img_src;     // elements of src per image
+    FastDiv div_KK, div_Wo, div_Hf;
+};
+
+template <int TM, bool FROM_X>
+__global__ void __launch_bounds__(TM * 4) conv_f32_kernel(F32Params p) {
+    constexpr int NT = TM * 4;
+    constexpr int A_PER = KC * TP / NT;   // window elements each thread stages
+    constexpr int B_PER = KC * TM / NT;   // filter elements each thread stages (4)
+    __shared__ __align__(16) float As[2][KC][TP + 4];
+    __shared__ __align__(16) float Bs[2][KC][TM + 4];
+
+    const int tid = threadIdx.x;
+    const int n = blockIdx.x / p.pos_tiles;
+    const int p0 = (blockIdx.x - n * p.pos_tiles) * TP;
+    const int co0 = blockIdx.y * TM;
+    const float *__restrict__ src = p.src + (int64_t)n * p.img_src;
+    const float *__restrict__ filt = p.filt;
+
+    // ---- per-thread staging coordinates (k fixed, A_PER pixels)
+    const int ka = tid % KC;
+    int pos_off[A_PER];
+#pragma unroll
+    for (int i = 0; i < A_PER; ++i) {
+        int pl = tid / KC + i * (NT / KC);
+        int pg = p0 + pl;
+        if (pg < p.P) {
+            int ho = (int)fdiv((uint32_t)pg, p.div_Wo);
+            int wo = pg - ho * p.W_o;
+            pos_off[i] = FROM_X ? (ho * p.s_h * p.W_i + wo * p.s_w) : (ho * p.L + wo * p.S);
+        } else {
+            pos_off[i] = -1;
+        }
+    }
+    const int kb = tid % KC;
+    int co_b[B_PER];
+#pragma unroll
+    for (int i = 0; i < B_PER; ++i) co_b[i] = tid / KC + i * (NT / KC);
+
+    // ---- compute coordinates
+    const int warp = tid >> 5, lane = tid & 31;
+    const int ty = (warp >> 2) * 4 + (lane >> 3);  // channel group: 8 channels
+    const int tx = (warp & 3) * 8 + (lane & 7);     // pixel group: 4 pixels
+
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+    float ra[A_PER], rb[B_PER];
+    auto load_chunk = [&](int kc0) {
+        const int kg = kc0 + ka;
+        int coff = -1;
+        if (kg < p.K) {
+            int ci = (int)fdiv((uint32_t)kg, p.div_KK);
+            int kk = kg - ci * p.KK;
+            if (FROM_X) {
+                int j = (int)fdiv((uint32_t)kk, p.div_Hf);
+                int r = kk - j * p.H_f;
+                coff = (ci * p.H_i + r) * p.W_i + j;
+            } else {
+                coff = ci * p.H_o * p.L + kk;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < A_PER; ++i)
+            ra[i] = (coff >= 0 && pos_off[i] >= 0) ? __ldg(src + pos_off[i] + coff) : 0.f;
+        const int kgb = kc0 + kb;
+#pragma unroll
+        for (int i = 0; i < B_PER; ++i) {
+            int co = co0 + co_b[i];
+            rb[i] = (kgb < p.K && co < p.C_o) ? __ldg(filt + (int64_t)co * p.K + kgb) : 0.f;
+        }
+    };
+    auto store_chunk = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < A_PER; ++i) As[buf][ka][tid / KC + i * (NT / KC)] = ra[i];
+#pragma unroll
+        for (int i = 0; i < B_PER; ++i) Bs[buf][kb][co_b[i]] = rb[i];
+    };
+
+    const int nchunks = (p.K + KC - 1) / KC;
+    load_chunk(0);
+    store_chunk(0);
+    __syncthreads();
+    for (int c = 0; c < nchunks; ++c) {
+        const int buf = c & 1;
+        if (c + 1 < nchunks) load_chunk((c + 1) * KC);
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+            const float4 a = *reinterpret_cast<const float4 *>(&As[buf][k][tx * 4]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8 + 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(bv[i], av[j], acc[i][j]);
+        }
+        if (c + 1 < nchunks) store_chunk(buf ^ 1);
+        __syncthreads();
+    }
+
+    // ---- epilogue: out[n][co][p]
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int co = co0 + ty * 8 + i;
+        if (co >= p.C_o) continue;
+        float *orow = p.out + ((int64_t)n * p.C_o + co) * p.P;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int pg = p0 + tx * 4 + j;
+            if (pg < p.P) orow[pg] = acc[i][j];
+        }
+    }
+}
+
+// filt'[co][ci*KK + j*H_f + r] = filt[co][ci][r][j]; block 0 also clears the
+// workspace status word for this call.
+__global__ void relayout_filter_f32(const float *__restrict__ filt, float *__restrict__ fp,
+                                    uint32_t *status, int64_t total, int C_i, int H_f, int W_f) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) status[0] = 0;
+    const int64_t KK = (int64_t)H_f * W_f;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        int64_t j = e % W_f;
+        int64_t t = e / W_f;
+        int64_t r = t % H_f;
+        int64_t cc = t / H_f;  // co*C_i + ci
+        fp[cc * KK + j * H_f + r] = filt[e];
+    }
+}
+
+template <int TM, bool FROM_X>
+cudaError_t launch_tm(const F32Params &p, int N, cudaStream_t st) {
+    dim3 grid((unsigned)(p.pos_tiles * N), (unsigned)((p.C_o + TM - 1) / TM));
+    conv_f32_kernel<TM, FROM_X><<<grid, TM * 4, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t conv_f32_filter_bytes(const Shape &s) {
+    return round_up((size_t)(s.C_o * s.C_i * s.H_f * s.W_f) * 4, 256);
+}
+
+bool conv_f32_supported(const Shape &s, bool from_x) {
+    const int64_t img = from_x ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * s.W_i * s.H_f;
+    const int64_t P = s.H_o * s.W_o;
+    const int64_t tiles = (P + TP - 1) / TP;
+    return img < (1ll << 31) && s.C_i * s.H_f * s.W_f < (1ll << 31) && tiles * s.N < (1ll << 31) &&
+           (s.C_o + 31) / 32 < 65536;
+}
+
+cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *ws,
+                            const Shape &s, bool from_x, cudaStream_t st) {
+    uint32_t *status = static_cast<uint32_t *>(ws);
+    float *fp = reinterpret_cast<float *>(static_cast<unsigned char *>(ws) + kStatusBytes);
+    const int64_t total = s.C_o * s.C_i * s.H_f * s.W_f;
+    relayout_filter_f32<<<(unsigned)std::min<int64_t>((total + 255) / 256, 4096), 256, 0, st>>>(
+        static_cast<const float *>(filt), fp, status, total, (int)s.C_i, (int)s.H_f, (int)s.W_f);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || s.N == 0) return e;
+
+    F32Params p;
+    p.src = static_cast<const float *>(src);
+    p.filt = fp;
+    p.out = static_cast<float *>(out);
+    p.status = status;
+    p.C_i = (int)s.C_i;
+    p.C_o = (int)s.C_o;
+    p.H_o = (int)s.H_o;
+    p.W_o = (int)s.W_o;
+    p.H_i = (int)s.H_i;
+    p.W_i = (int)s.W_i;
+    p.H_f = (int)s.H_f;
+    p.s_h = (int)s.s_h;
+    p.s_w = (int)s.s_w;
+    p.P = (int)(s.H_o * s.W_o);
+    p.K = (int)(s.C_i * s.H_f * s.W_f);
+    p.KK = (int)(s.H_f * s.W_f);
+    p.pos_tiles = (p.P + TP - 1) / TP;
+    p.L = (int)(s.W_i * s.H_f);
+    p.S = (int)(s.s_w * s.H_f);
+    p.img_src = from_x ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * s.W_i * s.H_f;
+    p.div_KK = make_fastdiv((uint32_t)(s.H_f * s.W_f));
+    p.div_Wo = make_fastdiv((uint32_t)s.W_o);
+    p.div_Hf = make_fastdiv((uint32_t)s.H_f);
+
+    // channel tile with the least padding (ties: the larger tile)
+    int best = 128;
+    int64_t best_pad = (s.C_o + 127) / 128 * 128 - s.C_o;
+    for (int tm : {64, 32}) {
+        int64_t pad = (s.C_o + tm - 1) / tm * tm - s.C_o;
+        if (pad < best_pad) { best = tm; best_pad = pad; }
+    }
+    const int N = (int)s.N;
+    if (from_x) {
+        if (best == 128) return launch_tm<128, true>(p, N, st);
+        if (best == 64) return launch_tm<64, true>(p, N, st);
+        return launch_tm<32, true>(p, N, st);
+    }
+    if (best == 128) return launch_tm<128, false>(p, N, st);
+    if (best == 64) return launch_tm<64, false>(p, N, st);
+    return launch_tm<32, false>(p, N, st);
+}
+
+}  // namespace im2win
