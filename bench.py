@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Benchmark of the im2win hot path on GB300.
+
+One step runs every operation of the path once over one batch of the cv1
+layer of Table I of "Enabling Memory-efficient Im2win Convolution with
+Multi-precision Support on GPU CUDA and Tensor Cores" (N=128, C_i=3, 227x227,
+C_o=96, 11x11, stride 4), in fp16 and fp32, with seeded synthetic inputs:
+
+  1. im2win transform, fp16             (x16 -> win16)
+  2. tensor-core conv from the window   (win16, w16 -> out16; filter re-layout + tcgen05 kernel)
+  3. fused tensor-core conv             (x16, w16 -> out16f; filter re-layout + tcgen05 kernel)
+  4. im2win transform, fp32             (x32 -> win32)
+  5. CUDA-core conv from the window     (win32, w32 -> out32; filter re-layout + FFMA kernel)
+
+value = conv FLOPs of the step (3 x 2*N*C_o*H_o*W_o*C_i*H_f*W_f) / step time, in TFLOP/s,
+summed over ranks (each rank runs its own batch: weak scaling, no collective on
+the data path). Inputs are resident in HBM when the timed region starts; L2 is
+flushed (a 512 MB write) between timed steps, outside the timed region.
+
+`--impl reference` times the CPU oracle (plain fp64 C, OpenMP) on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
+# kernel on this workload, from one ncu capture of the current kernel source
+# (summaries under profiles/); a kernel absent here has no capture of its
+# current version.
+DRAM_TRAFFIC: dict = {}
+
+METRIC = "im2win conv TFLOPS and % of dense peak per layer shape; workspace bytes"
+UNIT = "TFLOP/s"
+SMS = 152
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "sm_max_mhz": float(d.get("sm_max_mhz", 2070.0)), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.out = os.path.join("/tmp", f"im2win_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.out, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.out) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        try:
+            os.unlink(self.out)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def conv_flops(layer) -> float:
+    ho = (layer.H_i - layer.H_f) // layer.s_h + 1
+    wo = (layer.W_i - layer.W_f) // layer.s_w + 1
+    return 2.0 * layer.N * layer.C_o * ho * wo * layer.C_i * layer.H_f * layer.W_f
+
+
+def cpu_oracle_rate(layer, budget_s: float, max_images: int | None = None):
+    """The oracle as it stands (fp64 direct conv) on the first images of the
+    batch, fp16-rounded inputs then fp32 inputs, until `budget_s` is spent."""
+    import oracle
+    from memory_efficient_cnn_gb300 import workloads as wl
+
+    oracle.build()
+    x16, w16 = wl.make_inputs(layer, "f16", n_images=8)
+    x32, w32 = wl.make_inputs(layer, "f32", n_images=8)
+    per_img = conv_flops(layer) / layer.N
+    done_imgs, t_total = 0, 0.0
+    limit = max_images if max_images is not None else 10 ** 9
+    i = 0
+    while (t_total < budget_s or done_imgs == 0) and done_imgs < limit:
+        x, w = (x16, w16) if i % 2 == 0 else (x32, w32)
+        n = (i // 2) % x.shape[0]
+        xd, wd = x[n:n + 1].double().numpy(), w.double().numpy()
+        t0 = time.perf_counter()
+        oracle.im2win(xd, layer.H_f, layer.s_h)
+        oracle.conv_direct(xd, wd, (layer.s_h, layer.s_w))
+        t_total += time.perf_counter() - t0
+        done_imgs += 1
+        i += 1
+    return per_img * done_imgs / t_total / 1e12, done_imgs, t_total, oracle.num_threads()
+
+
+def run_reference(args, layer, rank, world):
+    if rank != 0:
+        return
+    # each step: the oracle on a bounded sample of images of the workload
+    steps = []
+    threads = 1
+    for s in range(args.warmup + args.steps):
+        rate, imgs, t, threads = cpu_oracle_rate(layer, budget_s=0.0, max_images=2)
+        if s >= args.warmup:
+            steps.append((rate, imgs, t))
+    flops = conv_flops(layer) / layer.N
+    tot_t = sum(t for _, _, t in steps)
+    tot_imgs = sum(i for _, i, _ in steps)
+    value = flops * tot_imgs / tot_t / 1e12
+    sample = (f"{tot_imgs // len(steps)} images of {layer.name} per step (im2win transform + fp64 "
+              f"direct conv; fp16-rounded and fp32 inputs alternate)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / len(steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{layer.name}: N={layer.N}, C_i={layer.C_i}, {layer.H_i}x{layer.W_i}, "
+                               f"C_o={layer.C_o}, {layer.H_f}x{layer.W_f}, stride {layer.s_h}",
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle time for the cpu_baseline (0 disables it)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from memory_efficient_cnn_gb300 import workloads as wl
+
+    layer = wl.CV1
+    rank, world, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, layer, rank, world)
+        return
+
+    import torch
+
+    import memory_efficient_cnn_gb300 as mec
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    mec.lib()  # fail loudly if the library is missing
+
+    # cpu baseline first (rank 0, N=1 only): before any other GPU work is queued
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        rate, imgs, t, threads = cpu_oracle_rate(layer, args.cpu_budget)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{imgs} images of {layer.name} (im2win transform + fp64 direct conv, "
+                         f"fp16-rounded and fp32 inputs alternating), {t:.1f} s"}
+
+    x16c, w16c = wl.make_inputs(layer, "f16")
+    x32c, w32c = wl.make_inputs(layer, "f32")
+    x16, w16, x32, w32 = (t.to(dev) for t in (x16c, w16c, x32c, w32c))
+    shp = layer.shape_args
+    stride = (layer.s_h, layer.s_w)
+    H_o, W_o = mec.out_hw(layer.H_i, layer.W_i, layer.H_f, layer.W_f, *stride)
+    N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w = shp
+    win16 = torch.empty((N, C_i, H_o, W_i * H_f), dtype=torch.float16, device=dev)
+    win32 = torch.empty((N, C_i, H_o, W_i * H_f), dtype=torch.float32, device=dev)
+    out16 = torch.empty((N, C_o, H_o, W_o), dtype=torch.float16, device=dev)
+    out16f = torch.empty_like(out16)
+    out32 = torch.empty((N, C_o, H_o, W_o), dtype=torch.float32, device=dev)
+    ws16 = mec.workspace(mec.OP_CONV, x16.shape, w16.shape, stride, torch.float16, dev)
+    ws16f = mec.workspace(mec.OP_CONV_FUSED, x16.shape, w16.shape, stride, torch.float16, dev)
+    ws32 = mec.workspace(mec.OP_CONV, x32.shape, w32.shape, stride, torch.float32, dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    names = ["transform_f16", "conv_tc_window_f16", "conv_tc_fused_f16", "transform_f32",
+             "conv_f32_window"]
+    LAUNCHES_PER_STEP = 8  # 2 transforms + 3 x (filter re-layout + convolution)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        mec.im2win_transform(x16, win16, C_o, H_f, W_f, s_h, s_w)
+        if evs:
+            evs[1].record(stream)
+        mec.im2win_conv(win16, w16, out16, ws16, *shp)
+        if evs:
+            evs[2].record(stream)
+        mec.im2win_conv_fused(x16, w16, out16f, ws16f, s_h, s_w)
+        if evs:
+            evs[3].record(stream)
+        mec.im2win_transform(x32, win32, C_o, H_f, W_f, s_h, s_w)
+        if evs:
+            evs[4].record(stream)
+        mec.im2win_conv(win32, w32, out32, ws32, *shp)
+        if evs:
+            evs[5].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    for k in range(args.steps):
+        step(ev[k])
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if dist:
+        dist.barrier()
+    per = [[ev[k][i].elapsed_time(ev[k][i + 1]) for i in range(5)] for k in range(args.steps)]
+    step_ms = sum(sum(p) for p in per)
+    kern_ms = [sum(p[i] for p in per) / args.steps for i in range(5)]
+
+    # ---- end to end through the public API from pinned host buffers
+    h_in = [t.pin_memory() for t in (x16c, w16c, x32c, w32c)]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (out16, out16f, out32)]
+    d_in = [x16, w16, x32, w32]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def e2e_step():
+        for d, h in zip(d_in, h_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(h_out, (out16, out16f, out32)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for k in range(args.steps):
+        e_start[k].record(stream)
+        e2e_step()
+        e_end[k].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(e_start[k].elapsed_time(e_end[k]) for k in range(args.steps))
+
+    if dist:
+        t = torch.tensor([step_ms, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, e2e_ms = float(t[0]), float(t[1])
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    f = conv_flops(layer)
+    ms = step_ms / args.steps
+    value = world * 3 * f / (ms * 1e-3) / 1e12
+    e2e_value = world * 3 * f / (e2e_ms / args.steps * 1e-3) / 1e12
+    pk = _peaks()
+    fp32_peak = SMS * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12  # FFMA lanes x 2 flop x clock
+    esz = {"f16": 2, "f32": 4}
+    x_b = {d: N * C_i * H_i * W_i * esz[d] for d in esz}
+    win_b = {d: N * C_i * H_o * W_i * H_f * esz[d] for d in esz}
+    out_b = {d: N * C_o * H_o * W_o * esz[d] for d in esz}
+    w_b = {d: C_o * C_i * H_f * W_f * esz[d] for d in esz}
+    col_b = {d: N * C_i * H_f * W_f * H_o * W_o * esz[d] for d in esz}
+    kernels = {}
+    for i, name in enumerate(names):
+        t_s = kern_ms[i] * 1e-3
+        d = "f32" if name.endswith("f32") or name.startswith("conv_f32") else "f16"
+        if name.startswith("transform"):
+            byts = x_b[d] + win_b[d]
+            kernels[name] = {"ms": kern_ms[i], "bound": "hbm", "achieved": byts / t_s / 1e9,
+                             "peak": pk["hbm_gbs"], "unit": "GB/s", "alg_bytes": byts}
+        elif name == "conv_f32_window":
+            kernels[name] = {"ms": kern_ms[i], "bound": "alu", "achieved": f / t_s / 1e12,
+                             "peak": fp32_peak, "unit": "TFLOP/s", "flops": f}
+        else:
+            byts = (win_b[d] if "window" in name else x_b[d]) + w_b[d] + out_b[d]
+            tc_peak = pk["bf16_tflops"]
+            hbm_cap = f / byts * pk["hbm_gbs"] * 1e9 / 1e12
+            bound = "tensor" if tc_peak < hbm_cap else "hbm"
+            kernels[name] = {"ms": kern_ms[i], "bound": bound, "achieved": f / t_s / 1e12,
+                             "peak": min(tc_peak, hbm_cap), "unit": "TFLOP/s", "flops": f,
+                             "alg_bytes": byts, "tensor_peak_frac": f / t_s / 1e12 / tc_peak}
+        kernels[name]["frac"] = kernels[name]["achieved"] / kernels[name]["peak"]
+    dom = max(kernels, key=lambda k: kernels[k]["ms"])
+    dk = kernels[dom]
+    traffic = DRAM_TRAFFIC.get(dom)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16+f32", "data": "synthetic",
+        "config": {"workload": f"{layer.name}: N={N}, C_i={C_i}, {H_i}x{W_i}, C_o={C_o}, "
+                               f"{H_f}x{W_f}, stride {s_h}; fp16 and fp32",
+                   "step": "transform f16, tc conv from window f16, fused tc conv f16, "
+                           "transform f32, fp32 conv from window",
+                   "parallelism": f"replicas x{world}", "l2": "flushed between steps (512 MB write)"},
+        "roofline": {"kernel": dom, "bound": dk["bound"], "achieved": dk["achieved"],
+                     "peak": dk["peak"], "unit": dk["unit"], "frac": dk["frac"],
+                     "traffic": traffic,
+                     "peak_source": "fp32 FFMA: 152 SMs x 128 lanes x 2 x max SM clock"
+                     if dk["bound"] == "alu" else pk["source"]},
+        "kernels": kernels,
+        "workspace_bytes": {
+            "two_step_f16": win_b["f16"] + ws16.numel(), "fused_f16": ws16f.numel(),
+            "im2col_f16": col_b["f16"], "two_step_f32": win_b["f32"] + ws32.numel(),
+            "im2col_f32": col_b["f32"]},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "peaks": pk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
