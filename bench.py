@@ -129,8 +129,9 @@ def cpu_oracle_rate(layer, budget_s: float, max_images: int | None = None):
     from memory_efficient_cnn_gb300 import workloads as wl
 
     oracle.build()
-    x16, w16 = wl.make_inputs(layer, "f16", n_images=8)
-    x32, w32 = wl.make_inputs(layer, "f32", n_images=8)
+    d_lo, d_hi = layer.dtypes[0], layer.dtypes[-1]
+    x16, w16 = wl.make_inputs(layer, d_lo, n_images=8)
+    x32, w32 = wl.make_inputs(layer, d_hi, n_images=8)
     per_img = conv_flops(layer) / layer.N
     done_imgs, t_total = 0, 0.0
     limit = max_images if max_images is not None else 10 ** 9
@@ -185,6 +186,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layer", default="cv1",
+                    help="workload: cv1 (default, the headline) or another layer of the parity set")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline (0 disables it)")
     args = ap.parse_args()
@@ -193,7 +196,10 @@ def main():
 
     from memory_efficient_cnn_gb300 import workloads as wl
 
-    layer = wl.CV1
+    layers = {l.name: l for l in wl.ALL}
+    if args.layer not in layers:
+        ap.error(f"--layer must be one of {sorted(layers)}")
+    layer = layers[args.layer]
     rank, world, local = _dist()
     if args.impl == "reference":
         run_reference(args, layer, rank, world)
@@ -217,55 +223,61 @@ def main():
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         rate, imgs, t, threads = cpu_oracle_rate(layer, args.cpu_budget)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"{imgs} images of {layer.name} (im2win transform + fp64 direct conv, "
-                         f"fp16-rounded and fp32 inputs alternating), {t:.1f} s"}
+               "sample": f"{imgs} images of {layer.name} (im2win transform + fp64 direct conv of the "
+                         f"{'/'.join(layer.dtypes)} inputs, alternating), {t:.1f} s"}
 
-    x16c, w16c = wl.make_inputs(layer, "f16")
-    x32c, w32c = wl.make_inputs(layer, "f32")
-    x16, w16, x32, w32 = (t.to(dev) for t in (x16c, w16c, x32c, w32c))
-    shp = layer.shape_args
     stride = (layer.s_h, layer.s_w)
-    H_o, W_o = mec.out_hw(layer.H_i, layer.W_i, layer.H_f, layer.W_f, *stride)
+    shp = layer.shape_args
     N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w = shp
-    win16 = torch.empty((N, C_i, H_o, W_i * H_f), dtype=torch.float16, device=dev)
-    win32 = torch.empty((N, C_i, H_o, W_i * H_f), dtype=torch.float32, device=dev)
-    out16 = torch.empty((N, C_o, H_o, W_o), dtype=torch.float16, device=dev)
-    out16f = torch.empty_like(out16)
-    out32 = torch.empty((N, C_o, H_o, W_o), dtype=torch.float32, device=dev)
-    ws16 = mec.workspace(mec.OP_CONV, x16.shape, w16.shape, stride, torch.float16, dev)
-    ws16f = mec.workspace(mec.OP_CONV_FUSED, x16.shape, w16.shape, stride, torch.float16, dev)
-    ws32 = mec.workspace(mec.OP_CONV, x32.shape, w32.shape, stride, torch.float32, dev)
+    H_o, W_o = mec.out_hw(H_i, W_i, H_f, W_f, *stride)
+
+    # one step: per dtype, the transform, the conv from the window tensor and
+    # (fp16/bf16) the fused conv; fp32 runs on the CUDA cores
+    ops, host_in, dev_in, outs = [], [], [], []
+    for d in layer.dtypes:
+        tdt = wl.DTYPES[d]
+        xc, wc = wl.make_inputs(layer, d)
+        x, w = xc.to(dev), wc.to(dev)
+        host_in += [xc, wc]
+        dev_in += [x, w]
+        win = torch.empty((N, C_i, H_o, W_i * H_f), dtype=tdt, device=dev)
+        out_w = torch.empty((N, C_o, H_o, W_o), dtype=tdt, device=dev)
+        ws = mec.workspace(mec.OP_CONV, x.shape, w.shape, stride, tdt, dev)
+        ops.append((f"transform_{d}", d, "transform",
+                    lambda x=x, win=win: mec.im2win_transform(x, win, C_o, H_f, W_f, s_h, s_w),
+                    {"win_bytes": win.numel() * win.element_size()}))
+        kind = "conv_f32" if d == "f32" else "conv_tc"
+        ops.append((f"{kind}_window_{d}", d, "window",
+                    lambda win=win, w=w, o=out_w, ws=ws: mec.im2win_conv(win, w, o, ws, *shp),
+                    {"ws_bytes": ws.numel()}))
+        outs.append(out_w)
+        if d != "f32":
+            out_f = torch.empty_like(out_w)
+            wsf = mec.workspace(mec.OP_CONV_FUSED, x.shape, w.shape, stride, tdt, dev)
+            ops.append((f"conv_tc_fused_{d}", d, "fused",
+                        lambda x=x, w=w, o=out_f, ws=wsf: mec.im2win_conv_fused(x, w, o, ws, s_h, s_w),
+                        {"ws_bytes": wsf.numel()}))
+            outs.append(out_f)
+    names = [o[0] for o in ops]
+    n_ops = len(ops)
+    n_convs = sum(1 for o in ops if o[2] != "transform")
+    LAUNCHES_PER_STEP = sum(1 if o[2] == "transform" else 2 for o in ops)  # conv: re-layout + kernel
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    names = ["transform_f16", "conv_tc_window_f16", "conv_tc_fused_f16", "transform_f32",
-             "conv_f32_window"]
-    LAUNCHES_PER_STEP = 8  # 2 transforms + 3 x (filter re-layout + convolution)
-
     def step(evs=None):
+        for i, op in enumerate(ops):
+            if evs:
+                evs[i].record(stream)
+            op[3]()
         if evs:
-            evs[0].record(stream)
-        mec.im2win_transform(x16, win16, C_o, H_f, W_f, s_h, s_w)
-        if evs:
-            evs[1].record(stream)
-        mec.im2win_conv(win16, w16, out16, ws16, *shp)
-        if evs:
-            evs[2].record(stream)
-        mec.im2win_conv_fused(x16, w16, out16f, ws16f, s_h, s_w)
-        if evs:
-            evs[3].record(stream)
-        mec.im2win_transform(x32, win32, C_o, H_f, W_f, s_h, s_w)
-        if evs:
-            evs[4].record(stream)
-        mec.im2win_conv(win32, w32, out32, ws32, *shp)
-        if evs:
-            evs[5].record(stream)
+            evs[n_ops].record(stream)
 
     for _ in range(args.warmup):
         step()
         flush.zero_()
     torch.cuda.synchronize(dev)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ops + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     if dist:
         dist.barrier()
@@ -279,23 +291,22 @@ def main():
     clocks = sampler.stop()
     if dist:
         dist.barrier()
-    per = [[ev[k][i].elapsed_time(ev[k][i + 1]) for i in range(5)] for k in range(args.steps)]
+    per = [[ev[k][i].elapsed_time(ev[k][i + 1]) for i in range(n_ops)] for k in range(args.steps)]
     step_ms = sum(sum(p) for p in per)
-    kern_ms = [sum(p[i] for p in per) / args.steps for i in range(5)]
+    kern_ms = [sum(p[i] for p in per) / args.steps for i in range(n_ops)]
 
     # ---- end to end through the public API from pinned host buffers
-    h_in = [t.pin_memory() for t in (x16c, w16c, x32c, w32c)]
-    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (out16, out16f, out32)]
-    d_in = [x16, w16, x32, w32]
+    h_in = [t.pin_memory() for t in host_in]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
 
     def e2e_step():
-        for d, h in zip(d_in, h_in):
-            d.copy_(h, non_blocking=True)
+        for d_, h in zip(dev_in, h_in):
+            d_.copy_(h, non_blocking=True)
         step()
-        for h, d in zip(h_out, (out16, out16f, out32)):
-            h.copy_(d, non_blocking=True)
+        for h, d_ in zip(h_out, outs):
+            h.copy_(d_, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -320,29 +331,28 @@ def main():
 
     f = conv_flops(layer)
     ms = step_ms / args.steps
-    value = world * 3 * f / (ms * 1e-3) / 1e12
-    e2e_value = world * 3 * f / (e2e_ms / args.steps * 1e-3) / 1e12
+    value = world * n_convs * f / (ms * 1e-3) / 1e12
+    e2e_value = world * n_convs * f / (e2e_ms / args.steps * 1e-3) / 1e12
     pk = _peaks()
     fp32_peak = SMS * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12  # FFMA lanes x 2 flop x clock
-    esz = {"f16": 2, "f32": 4}
+    esz = {"f16": 2, "bf16": 2, "f32": 4}
     x_b = {d: N * C_i * H_i * W_i * esz[d] for d in esz}
     win_b = {d: N * C_i * H_o * W_i * H_f * esz[d] for d in esz}
     out_b = {d: N * C_o * H_o * W_o * esz[d] for d in esz}
     w_b = {d: C_o * C_i * H_f * W_f * esz[d] for d in esz}
     col_b = {d: N * C_i * H_f * W_f * H_o * W_o * esz[d] for d in esz}
     kernels = {}
-    for i, name in enumerate(names):
+    for i, (name, d, kind, _, extra) in enumerate(ops):
         t_s = kern_ms[i] * 1e-3
-        d = "f32" if name.endswith("f32") or name.startswith("conv_f32") else "f16"
-        if name.startswith("transform"):
+        if kind == "transform":
             byts = x_b[d] + win_b[d]
             kernels[name] = {"ms": kern_ms[i], "bound": "hbm", "achieved": byts / t_s / 1e9,
                              "peak": pk["hbm_gbs"], "unit": "GB/s", "alg_bytes": byts}
-        elif name == "conv_f32_window":
+        elif d == "f32":
             kernels[name] = {"ms": kern_ms[i], "bound": "alu", "achieved": f / t_s / 1e12,
                              "peak": fp32_peak, "unit": "TFLOP/s", "flops": f}
         else:
-            byts = (win_b[d] if "window" in name else x_b[d]) + w_b[d] + out_b[d]
+            byts = (win_b[d] if kind == "window" else x_b[d]) + w_b[d] + out_b[d]
             tc_peak = pk["bf16_tflops"]
             hbm_cap = f / byts * pk["hbm_gbs"] * 1e9 / 1e12
             bound = "tensor" if tc_peak < hbm_cap else "hbm"
@@ -350,17 +360,25 @@ def main():
                              "peak": min(tc_peak, hbm_cap), "unit": "TFLOP/s", "flops": f,
                              "alg_bytes": byts, "tensor_peak_frac": f / t_s / 1e12 / tc_peak}
         kernels[name]["frac"] = kernels[name]["achieved"] / kernels[name]["peak"]
+        if "ws_bytes" in extra:
+            kernels[name]["workspace_bytes"] = extra["ws_bytes"]
+    workspace = {}
+    for d in layer.dtypes:
+        ws_conv = kernels[f"{'conv_f32' if d == 'f32' else 'conv_tc'}_window_{d}"]["workspace_bytes"]
+        workspace[f"two_step_{d}"] = win_b[d] + ws_conv
+        if d != "f32":
+            workspace[f"fused_{d}"] = kernels[f"conv_tc_fused_{d}"]["workspace_bytes"]
+        workspace[f"im2col_{d}"] = col_b[d]
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     dk = kernels[dom]
     traffic = DRAM_TRAFFIC.get(dom)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16+f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "+".join(layer.dtypes), "data": "synthetic",
         "config": {"workload": f"{layer.name}: N={N}, C_i={C_i}, {H_i}x{W_i}, C_o={C_o}, "
-                               f"{H_f}x{W_f}, stride {s_h}; fp16 and fp32",
-                   "step": "transform f16, tc conv from window f16, fused tc conv f16, "
-                           "transform f32, fp32 conv from window",
+                               f"{H_f}x{W_f}, stride {s_h}x{s_w}; {' and '.join(layer.dtypes)}",
+                   "step": ", ".join(names),
                    "parallelism": f"replicas x{world}", "l2": "flushed between steps (512 MB write)"},
         "roofline": {"kernel": dom, "bound": dk["bound"], "achieved": dk["achieved"],
                      "peak": dk["peak"], "unit": dk["unit"], "frac": dk["frac"],
@@ -368,10 +386,7 @@ def main():
                      "peak_source": "fp32 FFMA: 152 SMs x 128 lanes x 2 x max SM clock"
                      if dk["bound"] == "alu" else pk["source"]},
         "kernels": kernels,
-        "workspace_bytes": {
-            "two_step_f16": win_b["f16"] + ws16.numel(), "fused_f16": ws16f.numel(),
-            "im2col_f16": col_b["f16"], "two_step_f32": win_b["f32"] + ws32.numel(),
-            "im2col_f32": col_b["f32"]},
+        "workspace_bytes": workspace,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,

@@ -15,6 +15,10 @@ SMALL = [  # N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w
     (1, 3, 32, 32, 8, 3, 3, 1, 1), (2, 3, 47, 45, 96, 11, 11, 4, 4), (2, 5, 30, 33, 37, 3, 7, 1, 2),
     (3, 17, 12, 14, 130, 1, 1, 1, 1), (1, 64, 20, 21, 64, 7, 7, 2, 2), (2, 2, 9, 9, 5, 9, 9, 1, 1),
     (1, 1, 50, 3, 1, 2, 3, 3, 1), (2, 96, 24, 24, 256, 5, 5, 1, 1), (1, 16, 40, 40, 200, 3, 3, 1, 1),
+    # many input channels: the fused call takes the tap kernel (vector and scalar slab fills,
+    # one or two MMA halves, several row tiles, strides 1-3, channel counts not a multiple of 16)
+    (2, 32, 30, 64, 128, 3, 5, 3, 2), (1, 48, 60, 56, 64, 11, 11, 1, 1), (2, 128, 30, 56, 128, 3, 3, 1, 1),
+    (1, 24, 100, 16, 40, 2, 2, 2, 2), (2, 40, 33, 35, 136, 4, 3, 2, 1), (1, 64, 9, 600, 16, 3, 3, 1, 2),
 ]
 
 
