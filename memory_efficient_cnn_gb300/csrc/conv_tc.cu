@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) conv_tc_expand_kernel(const __gri
         for (int it = 0; it < p.kstages; ++it) {
             const int s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1;
-            if (!bar_wait(empty(s), ph ^ 1, ctl, SITE_EMPTY_PROD)) break;
+            if (!warp_bar_wait(empty(s), ph ^ 1, ctl, SITE_EMPTY_PROD)) break;
             uint8_t *dstB = sB + s * B_BYTES + row_off;
 #pragma unroll 2
             for (int c = 0; c < KS / 8; ++c) {
@@ -215,14 +215,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) conv_tc_expand_kernel(const __gri
             mbar_arrive(full_b(s));
         }
 
-        // ---------------- epilogue: TMEM -> registers -> smem -> coalesced stores
-        const bool ok = bar_wait(done, 0, ctl, SITE_DONE);
+        // ---------------- epilogue: TMEM -> registers -> smem transpose -> coalesced stores
+        const bool ok = warp_bar_wait(done, 0, ctl, SITE_DONE);
         tc_fence_after();
         if (ok) {
             const int q = warp & 3;              // TMEM lane quarter this warp may read
             const int hh = (warp - 2) >> 2;      // which half of the columns
             uint32_t *stage = reinterpret_cast<uint32_t *>(sB) + (warp - 2) * (32 * 17);
-            const int co_base = mt * BM + q * 32;
+            const uint16_t *st16 = reinterpret_cast<const uint16_t *>(stage);
+            const int co0 = mt * BM + q * 32;
+            const int rows = min(32, p.C_o - co0);
+            uint16_t *out_c = p.out + ((int64_t)n * p.C_o + co0) * p.P;
             for (int blk = 0; blk < NT / 64; ++blk) {
                 const int col = hh * (NT / 2) + blk * 32;
                 uint32_t r[32];
@@ -233,11 +236,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) conv_tc_expand_kernel(const __gri
                     stage[lane * 17 + i] = pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), p.bf16);
                 __syncwarp();
                 const int pidx = pos0 + col + lane;
-                const uint16_t *st16 = reinterpret_cast<const uint16_t *>(stage);
-                for (int row = 0; row < 32; ++row) {
-                    const int co = co_base + row;
-                    if (co < p.C_o && pidx < p.P)
-                        p.out[((int64_t)n * p.C_o + co) * p.P + pidx] = st16[row * 34 + lane];
+                if (pidx < p.P) {
+                    uint16_t *dst = out_c + pidx;
+                    for (int row = 0; row < rows; ++row, dst += p.P) *dst = st16[row * 34 + lane];
                 }
                 __syncwarp();
             }
@@ -284,54 +285,106 @@ __global__ void relayout_filter_expand(const uint16_t *__restrict__ filt, uint16
 }
 
 // =========================================================================
-// Tap kernel (fused path, many input channels).
+// Tap kernels: every K step is a plain descriptor offset into a staged slab,
+// so shared memory holds each staged element once (no im2col expansion).
 //
-// The CTA owns Q whole output rows of one image and 128 output channels.
-// Shared memory holds, per 16-channel chunk, the unique input elements under
-// those rows (the (Q-1)*s_h + H_f input rows, every column) with the 16
-// channels innermost, split into s_h x s_w polyphase blocks:
-//   slab[c8][row % s_h][col % s_w][row / s_h][col / s_w][8 channels]  (16 B per entry)
-// Output pixel (q, w') of the tile is "position" p = q*Wh + w' (Wh = ceil(W_i/s_w)),
-// and for filter tap (r, j) the 16 B entries of consecutive positions are
-// consecutive in the slab. So the B operand of tap (r, j) is the slab seen
-// from a constant offset -- a plain K-major descriptor (8-row groups 128 B
-// apart, the two 8-channel halves one plane apart) -- and no element is ever
-// duplicated: each tap is one tcgen05.mma (M=128 channels, N<=256 positions,
-// K=16 input channels) per half of the tile. Positions with w' >= W_o are
-// computed and discarded. The filter arrives per (chunk, group of taps) by
-// bulk copy, pre-laid by a re-layout kernel as [tap][co-group][8-ch half][8 co][8 ch].
+// TAP_CH (fused, many input channels). The CTA owns Q whole output rows of one
+// image and 128 output channels. Per 16-channel chunk the slab holds the
+// unique input elements under those rows with the channels innermost, split
+// into s_h x s_w polyphase blocks:
+//   slab[c8][row % s_h][col % s_w][row / s_h][col / s_w][8 channels]   (16 B entries)
+// Output pixel (q, w') is position p = q*pitch + w' (pitch = ceil(W_i/s_w));
+// for filter tap (r, j) consecutive positions are consecutive slab entries, so
+// the tap's B operand is the slab seen from a constant offset (K = the 16
+// channels, the two 8-channel halves one plane apart).
+//
+// TAP_WX / TAP_WW (few input channels; fused from x / from the window tensor).
+// The slab holds the im2win window rows of one channel under the tile's
+// output rows, re-laid so that K runs along the window: with S = s_w*H_f the
+// window row win[m*S + b] (b < S, m = column group) is stored as
+//   slab[b / 8][q][m][b % 8]                                             (16 B entries)
+// Output pixel (q, wo) uses window elements (wo + a)*S + b for a < ceil(W_f/s_w),
+// so tap a, K group u is again a constant offset (a entries along m, 2u chunks
+// along b): the contiguous-window property of im2win becomes a descriptor stride.
+//
+// In every mode one tcgen05.mma (M = 128 output channels, N <= 256 positions,
+// K = 16) is issued per tap and half tile; positions whose column is >= W_o are
+// computed and discarded. Filter tiles arrive per (chunk, group of taps) by
+// bulk copy, pre-laid by a re-layout kernel as [tap][co group][K half][8 co][8 K].
 // =========================================================================
+enum TapMode { TAP_CH = 0, TAP_WX = 1, TAP_WW = 2 };
+
 constexpr int TAP_PROD_WARPS = 8;
 constexpr int TAP_THREADS = (2 + TAP_PROD_WARPS) * 32;
-constexpr uint32_t TAP_A_BYTES = BM * 16 * 2;  // one tap of one 16-channel chunk: 4 KB
+constexpr uint32_t TAP_A_BYTES = BM * 16 * 2;  // one K=16 tap of 128 channels: 4 KB
 constexpr int TAP_MAX_NT = 512;
 
 struct TapParams {
-    const uint16_t *x;
+    const uint16_t *src;   // NCHW input (CH, WX) or window tensor (WW)
     const uint16_t *fa;
     uint16_t *out;
     uint32_t *status;
     int C_i, C_o, H_i, W_i, H_o, W_o, H_f, W_f, s_h, s_w;
-    int C16;               // 16-channel chunks
-    int T;                 // taps H_f*W_f
+    int NCH;               // chunks: 16-channel groups (CH) or channels (WX, WW)
+    int T;                 // K=16 taps per chunk
     int TG, ntg;           // taps per filter stage, filter stages per chunk
     int Q, tiles_h;        // output rows per tile, tiles per image
-    int Wh, HH, RR;        // positions per row, phase rows, input rows per tile
+    int pitch;             // positions per output row of the tile
+    int RR;                // CH: input rows per tile
     int NT, NTp, N0, N1;   // positions, padded, MMA N of the two halves
-    uint32_t PB, CH;       // bytes of a phase block, of an 8-channel plane
+    uint32_t lbo;          // CH: bytes of an 8-channel plane; W*: bytes of a K chunk
+    uint32_t PB;           // CH: bytes of a phase block
+    int U, S, A;           // W*: K=16 groups per window step, window step s_w*H_f, taps along m
+    int64_t L;             // WW: window row length W_i*H_f
+    int64_t win_elems;     // WW: elements of the window tensor
     uint32_t stage_b;      // bytes of one slab stage
     int BST, AST;          // slab stages, filter stages
     uint32_t tmem_cols;
-    int vec;               // 1: rows are 16 B aligned and W_i % 8 == 0 (vector loads)
+    int vec;               // CH: 16-byte row loads possible
     uint32_t idesc0, idesc1;
     int bf16;
 };
 
-__device__ __forceinline__ uint32_t tap_off(const TapParams &p, int r, int j) {
-    return (uint32_t)((((r % p.s_h) * p.s_w + (j % p.s_w)) * p.PB) +
-                      (((r / p.s_h) * p.Wh + (j / p.s_w)) * 16));
+template <int MODE>
+__device__ __forceinline__ uint32_t tap_offset(const TapParams &p, int t) {
+    if (MODE == TAP_CH) {
+        const int r = t / p.W_f, j = t - r * p.W_f;
+        return (uint32_t)((((r % p.s_h) * p.s_w + (j % p.s_w)) * p.PB) +
+                          (((r / p.s_h) * p.pitch + (j / p.s_w)) * 16));
+    } else {
+        const int a = t / p.U, u = t - a * p.U;
+        return (uint32_t)(2 * u) * p.lbo + (uint32_t)a * 16u;
+    }
 }
 
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// 8 consecutive 16-bit elements starting at element o of `base` (2-byte aligned),
+// from the two aligned 16-byte vectors that cover them.
+__device__ __forceinline__ uint4 load8_unaligned(const uint16_t *base, int64_t o) {
+    const int64_t vi = o >> 3;
+    const uint4 v0 = __ldg(reinterpret_cast<const uint4 *>(base) + vi);
+    const uint4 v1 = __ldg(reinterpret_cast<const uint4 *>(base) + vi + 1);
+    const int sh = (int)(o & 7);           // element shift 0..7
+    const int q = sh >> 1;                 // word shift 0..3
+    uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t u[5];
+#pragma unroll
+    for (int m = 0; m < 5; ++m) {
+        uint32_t t = w[m];
+        t = (q == 1) ? w[m + 1] : t;
+        t = (q == 2) ? w[m + 2] : t;
+        t = (q == 3) ? w[(m + 3) & 7] : t;
+        u[m] = t;
+    }
+    const uint32_t sel = (sh & 1) ? 0x5432u : 0x3210u;
+    return make_uint4(__byte_perm(u[0], u[1], sel), __byte_perm(u[1], u[2], sel),
+                      __byte_perm(u[2], u[3], sel), __byte_perm(u[3], u[4], sel));
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __grid_constant__ TapParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t a_stage = (uint32_t)p.TG * TAP_A_BYTES;
@@ -341,8 +394,10 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     // bars: full_a[AST] | empty_a[AST] | full_b[BST] | empty_b[BST] | done | drain
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * p.AST + 2 * p.BST + 2);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
+    uint32_t *toff = reinterpret_cast<uint32_t *>(bars + 2 * p.AST + 2 * p.BST + 4);  // [T] tap offsets
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = threadIdx.x; t < p.T; t += blockDim.x) toff[t] = tap_offset<MODE>(p, t);
     const int n = blockIdx.x / p.tiles_h;
     const int th = blockIdx.x - n * p.tiles_h;
     const int mt = blockIdx.y;
@@ -384,7 +439,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         if (lane == 0) {
             bool ok = true;
             int a_it = 0;
-            for (int cc = 0; cc < p.C16 && ok; ++cc) {
+            const uint64_t adesc0 = smem_desc(0, 128, 256), bdesc0 = smem_desc(0, p.lbo, 128);
+            for (int cc = 0; cc < p.NCH && ok; ++cc) {
                 const int sb = cc % p.BST;
                 if (!(ok = bar_wait(full_b(sb), (cc / p.BST) & 1, ctl, SITE_FULL_B))) break;
                 const uint32_t slab = smem_u32(sB + (size_t)sb * p.stage_b);
@@ -392,16 +448,14 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     const int sa = a_it % p.AST;
                     if (!(ok = bar_wait(full_a(sa), (a_it / p.AST) & 1, ctl, SITE_FULL_A))) break;
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + (size_t)sa * a_stage);
-                    const int t_end = min(p.T, (tg + 1) * p.TG);
-                    for (int t = tg * p.TG; t < t_end; ++t) {
-                        const int r = t / p.W_f, j = t - r * p.W_f;
-                        const uint64_t ad = smem_desc(a0 + (uint32_t)(t - tg * p.TG) * TAP_A_BYTES, 128, 256);
-                        const uint32_t bo = slab + tap_off(p, r, j);
+                    const int t0 = tg * p.TG;
+                    const int t_end = min(p.T, t0 + p.TG);
+                    uint64_t ad = adesc0 + ((uint64_t)((smem_u32(sA + (size_t)sa * a_stage) & 0x3FFFFu) >> 4));
+                    for (int t = t0; t < t_end; ++t, ad += TAP_A_BYTES >> 4) {
+                        const uint64_t bd = bdesc0 + (uint64_t)(((slab + toff[t]) & 0x3FFFFu) >> 4);
                         const uint32_t acc = (cc | t) != 0;
-                        mma_f16(tmem, ad, smem_desc(bo, p.CH, 128), p.idesc0, acc);
-                        if (p.N1 > 0)
-                            mma_f16(tmem + 256, ad, smem_desc(bo + 256 * 16, p.CH, 128), p.idesc1, acc);
+                        mma_f16(tmem, ad, bd, p.idesc0, acc);
+                        if (p.N1 > 0) mma_f16(tmem + 256, ad, bd + ((256 * 16) >> 4), p.idesc1, acc);
                     }
                     mma_commit(empty_a(sa));
                 }
@@ -416,7 +470,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         if (lane == 0) {
             int issued = 0;
             bool ok = true;
-            for (int cc = 0; cc < p.C16 && ok; ++cc) {
+            for (int cc = 0; cc < p.NCH && ok; ++cc) {
                 for (int tg = 0; tg < p.ntg; ++tg) {
                     const int sa = issued % p.AST;
                     if (!(ok = bar_wait(empty_a(sa), ((issued / p.AST) & 1) ^ 1, ctl, SITE_EMPTY_LOAD)))
@@ -424,7 +478,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     const int t0 = tg * p.TG;
                     const uint32_t bytes = (uint32_t)(min(p.T, t0 + p.TG) - t0) * TAP_A_BYTES;
                     const uint16_t *src =
-                        p.fa + (((int64_t)mt * p.C16 + cc) * p.T + t0) * (TAP_A_BYTES / 2);
+                        p.fa + (((int64_t)mt * p.NCH + cc) * p.T + t0) * (TAP_A_BYTES / 2);
                     mbar_arrive_expect_tx(full_a(sa), bytes);
                     bulk_g2s(smem_u32(sA + (size_t)sa * a_stage), src, bytes, full_a(sa));
                     ++issued;
@@ -437,102 +491,161 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         }
         __syncwarp();
     } else {
-        // ---------------- slab producers: NCHW -> [c8][phase][row][col][8 ch]
+        // ---------------- slab producers
         const int pt = threadIdx.x - 64;
-        const int R0 = ho0 * p.s_h;
-        const int rows = min(p.RR, p.H_i - R0);
-        const uint16_t *__restrict__ xn = p.x + (int64_t)n * p.C_i * p.H_i * p.W_i;
-        const int64_t plane = (int64_t)p.H_i * p.W_i;
-        for (int cc = 0; cc < p.C16; ++cc) {
+        constexpr int NPT = TAP_PROD_WARPS * 32;
+        for (int cc = 0; cc < p.NCH; ++cc) {
             const int sb = cc % p.BST;
-            if (!bar_wait(empty_b(sb), ((cc / p.BST) & 1) ^ 1, ctl, SITE_EMPTY_PROD)) break;
+            if (!warp_bar_wait(empty_b(sb), ((cc / p.BST) & 1) ^ 1, ctl, SITE_EMPTY_PROD)) break;
             uint8_t *slab = sB + (size_t)sb * p.stage_b;
-            if (p.vec) {
-                // 8 channels x 8 columns per item: 8 16-byte loads, 8x8 transpose, 8 16-byte stores
-                const int cgs = p.W_i / 8;
-                const int items = 2 * rows * cgs;
-                for (int it = pt; it < items; it += TAP_PROD_WARPS * 32) {
-                    const int cg = it % cgs;
-                    const int t2 = it / cgs;
-                    const int lr = t2 % rows;
-                    const int c8 = t2 / rows;
-                    const int ci0 = cc * 16 + c8 * 8;
-                    uint4 v[8];
-                    const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)(R0 + lr) * p.W_i + cg * 8;
+            if (MODE == TAP_CH) {
+                const int R0 = ho0 * p.s_h;
+                const int rows = min(p.RR, p.H_i - R0);
+                const int64_t plane = (int64_t)p.H_i * p.W_i;
+                const uint16_t *__restrict__ xn = p.src + (int64_t)n * p.C_i * plane;
+                if (p.vec) {
+                    // 8 channels x 8 columns per item: 8 16-byte loads, 8x8 transpose, 8 16-byte stores
+                    const int cgs = p.W_i / 8;
+                    const int items = 2 * rows * cgs;
+                    for (int it = pt; it < items; it += NPT) {
+                        const int cg = it % cgs;
+                        const int t2 = it / cgs;
+                        const int lr = t2 % rows;
+                        const int c8 = t2 / rows;
+                        const int ci0 = cc * 16 + c8 * 8;
+                        uint4 v[8];
+                        const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)(R0 + lr) * p.W_i + cg * 8;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        v[e] = (ci0 + e < p.C_i) ? __ldg(reinterpret_cast<const uint4 *>(src + e * plane))
-                                                 : make_uint4(0, 0, 0, 0);
-                    uint8_t *rowp = slab + (size_t)c8 * p.CH + (size_t)((lr % p.s_h) * p.s_w) * p.PB +
-                                    (size_t)((lr / p.s_h) * p.Wh) * 16;
+                        for (int e = 0; e < 8; ++e)
+                            v[e] = (ci0 + e < p.C_i) ? __ldg(reinterpret_cast<const uint4 *>(src + e * plane))
+                                                     : make_uint4(0, 0, 0, 0);
+                        uint8_t *rowp = slab + (size_t)c8 * p.lbo + (size_t)((lr % p.s_h) * p.s_w) * p.PB +
+                                        (size_t)((lr / p.s_h) * p.pitch) * 16;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int col = cg * 8 + k;
-                        const uint32_t sel = (k & 1) ? 0x7632u : 0x5410u;
-                        uint32_t w0, w1, w2, w3;
-                        const int wd = k >> 1;
-#define IM2WIN_WORD(vv, i) ((i) == 0 ? (vv).x : (i) == 1 ? (vv).y : (i) == 2 ? (vv).z : (vv).w)
-                        w0 = __byte_perm(IM2WIN_WORD(v[0], wd), IM2WIN_WORD(v[1], wd), sel);
-                        w1 = __byte_perm(IM2WIN_WORD(v[2], wd), IM2WIN_WORD(v[3], wd), sel);
-                        w2 = __byte_perm(IM2WIN_WORD(v[4], wd), IM2WIN_WORD(v[5], wd), sel);
-                        w3 = __byte_perm(IM2WIN_WORD(v[6], wd), IM2WIN_WORD(v[7], wd), sel);
-#undef IM2WIN_WORD
-                        uint8_t *dst = rowp + (size_t)(col % p.s_w) * p.PB + (size_t)(col / p.s_w) * 16;
-                        *reinterpret_cast<uint4 *>(dst) = make_uint4(w0, w1, w2, w3);
+                        for (int k = 0; k < 8; ++k) {
+                            const int col = cg * 8 + k;
+                            const uint32_t sel = (k & 1) ? 0x7632u : 0x5410u;
+                            const int wd = k >> 1;
+                            const uint32_t w0 = __byte_perm(word_of(v[0], wd), word_of(v[1], wd), sel);
+                            const uint32_t w1 = __byte_perm(word_of(v[2], wd), word_of(v[3], wd), sel);
+                            const uint32_t w2 = __byte_perm(word_of(v[4], wd), word_of(v[5], wd), sel);
+                            const uint32_t w3 = __byte_perm(word_of(v[6], wd), word_of(v[7], wd), sel);
+                            uint8_t *dst = rowp + (size_t)(col % p.s_w) * p.PB + (size_t)(col / p.s_w) * 16;
+                            *reinterpret_cast<uint4 *>(dst) = make_uint4(w0, w1, w2, w3);
+                        }
+                    }
+                } else {
+                    // one column of 8 channels per item
+                    const int items = 2 * rows * p.W_i;
+                    for (int it = pt; it < items; it += NPT) {
+                        const int col = it % p.W_i;
+                        const int t2 = it / p.W_i;
+                        const int lr = t2 % rows;
+                        const int c8 = t2 / rows;
+                        const int ci0 = cc * 16 + c8 * 8;
+                        const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)(R0 + lr) * p.W_i + col;
+                        uint32_t e16[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            e16[e] = (ci0 + e < p.C_i) ? (uint32_t)__ldg(src + e * plane) : 0u;
+                        uint8_t *dst = slab + (size_t)c8 * p.lbo +
+                                       (size_t)((lr % p.s_h) * p.s_w + col % p.s_w) * p.PB +
+                                       (size_t)((lr / p.s_h) * p.pitch + col / p.s_w) * 16;
+                        *reinterpret_cast<uint4 *>(dst) =
+                            make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
+                                       e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
                     }
                 }
-            } else {
-                // one column of 8 channels per item
-                const int items = 2 * rows * p.W_i;
-                for (int it = pt; it < items; it += TAP_PROD_WARPS * 32) {
-                    const int col = it % p.W_i;
-                    const int t2 = it / p.W_i;
-                    const int lr = t2 % rows;
-                    const int c8 = t2 / rows;
-                    const int ci0 = cc * 16 + c8 * 8;
-                    const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)(R0 + lr) * p.W_i + col;
+            } else if (MODE == TAP_WX) {
+                // window rows of channel cc built straight from x:
+                // entry (c, q, m)[e] = x[cc][(ho0+q)*s_h + r][m*s_w + jl] for b = 8c + e = jl*H_f + r
+                const int SC = 2 * p.U;
+                const int items = SC * p.Q * p.pitch;
+                const uint16_t *__restrict__ xc = p.src + ((int64_t)n * p.C_i + cc) * p.H_i * p.W_i;
+                for (int it = pt; it < items; it += NPT) {
+                    const int m = it % p.pitch;
+                    const int t2 = it / p.pitch;
+                    const int q = t2 % p.Q;
+                    const int c = t2 / p.Q;
                     uint32_t e16[8];
+                    const int b0 = 8 * c;
+                    int jl = b0 / p.H_f;
+                    int r = b0 - jl * p.H_f;
+                    const bool rowv = ho0 + q < p.H_o;
+                    const int rbase = (ho0 + q) * p.s_h;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) e16[e] = (ci0 + e < p.C_i) ? (uint32_t)__ldg(src + e * plane) : 0u;
-                    uint8_t *dst = slab + (size_t)c8 * p.CH +
-                                   (size_t)((lr % p.s_h) * p.s_w + col % p.s_w) * p.PB +
-                                   (size_t)((lr / p.s_h) * p.Wh + col / p.s_w) * 16;
-                    *reinterpret_cast<uint4 *>(dst) = make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
-                                                                 e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
+                    for (int e = 0; e < 8; ++e) {
+                        const int col = m * p.s_w + jl;
+                        const bool v = rowv && (b0 + e < p.S) && col < p.W_i;
+                        e16[e] = v ? (uint32_t)__ldg(xc + (int64_t)(rbase + r) * p.W_i + col) : 0u;
+                        if (++r == p.H_f) { r = 0; ++jl; }
+                    }
+                    *reinterpret_cast<uint4 *>(slab + (size_t)c * p.lbo + (size_t)(q * p.pitch + m) * 16) =
+                        make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
+                                   e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
+                }
+            } else {
+                // window rows of channel cc read from the window tensor:
+                // entry (c, q, m) = win[n][cc][ho0+q][m*S + 8c .. +8]
+                const int SC = 2 * p.U;
+                const int items = SC * p.Q * p.pitch;
+                const int64_t base_nc = ((int64_t)n * p.C_i + cc) * p.H_o;
+                for (int it = pt; it < items; it += NPT) {
+                    const int c = it % SC;
+                    const int t2 = it / SC;
+                    const int m = t2 % p.pitch;
+                    const int q = t2 / p.pitch;
+                    uint4 val = make_uint4(0, 0, 0, 0);
+                    if (ho0 + q < p.H_o) {
+                        const int64_t wo0 = (int64_t)m * p.S + 8 * c;   // within the window row
+                        const int64_t o = (base_nc + ho0 + q) * p.L + wo0;
+                        const int valid = (int)min((int64_t)min(8, p.S - 8 * c), p.L - wo0);
+                        if (valid == 8 && ((o >> 3) + 2) * 8 <= p.win_elems) {
+                            val = load8_unaligned(p.src, o);
+                        } else if (valid > 0) {
+                            uint32_t e16[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) e16[e] = (e < valid) ? (uint32_t)__ldg(p.src + o + e) : 0u;
+                            val = make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
+                                             e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>(slab + (size_t)c * p.lbo + (size_t)(q * p.pitch + m) * 16) = val;
                 }
             }
             fence_async_smem();
             mbar_arrive(full_b(sb));
         }
 
-        // ---------------- epilogue
-        const bool ok = bar_wait(done, 0, ctl, SITE_DONE);
+        // ---------------- epilogue: TMEM -> registers -> smem transpose -> coalesced stores
+        const bool ok = warp_bar_wait(done, 0, ctl, SITE_DONE);
         tc_fence_after();
         if (ok) {
-            const int q = warp & 3;
+            const int q4 = warp & 3;
             const int hh = (warp - 2) >> 2;
             uint32_t *stage = reinterpret_cast<uint32_t *>(sB) + (warp - 2) * (32 * 17);
-            const int co_base = mt * BM + q * 32;
+            const uint16_t *st16 = reinterpret_cast<const uint16_t *>(stage);
+            const int co0 = mt * BM + q4 * 32;
+            const int rows = min(32, p.C_o - co0);
+            const int64_t plane = (int64_t)p.H_o * p.W_o;
+            uint16_t *out_c = p.out + ((int64_t)n * p.C_o + co0) * plane;
             const int nblk = (p.NTp + 31) / 32;
             for (int blk = hh; blk < nblk; blk += 2) {
                 const int col = blk * 32;
                 uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)col, r);
+                tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)col, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     stage[lane * 17 + i] = pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), p.bf16);
                 __syncwarp();
                 const int pp = col + lane;
-                const int qrow = pp / p.Wh;
-                const int wo = pp - qrow * p.Wh;
+                const int qrow = pp / p.pitch;
+                const int wo = pp - qrow * p.pitch;
                 const int ho = ho0 + qrow;
-                const bool pv = pp < p.NT && wo < p.W_o && ho < p.H_o;
-                const uint16_t *st16 = reinterpret_cast<const uint16_t *>(stage);
-                for (int row = 0; row < 32; ++row) {
-                    const int co = co_base + row;
-                    if (pv && co < p.C_o)
-                        p.out[(((int64_t)n * p.C_o + co) * p.H_o + ho) * p.W_o + wo] = st16[row * 34 + lane];
+                if (pp < p.NT && wo < p.W_o && ho < p.H_o) {
+                    uint16_t *dst = out_c + (int64_t)ho * p.W_o + wo;
+                    for (int row = 0; row < rows; ++row, dst += plane) *dst = st16[row * 34 + lane];
                 }
                 __syncwarp();
             }
@@ -547,11 +660,14 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     }
 }
 
-// Filter tiles for the tap kernel: fa[mt][cc][t][g][c][row][e] holds
-// filt[mt*128 + g*8 + row][cc*16 + c*8 + e][r][j] for tap t = r*W_f + j
-// (zero outside the filter). Block 0 also clears the status word.
+// Filter tiles of the tap kernels: fa[mt][cc][t][g][h][row][e] (h = K half)
+// holds, for output channel mt*128 + g*8 + row and K index k = h*8 + e of tap t:
+//   TAP_CH: filt[co][cc*16 + k][r][j] with t = r*W_f + j;
+//   TAP_W*: filt[co][cc][r][a*s_w + jl] with t = a*U + u, b = 16u + k = jl*H_f + r (b < S);
+// zero outside the filter. Block 0 also clears the status word.
 __global__ void relayout_filter_tap(const uint16_t *__restrict__ filt, uint16_t *__restrict__ fa,
-                                    uint32_t *status, int64_t total, int C_i, int C_o, int T, int C16) {
+                                    uint32_t *status, int64_t total, int mode, int C_i, int C_o,
+                                    int H_f, int W_f, int s_w, int T, int NCH, int U, int S) {
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         status[0] = 0;
         status[1] = 0;
@@ -559,60 +675,96 @@ __global__ void relayout_filter_tap(const uint16_t *__restrict__ filt, uint16_t 
     }
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        const int e = (int)(idx & 7), rw = (int)((idx >> 3) & 7), c = (int)((idx >> 6) & 1),
+        const int e = (int)(idx & 7), rw = (int)((idx >> 3) & 7), h = (int)((idx >> 6) & 1),
                   g = (int)((idx >> 7) & 15);
         const int64_t rest = idx >> 11;
         const int t = (int)(rest % T);
         const int64_t rest2 = rest / T;
-        const int cc = (int)(rest2 % C16);
-        const int mt = (int)(rest2 / C16);
+        const int cc = (int)(rest2 % NCH);
+        const int mt = (int)(rest2 / NCH);
         const int co = mt * BM + g * 8 + rw;
-        const int ci = cc * 16 + c * 8 + e;
+        const int k = h * 8 + e;
         uint16_t v = 0;
-        if (co < C_o && ci < C_i) v = filt[((int64_t)co * C_i + ci) * T + t];
+        if (co < C_o) {
+            if (mode == TAP_CH) {
+                const int ci = cc * 16 + k;
+                if (ci < C_i) v = filt[((int64_t)co * C_i + ci) * H_f * W_f + t];
+            } else {
+                const int a = t / U, u = t - a * U;
+                const int b = 16 * u + k;
+                if (b < S) {
+                    const int jl = b / H_f, r = b - jl * H_f;
+                    const int j = a * s_w + jl;
+                    if (j < W_f) v = filt[(((int64_t)co * C_i + cc) * H_f + r) * W_f + j];
+                }
+            }
+        }
         fa[idx] = v;
     }
 }
 
 struct TapPlan {
     bool ok;
+    int mode;
     TapParams p;
     size_t smem;
     int mtiles;
+    int64_t kslots;        // MMA K values per output pixel (cost model)
 };
 
-// Choose the tap kernel's tiling for a shape, or report that it does not fit.
-TapPlan plan_tap(const Shape &s) {
+// Tiling of a tap kernel for a shape (mode TAP_CH / TAP_WX / TAP_WW), or !ok.
+TapPlan plan_tap(const Shape &s, int mode) {
     TapPlan pl{};
     pl.ok = false;
-    if (s.C_i < 16) return pl;
-    const int64_t Wh = (s.W_i + s.s_w - 1) / s.s_w;
-    if (Wh > TAP_MAX_NT || s.C_i * s.H_i * s.W_i >= (1ll << 31)) return pl;
-    const int T = (int)(s.H_f * s.W_f);
+    pl.mode = mode;
     const int64_t smem_max = 227 * 1024 - 1024;
-    for (int64_t Qmax = std::min<int64_t>(s.H_o, TAP_MAX_NT / Wh); Qmax >= 1; --Qmax) {
+    if (s.C_i * s.H_i * s.W_i >= (1ll << 31)) return pl;
+    int64_t pitch, T, U = 0, S = 0, A = 0, NCH;
+    if (mode == TAP_CH) {
+        pitch = (s.W_i + s.s_w - 1) / s.s_w;
+        T = s.H_f * s.W_f;
+        NCH = (s.C_i + 15) / 16;
+    } else {
+        S = s.s_w * s.H_f;
+        U = (S + 15) / 16;
+        A = (s.W_f + s.s_w - 1) / s.s_w;
+        pitch = std::max<int64_t>((s.W_i + s.s_w - 1) / s.s_w, s.W_o + A - 1);
+        T = A * U;
+        NCH = s.C_i;
+        if (mode == TAP_WW && s.N * s.C_i * s.H_o * s.W_i * s.H_f >= (1ll << 40)) return pl;
+    }
+    if (pitch > TAP_MAX_NT) return pl;
+    for (int64_t Qmax = std::min<int64_t>(s.H_o, TAP_MAX_NT / pitch); Qmax >= 1; --Qmax) {
         const int64_t tiles = (s.H_o + Qmax - 1) / Qmax;
         const int64_t Q = (s.H_o + tiles - 1) / tiles;
-        const int64_t NT = Q * Wh;
+        const int64_t NT = Q * pitch;
         const int64_t NTp = (NT + 15) / 16 * 16;
-        const int64_t RR = (Q - 1) * s.s_h + s.H_f;
-        const int64_t HH = (RR + s.s_h - 1) / s.s_h;
-        const int64_t PB = HH * Wh * 16;
-        const int64_t CH = s.s_h * s.s_w * PB;
-        int64_t max_tap = 0;
-        for (int64_t r = 0; r < s.H_f; ++r)
-            for (int64_t j = 0; j < s.W_f; ++j)
-                max_tap = std::max(max_tap, ((r % s.s_h) * s.s_w + j % s.s_w) * PB +
-                                                ((r / s.s_h) * Wh + j / s.s_w) * 16);
-        // plane 1 is written up to 2*CH and read up to CH + max_tap + NTp*16
-        const int64_t stage_b = (std::max(2 * CH, CH + max_tap + NTp * 16) + 127) / 128 * 128;
-        if (stage_b < 8 * 32 * 17 * 4) continue;  // too small to stage the epilogue (never at these sizes)
+        int64_t RR = 0, PB = 0, lbo, stage_b;
+        if (mode == TAP_CH) {
+            RR = (Q - 1) * s.s_h + s.H_f;
+            const int64_t HH = (RR + s.s_h - 1) / s.s_h;
+            PB = HH * pitch * 16;
+            lbo = s.s_h * s.s_w * PB;
+            int64_t max_tap = 0;
+            for (int64_t r = 0; r < s.H_f; ++r)
+                for (int64_t j = 0; j < s.W_f; ++j)
+                    max_tap = std::max(max_tap, ((r % s.s_h) * s.s_w + j % s.s_w) * PB +
+                                                    ((r / s.s_h) * pitch + j / s.s_w) * 16);
+            // plane 1 is written up to 2*lbo and read up to lbo + max_tap + NTp*16
+            stage_b = std::max(2 * lbo, lbo + max_tap + NTp * 16);
+        } else {
+            lbo = Q * pitch * 16;
+            // chunks 0..2U-1 are written; tap (a, u) reads chunks 2u, 2u+1 from a*16
+            stage_b = std::max(2 * U * lbo, (2 * U - 1) * lbo + (A - 1 + NTp) * 16);
+        }
+        stage_b = (stage_b + 127) / 128 * 128;
+        if (stage_b < 8 * 32 * 17 * 4) stage_b = 8 * 32 * 17 * 4;  // epilogue staging reuses it
         for (int BST : {3, 2}) {
-            for (int TG : {8, 5, 4, 3, 2, 1}) {
+            for (int TG : {9, 8, 6, 5, 4, 3, 2, 1}) {
+                const int tg = (int)std::min<int64_t>(TG, T);
                 if (TG > T && TG != 1) continue;
-                const int tg = std::min(TG, T);
                 for (int AST : {4, 3, 2}) {
-                    int64_t total = (int64_t)AST * tg * TAP_A_BYTES + BST * stage_b + 256;
+                    int64_t total = (int64_t)AST * tg * TAP_A_BYTES + BST * stage_b + 256 + 4 * T;
                     if (total > smem_max) continue;
                     // a 512-column TMEM accumulator needs the SM to itself
                     if (NTp > 256) total = std::max<int64_t>(total, 120 * 1024);
@@ -620,27 +772,32 @@ TapPlan plan_tap(const Shape &s) {
                     p.C_i = (int)s.C_i; p.C_o = (int)s.C_o; p.H_i = (int)s.H_i; p.W_i = (int)s.W_i;
                     p.H_o = (int)s.H_o; p.W_o = (int)s.W_o; p.H_f = (int)s.H_f; p.W_f = (int)s.W_f;
                     p.s_h = (int)s.s_h; p.s_w = (int)s.s_w;
-                    p.C16 = (int)((s.C_i + 15) / 16);
-                    p.T = T;
+                    p.NCH = (int)NCH;
+                    p.T = (int)T;
                     p.TG = tg;
-                    p.ntg = (T + tg - 1) / tg;
+                    p.ntg = (int)((T + tg - 1) / tg);
                     p.Q = (int)Q;
                     p.tiles_h = (int)tiles;
-                    p.Wh = (int)Wh;
-                    p.HH = (int)HH;
+                    p.pitch = (int)pitch;
                     p.RR = (int)RR;
                     p.NT = (int)NT;
                     p.NTp = (int)NTp;
                     p.N0 = (int)std::min<int64_t>(256, NTp);
                     p.N1 = (int)(NTp - p.N0);
+                    p.lbo = (uint32_t)lbo;
                     p.PB = (uint32_t)PB;
-                    p.CH = (uint32_t)CH;
+                    p.U = (int)U;
+                    p.S = (int)S;
+                    p.A = (int)A;
+                    p.L = s.W_i * s.H_f;
+                    p.win_elems = s.N * s.C_i * s.H_o * s.W_i * s.H_f;
                     p.stage_b = (uint32_t)stage_b;
                     p.BST = BST;
                     p.AST = AST;
                     p.tmem_cols = NTp > 256 ? 512 : 256;
                     pl.smem = (size_t)total;
                     pl.mtiles = (int)((s.C_o + BM - 1) / BM);
+                    pl.kslots = NCH * T * 16;
                     pl.ok = tiles * s.N < (1ll << 31) && pl.mtiles < 65536;
                     return pl;
                 }
@@ -668,21 +825,32 @@ ExpandGeom expand_geom(const Shape &s) {
 
 }  // namespace
 
-// The fused path takes the tap kernel when its tiling fits, else the expand
-// kernel (which also serves the two-step path).
-static bool use_tap(const Shape &s, bool fused) { return fused && plan_tap(s).ok; }
+// Kernel choice. Fused: the tap kernel over channels or over window rows,
+// whichever needs fewer MMA K values per pixel; from the window tensor: the
+// window-row tap kernel. Either falls back to the expand kernel when its K
+// padding costs more than half again the expand kernel's K.
+static TapPlan choose_tap(const Shape &s, bool fused) {
+    const int64_t expand_k = s.C_i * ((s.H_f * s.W_f + 7) / 8 * 8);
+    TapPlan best{};
+    best.ok = false;
+    for (int mode : {TAP_CH, TAP_WX, TAP_WW}) {
+        if ((mode == TAP_WW) == fused) continue;
+        TapPlan pl = plan_tap(s, mode);
+        if (pl.ok && (!best.ok || pl.kslots < best.kslots)) best = pl;
+    }
+    if (best.ok && best.kslots * 2 > expand_k * 3) best.ok = false;
+    return best;
+}
 
 size_t conv_tc_filter_bytes(const Shape &s, bool fused) {
-    if (use_tap(s, fused)) {
-        const TapPlan pl = plan_tap(s);
-        return round_up((size_t)pl.mtiles * pl.p.C16 * pl.p.T * TAP_A_BYTES, 256);
-    }
+    const TapPlan pl = choose_tap(s, fused);
+    if (pl.ok) return round_up((size_t)pl.mtiles * pl.p.NCH * pl.p.T * TAP_A_BYTES, 256);
     const ExpandGeom g = expand_geom(s);
     return round_up((size_t)g.mtiles * BM * (size_t)g.K_pad * 2, 256);
 }
 
 bool conv_tc_supported(const Shape &s, bool fused) {
-    if (use_tap(s, fused)) return true;
+    if (choose_tap(s, fused).ok) return true;
     const int64_t img = fused ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * s.W_i * s.H_f;
     const int64_t KKP = (s.H_f * s.W_f + 7) / 8 * 8;
     const int64_t P = s.H_o * s.W_o;
@@ -691,35 +859,41 @@ bool conv_tc_supported(const Shape &s, bool fused) {
            pos_tiles * s.N < (1ll << 31) && (s.C_o + BM - 1) / BM < 65536;
 }
 
-static cudaError_t launch_tap(const void *x, const void *filt, void *out, void *ws, const Shape &s,
-                              bool bf16, cudaStream_t st) {
-    TapPlan pl = plan_tap(s);
+static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *filt, void *out,
+                              void *ws, const Shape &s, bool bf16, cudaStream_t st) {
     TapParams p = pl.p;
     uint32_t *status = static_cast<uint32_t *>(ws);
     uint16_t *fa = reinterpret_cast<uint16_t *>(static_cast<unsigned char *>(ws) + kStatusBytes);
-    const int64_t total = (int64_t)pl.mtiles * p.C16 * p.T * (TAP_A_BYTES / 2);
+    const int64_t total = (int64_t)pl.mtiles * p.NCH * p.T * (TAP_A_BYTES / 2);
     relayout_filter_tap<<<(unsigned)std::min<int64_t>((total + 255) / 256, 8192), 256, 0, st>>>(
-        static_cast<const uint16_t *>(filt), fa, status, total, p.C_i, p.C_o, p.T, p.C16);
+        static_cast<const uint16_t *>(filt), fa, status, total, pl.mode, p.C_i, p.C_o, p.H_f, p.W_f,
+        p.s_w, p.T, p.NCH, p.U, p.S);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    p.x = static_cast<const uint16_t *>(x);
+    p.src = static_cast<const uint16_t *>(src);
     p.fa = fa;
     p.out = static_cast<uint16_t *>(out);
     p.status = status;
-    p.vec = (s.W_i % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) ? 1 : 0;
+    p.vec = (s.W_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
     p.idesc0 = make_idesc(bf16, BM, p.N0);
     p.idesc1 = make_idesc(bf16, BM, p.N1 > 0 ? p.N1 : 16);
     p.bf16 = bf16 ? 1 : 0;
-    e = cudaFuncSetAttribute(conv_tc_tap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
-    if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.tiles_h * s.N), (unsigned)pl.mtiles);
-    conv_tc_tap_kernel<<<grid, TAP_THREADS, pl.smem, st>>>(p);
-    return cudaGetLastError();
+    auto go = [&](auto kernel) -> cudaError_t {
+        cudaError_t e2 = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (e2 != cudaSuccess) return e2;
+        kernel<<<grid, TAP_THREADS, pl.smem, st>>>(p);
+        return cudaGetLastError();
+    };
+    if (pl.mode == TAP_CH) return go(conv_tc_tap_kernel<TAP_CH>);
+    if (pl.mode == TAP_WX) return go(conv_tc_tap_kernel<TAP_WX>);
+    return go(conv_tc_tap_kernel<TAP_WW>);
 }
 
 cudaError_t launch_conv_tc(const void *src, const void *filt, void *out, void *ws, const Shape &s,
                            bool fused, bool bf16, cudaStream_t st) {
-    if (use_tap(s, fused)) return launch_tap(src, filt, out, ws, s, bf16, st);
+    const TapPlan pl = choose_tap(s, fused);
+    if (pl.ok) return launch_tap(pl, src, filt, out, ws, s, bf16, st);
     const ExpandGeom g = expand_geom(s);
     uint32_t *status = static_cast<uint32_t *>(ws);
     uint16_t *fa = reinterpret_cast<uint16_t *>(static_cast<unsigned char *>(ws) + kStatusBytes);

@@ -141,21 +141,23 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, const Ct
     for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
         if (honour_abort && *c.abort_flag) return false;
-        if ((spin & 63u) == 0) {
-            if (honour_abort && *reinterpret_cast<volatile uint32_t *>(c.status) != 0) {
-                *c.abort_flag = 1;
-                return false;
+        if ((spin & 255u) == 0 && globaltimer() - t0 > kTimeoutNs) {
+            *c.abort_flag = 1;
+            if (atomicCAS(c.status, 0u, (uint32_t)IM2WIN_ERR_TIMEOUT) == 0u) {
+                c.status[1] = site;
+                c.status[2] = blockIdx.x + blockIdx.y * gridDim.x;
             }
-            if (globaltimer() - t0 > kTimeoutNs) {
-                *c.abort_flag = 1;
-                if (atomicCAS(c.status, 0u, (uint32_t)IM2WIN_ERR_TIMEOUT) == 0u) {
-                    c.status[1] = site;
-                    c.status[2] = blockIdx.x + blockIdx.y * gridDim.x;
-                }
-                return false;
-            }
+            return false;
         }
     }
+}
+
+// The same wait for a whole warp: lane 0 polls, the others sleep in the
+// warp barrier; every lane gets lane 0's result.
+__device__ __forceinline__ bool warp_bar_wait(uint32_t bar, uint32_t parity, const Ctl &c, uint32_t site) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = bar_wait(bar, parity, c, site) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
