@@ -132,7 +132,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) conv_tc_expand_kernel(const __gri
                 for (int u = 0; u < KS / 16; ++u) {
                     const uint64_t ad = smem_desc(a0 + u * 256, 128, 1024);
                     const uint64_t bd = smem_desc(b0 + u * 256, 128, 1024);
+                    // pixels 0..127 and 128..255 in two accumulators: independent MMAs
                     mma_f16(tmem, ad, bd, p.idesc, (it | u) != 0);
+                    mma_f16(tmem + NT / 2, ad, bd + ((NT / 2 / 8 * 1024) >> 4), p.idesc, (it | u) != 0);
                 }
                 mma_commit(empty(s));
             }
@@ -220,28 +222,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) conv_tc_expand_kernel(const __gri
         tc_fence_after();
         if (ok) {
             const int q = warp & 3;              // TMEM lane quarter this warp may read
-            const int hh = (warp - 2) >> 2;      // which half of the columns
-            uint32_t *stage = reinterpret_cast<uint32_t *>(sB) + (warp - 2) * (32 * 17);
-            const uint16_t *st16 = reinterpret_cast<const uint16_t *>(stage);
+            const int hh = (warp - 2) >> 2;      // which half of the column blocks
             const int co0 = mt * BM + q * 32;
-            const int rows = min(32, p.C_o - co0);
             uint16_t *out_c = p.out + ((int64_t)n * p.C_o + co0) * p.P;
-            for (int blk = 0; blk < NT / 64; ++blk) {
-                const int col = hh * (NT / 2) + blk * 32;
-                uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)col, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    stage[lane * 17 + i] = pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), p.bf16);
-                __syncwarp();
-                const int pidx = pos0 + col + lane;
-                if (pidx < p.P) {
-                    uint16_t *dst = out_c + pidx;
-                    for (int row = 0; row < rows; ++row, dst += p.P) *dst = st16[row * 34 + lane];
-                }
-                __syncwarp();
-            }
+            drain_accumulator(tmem + ((uint32_t)(q * 32) << 16), hh, NT / 32, 2,
+                              reinterpret_cast<uint32_t *>(sB) + (warp - 2) * (32 * 17),
+                              min(32, p.C_o - co0), (int64_t)p.P, p.bf16, [&](int col) -> uint16_t * {
+                                  const int pidx = pos0 + col;
+                                  return pidx < p.P ? out_c + pidx : nullptr;
+                              });
         }
     }
 
@@ -455,7 +444,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                         const uint64_t bd = bdesc0 + (uint64_t)(((slab + toff[t]) & 0x3FFFFu) >> 4);
                         const uint32_t acc = (cc | t) != 0;
                         mma_f16(tmem, ad, bd, p.idesc0, acc);
-                        if (p.N1 > 0) mma_f16(tmem + 256, ad, bd + ((256 * 16) >> 4), p.idesc1, acc);
+                        if (p.N1 > 0) mma_f16(tmem + p.N0, ad, bd + (uint64_t)p.N0, p.idesc1, acc);
                     }
                     mma_commit(empty_a(sa));
                 }
@@ -623,32 +612,19 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         if (ok) {
             const int q4 = warp & 3;
             const int hh = (warp - 2) >> 2;
-            uint32_t *stage = reinterpret_cast<uint32_t *>(sB) + (warp - 2) * (32 * 17);
-            const uint16_t *st16 = reinterpret_cast<const uint16_t *>(stage);
             const int co0 = mt * BM + q4 * 32;
-            const int rows = min(32, p.C_o - co0);
             const int64_t plane = (int64_t)p.H_o * p.W_o;
             uint16_t *out_c = p.out + ((int64_t)n * p.C_o + co0) * plane;
-            const int nblk = (p.NTp + 31) / 32;
-            for (int blk = hh; blk < nblk; blk += 2) {
-                const int col = blk * 32;
-                uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)col, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    stage[lane * 17 + i] = pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), p.bf16);
-                __syncwarp();
-                const int pp = col + lane;
-                const int qrow = pp / p.pitch;
-                const int wo = pp - qrow * p.pitch;
-                const int ho = ho0 + qrow;
-                if (pp < p.NT && wo < p.W_o && ho < p.H_o) {
-                    uint16_t *dst = out_c + (int64_t)ho * p.W_o + wo;
-                    for (int row = 0; row < rows; ++row, dst += plane) *dst = st16[row * 34 + lane];
-                }
-                __syncwarp();
-            }
+            drain_accumulator(tmem + ((uint32_t)(q4 * 32) << 16), hh, (p.NTp + 31) / 32, 2,
+                              reinterpret_cast<uint32_t *>(sB) + (warp - 2) * (32 * 17),
+                              min(32, p.C_o - co0), plane, p.bf16, [&](int pp) -> uint16_t * {
+                                  const int qrow = pp / p.pitch;
+                                  const int wo = pp - qrow * p.pitch;
+                                  const int ho = ho0 + qrow;
+                                  if (pp < p.NT && wo < p.W_o && ho < p.H_o)
+                                      return out_c + (int64_t)ho * p.W_o + wo;
+                                  return nullptr;
+                              });
         }
     }
 
@@ -782,7 +758,9 @@ TapPlan plan_tap(const Shape &s, int mode) {
                     p.RR = (int)RR;
                     p.NT = (int)NT;
                     p.NTp = (int)NTp;
-                    p.N0 = (int)std::min<int64_t>(256, NTp);
+                    // two accumulators (positions [0, N0) and [N0, NTp)) so that
+                    // consecutive MMAs never wait on each other's result
+                    p.N0 = NTp > 256 ? 256 : NTp >= 32 ? (int)((NTp / 2 + 15) / 16 * 16) : (int)NTp;
                     p.N1 = (int)(NTp - p.N0);
                     p.lbo = (uint32_t)lbo;
                     p.PB = (uint32_t)PB;
@@ -931,7 +909,7 @@ cudaError_t launch_conv_tc(const void *src, const void *filt, void *out, void *w
     p.div_KKP = make_fastdiv((uint32_t)g.KKP);
     p.div_Hf = make_fastdiv((uint32_t)s.H_f);
     p.div_Wo = make_fastdiv((uint32_t)s.W_o);
-    p.idesc = make_idesc(bf16, BM, NT);
+    p.idesc = make_idesc(bf16, BM, NT / 2);
     p.bf16 = bf16 ? 1 : 0;
 
     dim3 grid((unsigned)(g.pos_tiles * s.N), (unsigned)g.mtiles);

@@ -161,17 +161,53 @@ __device__ __forceinline__ bool warp_bar_wait(uint32_t bar, uint32_t parity, con
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {
-    uint16_t a, b;
     if (bf16) {
-        a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-        b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    } else {
-        a = __half_as_ushort(__float2half_rn(lo));
-        b = __half_as_ushort(__float2half_rn(hi));
+        const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t *>(&v);
     }
-    return (uint32_t)a | ((uint32_t)b << 16);
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// Epilogue of one warp: drains TMEM column blocks first_blk, first_blk+step, ...
+// (< nblk, 32 columns each) of the warp's 32 accumulator lanes (taddr = lane
+// quarter base), rounds to fp16/bf16, transposes through the warp's shared
+// staging area (32 x 17 words) and stores: lane l writes column blk*32 + l of
+// rows 0..rows-1 at dst_of(blk*32 + l) + row*row_stride (dst_of returns
+// nullptr for columns that are not outputs). The TMEM load of the next block
+// is in flight while the current block is stored.
+template <typename DstFn>
+__device__ __forceinline__ void drain_accumulator(uint32_t taddr, int first_blk, int nblk, int step,
+                                                  uint32_t *stage, int rows, int64_t row_stride,
+                                                  int bf16, DstFn dst_of) {
+    const int lane = threadIdx.x & 31;
+    const uint16_t *st16 = reinterpret_cast<const uint16_t *>(stage);
+    if (first_blk >= nblk) return;
+    uint32_t r[32];
+    int blk = first_blk;
+    tmem_ld32(taddr + (uint32_t)(blk * 32), r);
+    while (true) {
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            stage[lane * 17 + i] = pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), bf16);
+        __syncwarp();
+        const int next = blk + step;
+        if (next < nblk) tmem_ld32(taddr + (uint32_t)(next * 32), r);
+        uint16_t v[32];
+#pragma unroll
+        for (int row = 0; row < 32; ++row) v[row] = st16[row * 34 + lane];
+        __syncwarp();
+        uint16_t *d = dst_of(blk * 32 + lane);
+        if (d != nullptr) {
+#pragma unroll
+            for (int row = 0; row < 32; ++row)
+                if (row < rows) d[row * row_stride] = v[row];
+        }
+        if (next >= nblk) break;
+        blk = next;
+    }
+}
 
 }  // namespace tc
 }  // namespace im2win

@@ -12,11 +12,15 @@
 //    of the band form one contiguous range of x, staged once into shared
 //    memory with 16-byte loads (rows shared by neighbouring output rows are
 //    read from HBM once per band);
-//  * the band's output is one contiguous range of win; every thread writes
-//    whole 16-byte vectors of it (coalesced, 128-bit stores), assembling each
-//    vector from shared memory; the unaligned head and tail of the range are
-//    written element by element, so neighbouring CTAs never overlap;
-//  * index arithmetic inside a band is 32-bit with multiply-high division.
+//  * the band's window rows are assembled in shared memory: a thread takes one
+//    input column w of one output row and copies its H_f elements (one per
+//    staged row) to window positions w*H_f .. w*H_f + H_f - 1, so consecutive
+//    lanes read consecutive shared-memory elements;
+//  * the band's output is one contiguous range of win; it leaves shared
+//    memory as whole 16-byte vectors (coalesced 128-bit stores), the buffer
+//    being offset so that its vectors line up with the global ones; the
+//    unaligned head and tail are written element by element, so neighbouring
+//    CTAs never overlap.
 // The element type is the raw bit pattern (uint16_t / uint32_t), so the copy
 // is bit-exact for every dtype.
 #include "im2win_internal.cuh"
@@ -25,7 +29,7 @@ namespace im2win {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kSmemBudget = 40 * 1024;  // per CTA, leaves room for 5 CTAs/SM
+constexpr int kSmemBudget = 56 * 1024;  // per CTA (input + output band), 4 CTAs/SM
 
 struct TParams {
     const void *x;
@@ -34,15 +38,16 @@ struct TParams {
     int64_t H_i, W_i, H_f, s_h, H_o;
     int64_t tiles_per_plane;
     int T;                // output rows per band
+    int in_cap;           // elements reserved for the staged input band (multiple of 8)
     uint32_t L;           // W_i * H_f
-    FastDiv div_L, div_Hf;
 };
 
 template <typename E>
 __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    E *s = reinterpret_cast<E *>(smem_raw);
     constexpr int V = 16 / sizeof(E);
+    E *s_in = reinterpret_cast<E *>(smem_raw);
+    E *s_out = s_in + p.in_cap;
 
     const E *__restrict__ x = static_cast<const E *>(p.x);
     E *__restrict__ win = static_cast<E *>(p.win);
@@ -54,8 +59,9 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
     const int rows_out = (int)(ho1 - ho0);
     const int rows_in = (int)((rows_out - 1) * p.s_h + p.H_f);
     const int W_i = (int)p.W_i, H_f = (int)p.H_f, s_h = (int)p.s_h;
+    const int L = (int)p.L;
 
-    // ---- stage the band's input rows: x[in0, in0 + cnt) -> s[lead, lead + cnt)
+    // ---- stage the band's input rows: x[in0, in0 + cnt) -> s_in[lead, lead + cnt)
     const int64_t in0 = (plane * p.H_i + ho0 * p.s_h) * p.W_i;
     const int cnt = rows_in * W_i;
     const int64_t base = in0 - (in0 % V);
@@ -64,87 +70,61 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
     for (int v = threadIdx.x; v < nvec; v += kThreads) {
         const int64_t g = base + (int64_t)v * V;
         if (g + V <= p.x_elems) {
-            *reinterpret_cast<uint4 *>(s + v * V) = __ldg(reinterpret_cast<const uint4 *>(x + g));
+            *reinterpret_cast<uint4 *>(s_in + v * V) = __ldg(reinterpret_cast<const uint4 *>(x + g));
         } else {
 #pragma unroll
             for (int i = 0; i < V; ++i)
-                if (g + i < p.x_elems) s[v * V + i] = x[g + i];
+                if (g + i < p.x_elems) s_in[v * V + i] = x[g + i];
         }
     }
     __syncthreads();
 
-    // ---- write the band's window rows: win[o0, o0 + rows_out*L)
-    const uint32_t L = p.L;
+    // ---- assemble the window rows: s_out[olead + hl*L + w*H_f + r] = s_in[lead + (hl*s_h + r)*W_i + w]
     const int64_t o0 = (plane * p.H_o + ho0) * (int64_t)L;
     const int64_t o1 = o0 + (int64_t)rows_out * L;
+    const int olead = (int)(o0 % V);
+    const E *sl = s_in + lead;
+    E *so = s_out + olead;
+    const int items = rows_out * W_i;
+    for (int it = threadIdx.x; it < items; it += kThreads) {
+        const int hl = it / W_i;
+        const int w = it - hl * W_i;
+        const E *src = sl + hl * s_h * W_i + w;
+        E *dst = so + hl * L + w * H_f;
+        for (int r = 0; r < H_f; ++r) dst[r] = src[r * W_i];
+    }
+    __syncthreads();
+
+    // ---- write win[o0, o1): aligned 16-byte vectors, ragged head and tail by element
     int64_t a0 = (o0 + V - 1) / V * V;
     int64_t a1 = o1 / V * V;
     if (a0 > o1) a0 = o1;
     if (a1 < a0) a1 = a0;
-    const E *sl = s + lead;
-
-    // element at local window index q (0 <= q < rows_out*L)
-    auto fetch = [&](uint32_t q) -> E {
-        uint32_t hl = fdiv(q, p.div_L);
-        uint32_t rem = q - hl * L;
-        uint32_t w = fdiv(rem, p.div_Hf);
-        uint32_t r = rem - w * (uint32_t)H_f;
-        return sl[((int)hl * s_h + (int)r) * W_i + (int)w];
-    };
-
-    // head and tail (fewer than V elements each)
     const int head = (int)(a0 - o0), tail = (int)(o1 - a1);
-    if ((int)threadIdx.x < head) win[o0 + threadIdx.x] = fetch(threadIdx.x);
-    if ((int)threadIdx.x < tail) {
-        uint32_t q = (uint32_t)(a1 - o0) + threadIdx.x;
-        win[a1 + threadIdx.x] = fetch(q);
-    }
-
-    // aligned body: whole 16-byte vectors
-    const uint32_t nbody = (uint32_t)((a1 - a0) / V);
-    for (uint32_t v = threadIdx.x; v < nbody; v += kThreads) {
-        uint32_t q = (uint32_t)(a0 - o0) + v * V;
-        uint32_t hl = fdiv(q, p.div_L);
-        uint32_t rem = q - hl * L;
-        uint32_t w = fdiv(rem, p.div_Hf);
-        uint32_t r = rem - w * (uint32_t)H_f;
-        int row = (int)hl * s_h + (int)r;
-        int col = (int)w;
-        union { uint4 u; E e[V]; } pack;
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-            pack.e[i] = sl[row * W_i + col];
-            // advance (r, w, hl) by one window element
-            ++r;
-            ++row;
-            if ((int)r == H_f) {
-                r = 0;
-                row -= H_f;
-                ++col;
-                if (col == W_i) {
-                    col = 0;
-                    row += s_h;
-                }
-            }
-        }
-        *reinterpret_cast<uint4 *>(win + a0 + (int64_t)v * V) = pack.u;
-    }
+    if ((int)threadIdx.x < head) win[o0 + threadIdx.x] = so[threadIdx.x];
+    if ((int)threadIdx.x < tail) win[a1 + threadIdx.x] = so[(int)(a1 - o0) + threadIdx.x];
+    const int nbody = (int)((a1 - a0) / V);
+    const uint4 *sv = reinterpret_cast<const uint4 *>(so + (a0 - o0));  // 16-byte aligned by olead
+    uint4 *gv = reinterpret_cast<uint4 *>(win + a0);
+    for (int v = threadIdx.x; v < nbody; v += kThreads) gv[v] = sv[v];
 }
 
 }  // namespace
 
 cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, cudaStream_t st) {
     if (s.N == 0) return cudaSuccess;
-    const int64_t row_bytes = s.W_i * esz;
-    // largest band whose staged input fits the budget (at least one output row)
-    int64_t T = (kSmemBudget / row_bytes - s.H_f) / s.s_h + 1;
-    if (T < 1) T = 1;
-    if (T > s.H_o) T = s.H_o;
+    const int64_t L = s.W_i * s.H_f;
+    // bytes of a band of T output rows: staged input rows + assembled window rows
+    auto band_bytes = [&](int64_t T) {
+        const int64_t in_elems = ((T - 1) * s.s_h + s.H_f) * s.W_i + 16;
+        return (in_elems + 8) / 8 * 8 * esz + (T * L + 16) * esz;
+    };
+    int64_t T = 1;
+    while (T < s.H_o && band_bytes(T + 1) <= kSmemBudget) ++T;
     // balance the bands of a plane
     const int64_t tiles = (s.H_o + T - 1) / T;
     T = (s.H_o + tiles - 1) / tiles;
-    const int64_t rows_in = (T - 1) * s.s_h + s.H_f;
-    const size_t smem = (size_t)(rows_in * row_bytes + 16);
+    const int64_t in_elems = ((T - 1) * s.s_h + s.H_f) * s.W_i + 16;
 
     TParams p;
     p.x = x;
@@ -157,9 +137,9 @@ cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, 
     p.H_o = s.H_o;
     p.tiles_per_plane = tiles;
     p.T = (int)T;
-    p.L = (uint32_t)(s.W_i * s.H_f);
-    p.div_L = make_fastdiv(p.L);
-    p.div_Hf = make_fastdiv((uint32_t)s.H_f);
+    p.in_cap = (int)((in_elems + 8) / 8 * 8);
+    p.L = (uint32_t)L;
+    const size_t smem = (size_t)band_bytes(T);
 
     const int64_t blocks = s.N * s.C_i * tiles;
     cudaError_t e;
@@ -177,10 +157,11 @@ cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, 
     return cudaGetLastError();
 }
 
-// The transform stages at least one output row's input rows (H_f rows of
-// W_i elements) and indexes a band with 32-bit arithmetic.
+// The transform stages at least one output row (its H_f input rows and its
+// window row) and indexes a band with 32-bit arithmetic.
 bool transform_supported(const Shape &s, int esz) {
-    const int64_t one_row = s.H_f * s.W_i * esz + 16;
+    // one output row: H_f staged rows plus one window row
+    const int64_t one_row = (s.H_f * s.W_i + 32) * esz + (s.W_i * s.H_f + 16) * esz;
     return one_row <= 200 * 1024 && s.W_i * s.H_f * s.H_o < (1ll << 31) &&
            s.N * s.C_i * s.H_o < (1ll << 31);
 }
