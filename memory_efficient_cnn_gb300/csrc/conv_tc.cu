@@ -304,9 +304,11 @@ __global__ void relayout_filter_expand(const uint16_t *__restrict__ filt, uint16
 enum TapMode { TAP_CH = 0, TAP_WX = 1, TAP_WW = 2 };
 
 constexpr int TAP_PROD_WARPS = 8;
-constexpr int TAP_THREADS = (2 + TAP_PROD_WARPS) * 32;
+constexpr int TAP_EPI_WARPS = 8;
+constexpr int TAP_THREADS = (2 + TAP_PROD_WARPS + TAP_EPI_WARPS) * 32;
 constexpr uint32_t TAP_A_BYTES = BM * 16 * 2;  // one K=16 tap of 128 channels: 4 KB
 constexpr int TAP_MAX_NT = 512;
+constexpr uint32_t TAP_EPI_BYTES = TAP_EPI_WARPS * 32 * 33 * 4;
 
 struct TapParams {
     const uint16_t *src;   // NCHW input (CH, WX) or window tensor (WW)
@@ -314,25 +316,49 @@ struct TapParams {
     uint16_t *out;
     uint32_t *status;
     int C_i, C_o, H_i, W_i, H_o, W_o, H_f, W_f, s_h, s_w;
+    int MT;                // 128-channel output tiles
     int NCH;               // chunks: 16-channel groups (CH) or channels (WX, WW)
     int T;                 // K=16 taps per chunk
     int TG, ntg;           // taps per filter stage, filter stages per chunk
-    int Q, tiles_h;        // output rows per tile, tiles per image
-    int pitch;             // positions per output row of the tile
-    int RR;                // CH: input rows per tile
-    int NT, NTp, N0, N1;   // positions, padded, MMA N of the two halves
+    int Qmax;              // output rows per tile at most
+    int tps;               // tiles per (image, channel tile)
+    int64_t tiles_total;   // N * MT * tps
+    int pitch;             // positions per output row of a tile
     uint32_t lbo;          // CH: bytes of an 8-channel plane; W*: bytes of a K chunk
     uint32_t PB;           // CH: bytes of a phase block
     int U, S, A;           // W*: K=16 groups per window step, window step s_w*H_f, taps along m
     int64_t L;             // WW: window row length W_i*H_f
     int64_t win_elems;     // WW: elements of the window tensor
+    int N_img;             // images (bound of the staged reads)
+    int raw_elems;         // W*: elements of the raw staging buffer
     uint32_t stage_b;      // bytes of one slab stage
     int BST, AST;          // slab stages, filter stages
-    uint32_t tmem_cols;
     int vec;               // CH: 16-byte row loads possible
-    uint32_t idesc0, idesc1;
     int bf16;
 };
+
+// A tile: output rows [ho0, ho0 + Q) of image n, output channels [mt*128, mt*128 + 128).
+struct TapTile {
+    int n, mt, ho0, Q;
+};
+
+// Tiles: each (image, channel tile) segment of H_o output rows is cut into
+// tps tiles of at most Qmax rows; tile id = (n*MT + mt)*tps + th. CTA b takes
+// tiles b, b + gridDim.x, ... Every role of the CTA walks the same sequence.
+__device__ __forceinline__ void tile_at(const TapParams &p, int64_t id, TapTile &t) {
+    const int64_t nm = id / p.tps;
+    const int th = (int)(id - nm * p.tps);
+    t.n = (int)(nm / p.MT);
+    t.mt = (int)(nm - (int64_t)t.n * p.MT);
+    t.ho0 = th * p.Qmax;
+    t.Q = min(p.Qmax, p.H_o - t.ho0);
+}
+
+// MMA split of a tile's NTp positions into two accumulators [0, N0) and
+// [N0, NTp) so that consecutive MMAs never wait on each other.
+__device__ __forceinline__ int split_n0(int NTp) {
+    return NTp >= 32 ? (NTp / 2 + 15) / 16 * 16 : NTp;
+}
 
 template <int MODE>
 __device__ __forceinline__ uint32_t tap_offset(const TapParams &p, int t) {
@@ -373,31 +399,37 @@ __device__ __forceinline__ uint4 load8_unaligned(const uint16_t *base, int64_t o
                       __byte_perm(u[2], u[3], sel), __byte_perm(u[3], u[4], sel));
 }
 
+// Persistent: one CTA per SM, each owning an equal share of the output rows.
+// Warp 0 issues the MMAs, warp 1 streams filter tiles, warps 2..9 fill the
+// slabs and warps 10..17 drain the accumulators, so the epilogue of one tile
+// and the slab fill of the next overlap the MMAs.
 template <int MODE>
 __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __grid_constant__ TapParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t a_stage = (uint32_t)p.TG * TAP_A_BYTES;
     uint8_t *sA = smem;
     uint8_t *sB = smem + (size_t)p.AST * a_stage;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + (size_t)p.BST * p.stage_b);
-    // bars: full_a[AST] | empty_a[AST] | full_b[BST] | empty_b[BST] | done | drain
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * p.AST + 2 * p.BST + 2);
+    uint16_t *sRaw = reinterpret_cast<uint16_t *>(sB + (size_t)p.BST * p.stage_b);
+    uint32_t *sE = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(sRaw) +
+                                                ((size_t)p.raw_elems * 2 + 127) / 128 * 128);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sE) + TAP_EPI_BYTES);
+    // [A stages][slab stages][raw rows (W modes)][epilogue staging] then
+    // bars: full_a[AST] | empty_a[AST] | full_b[BST] | empty_b[BST] | tmem_full | tmem_empty | drain
+    const int nb = 2 * p.AST + 2 * p.BST + 3;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + nb);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
-    uint32_t *toff = reinterpret_cast<uint32_t *>(bars + 2 * p.AST + 2 * p.BST + 4);  // [T] tap offsets
+    uint32_t *toff = reinterpret_cast<uint32_t *>(bars + nb + 1);  // [T] tap offsets
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int t = threadIdx.x; t < p.T; t += blockDim.x) toff[t] = tap_offset<MODE>(p, t);
-    const int n = blockIdx.x / p.tiles_h;
-    const int th = blockIdx.x - n * p.tiles_h;
-    const int mt = blockIdx.y;
-    const int ho0 = th * p.Q;
 
     auto full_a = [&](int s) { return smem_u32(bars + s); };
     auto empty_a = [&](int s) { return smem_u32(bars + p.AST + s); };
     auto full_b = [&](int s) { return smem_u32(bars + 2 * p.AST + s); };
     auto empty_b = [&](int s) { return smem_u32(bars + 2 * p.AST + p.BST + s); };
-    const uint32_t done = smem_u32(bars + 2 * p.AST + 2 * p.BST);
-    const uint32_t drain = smem_u32(bars + 2 * p.AST + 2 * p.BST + 1);
+    const uint32_t tmem_full = smem_u32(bars + 2 * p.AST + 2 * p.BST);
+    const uint32_t tmem_empty = smem_u32(bars + 2 * p.AST + 2 * p.BST + 1);
+    const uint32_t drain = smem_u32(bars + 2 * p.AST + 2 * p.BST + 2);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.AST; ++s) {
@@ -408,13 +440,14 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             mbar_init(full_b(s), TAP_PROD_WARPS * 32);
             mbar_init(empty_b(s), 1);
         }
-        mbar_init(done, 1);
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, TAP_EPI_WARPS);
         mbar_init(drain, 1);
         *abort_word = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+        tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -427,31 +460,47 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         // ---------------- MMA issuer
         if (lane == 0) {
             bool ok = true;
-            int a_it = 0;
+            int gb = 0, ga = 0, k = 0;
             const uint64_t adesc0 = smem_desc(0, 128, 256), bdesc0 = smem_desc(0, p.lbo, 128);
-            for (int cc = 0; cc < p.NCH && ok; ++cc) {
-                const int sb = cc % p.BST;
-                if (!(ok = bar_wait(full_b(sb), (cc / p.BST) & 1, ctl, SITE_FULL_B))) break;
-                const uint32_t slab = smem_u32(sB + (size_t)sb * p.stage_b);
-                for (int tg = 0; tg < p.ntg && ok; ++tg, ++a_it) {
-                    const int sa = a_it % p.AST;
-                    if (!(ok = bar_wait(full_a(sa), (a_it / p.AST) & 1, ctl, SITE_FULL_A))) break;
+            TapTile tl;
+            for (int64_t id = blockIdx.x; ok && id < p.tiles_total; id += gridDim.x) {
+                tile_at(p, id, tl);
+                if (k > 0) {
+                    // the previous tile's accumulators must be drained
+                    if (!(ok = bar_wait(tmem_empty, (k - 1) & 1, ctl, SITE_EMPTY_MMA))) break;
                     tc_fence_after();
-                    const int t0 = tg * p.TG;
-                    const int t_end = min(p.T, t0 + p.TG);
-                    uint64_t ad = adesc0 + ((uint64_t)((smem_u32(sA + (size_t)sa * a_stage) & 0x3FFFFu) >> 4));
-                    for (int t = t0; t < t_end; ++t, ad += TAP_A_BYTES >> 4) {
-                        const uint64_t bd = bdesc0 + (uint64_t)(((slab + toff[t]) & 0x3FFFFu) >> 4);
-                        const uint32_t acc = (cc | t) != 0;
-                        mma_f16(tmem, ad, bd, p.idesc0, acc);
-                        if (p.N1 > 0) mma_f16(tmem + p.N0, ad, bd + (uint64_t)p.N0, p.idesc1, acc);
-                    }
-                    mma_commit(empty_a(sa));
                 }
-                if (ok) mma_commit(empty_b(sb));
+                const int NTp = (tl.Q * p.pitch + 15) / 16 * 16;
+                const int N0 = split_n0(NTp), N1 = NTp - N0;
+                const uint32_t idesc0 = make_idesc(p.bf16 != 0, BM, N0);
+                const uint32_t idesc1 = make_idesc(p.bf16 != 0, BM, N1 > 0 ? N1 : 16);
+                for (int cc = 0; cc < p.NCH && ok; ++cc, ++gb) {
+                    const int sb = gb % p.BST;
+                    if (!(ok = bar_wait(full_b(sb), (gb / p.BST) & 1, ctl, SITE_FULL_B))) break;
+                    const uint32_t slab = smem_u32(sB + (size_t)sb * p.stage_b);
+                    for (int tg = 0; tg < p.ntg && ok; ++tg, ++ga) {
+                        const int sa = ga % p.AST;
+                        if (!(ok = bar_wait(full_a(sa), (ga / p.AST) & 1, ctl, SITE_FULL_A))) break;
+                        tc_fence_after();
+                        const int t0 = tg * p.TG;
+                        const int t_end = min(p.T, t0 + p.TG);
+                        uint64_t ad = adesc0 + ((uint64_t)((smem_u32(sA + (size_t)sa * a_stage) & 0x3FFFFu) >> 4));
+                        for (int t = t0; t < t_end; ++t, ad += TAP_A_BYTES >> 4) {
+                            const uint64_t bd = bdesc0 + (uint64_t)(((slab + toff[t]) & 0x3FFFFu) >> 4);
+                            const uint32_t acc = (cc | t) != 0;
+                            mma_f16(tmem, ad, bd, idesc0, acc);
+                            if (N1 > 0) mma_f16(tmem + N0, ad, bd + (uint64_t)N0, idesc1, acc);
+                        }
+                        mma_commit(empty_a(sa));
+                    }
+                    if (ok) mma_commit(empty_b(sb));
+                }
+                if (ok) mma_commit(tmem_full);
+                ++k;
             }
-            mma_commit(done);
-            if (!ok) bar_wait(done, 0, ctl, SITE_DRAIN, false);
+            // let every MMA in flight finish before the CTA tears down
+            mma_commit(drain);
+            bar_wait(drain, 0, ctl, SITE_DRAIN, false);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -459,18 +508,22 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         if (lane == 0) {
             int issued = 0;
             bool ok = true;
-            for (int cc = 0; cc < p.NCH && ok; ++cc) {
-                for (int tg = 0; tg < p.ntg; ++tg) {
-                    const int sa = issued % p.AST;
-                    if (!(ok = bar_wait(empty_a(sa), ((issued / p.AST) & 1) ^ 1, ctl, SITE_EMPTY_LOAD)))
-                        break;
-                    const int t0 = tg * p.TG;
-                    const uint32_t bytes = (uint32_t)(min(p.T, t0 + p.TG) - t0) * TAP_A_BYTES;
-                    const uint16_t *src =
-                        p.fa + (((int64_t)mt * p.NCH + cc) * p.T + t0) * (TAP_A_BYTES / 2);
-                    mbar_arrive_expect_tx(full_a(sa), bytes);
-                    bulk_g2s(smem_u32(sA + (size_t)sa * a_stage), src, bytes, full_a(sa));
-                    ++issued;
+            TapTile tl;
+            for (int64_t id = blockIdx.x; ok && id < p.tiles_total; id += gridDim.x) {
+                tile_at(p, id, tl);
+                for (int cc = 0; cc < p.NCH && ok; ++cc) {
+                    for (int tg = 0; tg < p.ntg; ++tg) {
+                        const int sa = issued % p.AST;
+                        if (!(ok = bar_wait(empty_a(sa), ((issued / p.AST) & 1) ^ 1, ctl, SITE_EMPTY_LOAD)))
+                            break;
+                        const int t0 = tg * p.TG;
+                        const uint32_t bytes = (uint32_t)(min(p.T, t0 + p.TG) - t0) * TAP_A_BYTES;
+                        const uint16_t *src =
+                            p.fa + (((int64_t)tl.mt * p.NCH + cc) * p.T + t0) * (TAP_A_BYTES / 2);
+                        mbar_arrive_expect_tx(full_a(sa), bytes);
+                        bulk_g2s(smem_u32(sA + (size_t)sa * a_stage), src, bytes, full_a(sa));
+                        ++issued;
+                    }
                 }
             }
             if (!ok) {
@@ -479,152 +532,193 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < 2 + TAP_PROD_WARPS) {
         // ---------------- slab producers
         const int pt = threadIdx.x - 64;
         constexpr int NPT = TAP_PROD_WARPS * 32;
-        for (int cc = 0; cc < p.NCH; ++cc) {
-            const int sb = cc % p.BST;
-            if (!warp_bar_wait(empty_b(sb), ((cc / p.BST) & 1) ^ 1, ctl, SITE_EMPTY_PROD)) break;
-            uint8_t *slab = sB + (size_t)sb * p.stage_b;
-            if (MODE == TAP_CH) {
-                const int R0 = ho0 * p.s_h;
-                const int rows = min(p.RR, p.H_i - R0);
-                const int64_t plane = (int64_t)p.H_i * p.W_i;
-                const uint16_t *__restrict__ xn = p.src + (int64_t)n * p.C_i * plane;
-                if (p.vec) {
-                    // 8 channels x 8 columns per item: 8 16-byte loads, 8x8 transpose, 8 16-byte stores
-                    const int cgs = p.W_i / 8;
-                    const int items = 2 * rows * cgs;
-                    for (int it = pt; it < items; it += NPT) {
-                        const int cg = it % cgs;
-                        const int t2 = it / cgs;
-                        const int lr = t2 % rows;
-                        const int c8 = t2 / rows;
-                        const int ci0 = cc * 16 + c8 * 8;
-                        uint4 v[8];
-                        const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)(R0 + lr) * p.W_i + cg * 8;
+        typedef uint16_t E16;
+        bool pok = true;
+        int gb = 0;
+        TapTile tl;
+        for (int64_t id = blockIdx.x; id < p.tiles_total; id += gridDim.x) {
+            tile_at(p, id, tl);
+            const int n = tl.n, ho0 = tl.ho0, Q = tl.Q;
+            for (int cc = 0; cc < p.NCH; ++cc, ++gb) {
+                const int sb = gb % p.BST;
+                int raw_lead = 0;
+                if (MODE != TAP_CH) {
+                    // stage the chunk's source rows (contiguous in global memory) with 16-byte
+                    // loads while earlier chunks are still being multiplied
+                    int64_t g0, cnt, total;
+                    if (MODE == TAP_WX) {
+                        const int R0 = ho0 * p.s_h;
+                        const int rows = (Q - 1) * p.s_h + p.H_f;
+                        g0 = (((int64_t)n * p.C_i + cc) * p.H_i + R0) * p.W_i;
+                        cnt = (int64_t)rows * p.W_i;
+                        total = (int64_t)p.N_img * p.C_i * p.H_i * p.W_i;
+                    } else {
+                        g0 = (((int64_t)n * p.C_i + cc) * p.H_o + ho0) * p.L;
+                        cnt = (int64_t)Q * p.L;
+                        total = p.win_elems;
+                    }
+                    raw_lead = (int)(g0 & 7);
+                    if (pok) {
+                        const int64_t base = g0 - raw_lead;
+                        const int nvec = (int)((raw_lead + cnt + 7) / 8);
+                        for (int v = pt; v < nvec; v += NPT) {
+                            const int64_t gg = base + (int64_t)v * 8;
+                            if (gg + 8 <= total) {
+                                *reinterpret_cast<uint4 *>(sRaw + v * 8) =
+                                    __ldg(reinterpret_cast<const uint4 *>(p.src + gg));
+                            } else {
+                                for (int i = 0; i < 8; ++i)
+                                    sRaw[v * 8 + i] = gg + i < total ? p.src[gg + i] : (E16)0;
+                            }
+                        }
+                    }
+                    asm volatile("bar.sync 1, %0;" ::"r"(NPT) : "memory");
+                }
+                if (pok) pok = warp_bar_wait(empty_b(sb), ((gb / p.BST) & 1) ^ 1, ctl, SITE_EMPTY_PROD);
+                uint8_t *slab = sB + (size_t)sb * p.stage_b;
+                if (!pok) {
+                    // aborted: keep meeting the producers' barrier, do no work
+                } else if (MODE == TAP_CH) {
+                    const int R0 = ho0 * p.s_h;
+                    const int rows = (Q - 1) * p.s_h + p.H_f;
+                    const int64_t plane = (int64_t)p.H_i * p.W_i;
+                    const uint16_t *__restrict__ xn = p.src + (int64_t)n * p.C_i * plane;
+                    if (p.vec) {
+                        // 8 channels x 8 columns per item: 8 16-byte loads, 8x8 transpose, 8 16-byte stores
+                        const int cgs = p.W_i / 8;
+                        const int items = 2 * rows * cgs;
+                        for (int it = pt; it < items; it += NPT) {
+                            const int cg = it % cgs;
+                            const int t2 = it / cgs;
+                            const int lr = t2 % rows;
+                            const int c8 = t2 / rows;
+                            const int ci0 = cc * 16 + c8 * 8;
+                            uint4 v[8];
+                            const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)(R0 + lr) * p.W_i + cg * 8;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            v[e] = (ci0 + e < p.C_i) ? __ldg(reinterpret_cast<const uint4 *>(src + e * plane))
-                                                     : make_uint4(0, 0, 0, 0);
-                        uint8_t *rowp = slab + (size_t)c8 * p.lbo + (size_t)((lr % p.s_h) * p.s_w) * p.PB +
-                                        (size_t)((lr / p.s_h) * p.pitch) * 16;
+                            for (int e = 0; e < 8; ++e)
+                                v[e] = (ci0 + e < p.C_i) ? __ldg(reinterpret_cast<const uint4 *>(src + e * plane))
+                                                         : make_uint4(0, 0, 0, 0);
+                            uint8_t *rowp = slab + (size_t)c8 * p.lbo + (size_t)((lr % p.s_h) * p.s_w) * p.PB +
+                                            (size_t)((lr / p.s_h) * p.pitch) * 16;
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const int col = cg * 8 + k;
-                            const uint32_t sel = (k & 1) ? 0x7632u : 0x5410u;
-                            const int wd = k >> 1;
-                            const uint32_t w0 = __byte_perm(word_of(v[0], wd), word_of(v[1], wd), sel);
-                            const uint32_t w1 = __byte_perm(word_of(v[2], wd), word_of(v[3], wd), sel);
-                            const uint32_t w2 = __byte_perm(word_of(v[4], wd), word_of(v[5], wd), sel);
-                            const uint32_t w3 = __byte_perm(word_of(v[6], wd), word_of(v[7], wd), sel);
-                            uint8_t *dst = rowp + (size_t)(col % p.s_w) * p.PB + (size_t)(col / p.s_w) * 16;
-                            *reinterpret_cast<uint4 *>(dst) = make_uint4(w0, w1, w2, w3);
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const int col = cg * 8 + kk;
+                                const uint32_t sel = (kk & 1) ? 0x7632u : 0x5410u;
+                                const int wd = kk >> 1;
+                                const uint32_t w0 = __byte_perm(word_of(v[0], wd), word_of(v[1], wd), sel);
+                                const uint32_t w1 = __byte_perm(word_of(v[2], wd), word_of(v[3], wd), sel);
+                                const uint32_t w2 = __byte_perm(word_of(v[4], wd), word_of(v[5], wd), sel);
+                                const uint32_t w3 = __byte_perm(word_of(v[6], wd), word_of(v[7], wd), sel);
+                                uint8_t *dst = rowp + (size_t)(col % p.s_w) * p.PB + (size_t)(col / p.s_w) * 16;
+                                *reinterpret_cast<uint4 *>(dst) = make_uint4(w0, w1, w2, w3);
+                            }
+                        }
+                    } else {
+                        // one column of 8 channels per item
+                        const int items = 2 * rows * p.W_i;
+                        for (int it = pt; it < items; it += NPT) {
+                            const int col = it % p.W_i;
+                            const int t2 = it / p.W_i;
+                            const int lr = t2 % rows;
+                            const int c8 = t2 / rows;
+                            const int ci0 = cc * 16 + c8 * 8;
+                            const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)(R0 + lr) * p.W_i + col;
+                            uint32_t e16[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                e16[e] = (ci0 + e < p.C_i) ? (uint32_t)__ldg(src + e * plane) : 0u;
+                            uint8_t *dst = slab + (size_t)c8 * p.lbo +
+                                           (size_t)((lr % p.s_h) * p.s_w + col % p.s_w) * p.PB +
+                                           (size_t)((lr / p.s_h) * p.pitch + col / p.s_w) * 16;
+                            *reinterpret_cast<uint4 *>(dst) =
+                                make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
+                                           e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
                         }
                     }
                 } else {
-                    // one column of 8 channels per item
-                    const int items = 2 * rows * p.W_i;
+                    // window rows of channel cc, re-laid from the staged raw rows:
+                    //   entry (c, q, m)[e] = window row q of the tile at m*S + 8c + e
+                    // TAP_WX: that element is x[cc][(ho0+q)*s_h + r][m*s_w + jl] with 8c + e = jl*H_f + r
+                    // TAP_WW: it is read straight from the staged window row
+                    const int SC = 2 * p.U;
+                    const int items = SC * Q * p.pitch;
+                    const E16 *raw = sRaw + raw_lead;
                     for (int it = pt; it < items; it += NPT) {
-                        const int col = it % p.W_i;
-                        const int t2 = it / p.W_i;
-                        const int lr = t2 % rows;
-                        const int c8 = t2 / rows;
-                        const int ci0 = cc * 16 + c8 * 8;
-                        const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)(R0 + lr) * p.W_i + col;
+                        const int m = it % p.pitch;
+                        const int t2 = it / p.pitch;
+                        const int q = t2 % Q;
+                        const int c = t2 / Q;
                         uint32_t e16[8];
+                        const int b0 = 8 * c;
+                        if (MODE == TAP_WX) {
+                            int jl = b0 / p.H_f;
+                            int r = b0 - jl * p.H_f;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            e16[e] = (ci0 + e < p.C_i) ? (uint32_t)__ldg(src + e * plane) : 0u;
-                        uint8_t *dst = slab + (size_t)c8 * p.lbo +
-                                       (size_t)((lr % p.s_h) * p.s_w + col % p.s_w) * p.PB +
-                                       (size_t)((lr / p.s_h) * p.pitch + col / p.s_w) * 16;
-                        *reinterpret_cast<uint4 *>(dst) =
+                            for (int e = 0; e < 8; ++e) {
+                                const int col = m * p.s_w + jl;
+                                const bool v = (b0 + e < p.S) && col < p.W_i;
+                                e16[e] = v ? (uint32_t)raw[(q * p.s_h + r) * p.W_i + col] : 0u;
+                                if (++r == p.H_f) { r = 0; ++jl; }
+                            }
+                        } else {
+                            const int idx0 = m * p.S + b0;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const bool v = (b0 + e < p.S) && (idx0 + e < (int)p.L);
+                                e16[e] = v ? (uint32_t)raw[q * (int)p.L + idx0 + e] : 0u;
+                            }
+                        }
+                        *reinterpret_cast<uint4 *>(slab + (size_t)c * p.lbo + (size_t)(q * p.pitch + m) * 16) =
                             make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
                                        e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
                     }
                 }
-            } else if (MODE == TAP_WX) {
-                // window rows of channel cc built straight from x:
-                // entry (c, q, m)[e] = x[cc][(ho0+q)*s_h + r][m*s_w + jl] for b = 8c + e = jl*H_f + r
-                const int SC = 2 * p.U;
-                const int items = SC * p.Q * p.pitch;
-                const uint16_t *__restrict__ xc = p.src + ((int64_t)n * p.C_i + cc) * p.H_i * p.W_i;
-                for (int it = pt; it < items; it += NPT) {
-                    const int m = it % p.pitch;
-                    const int t2 = it / p.pitch;
-                    const int q = t2 % p.Q;
-                    const int c = t2 / p.Q;
-                    uint32_t e16[8];
-                    const int b0 = 8 * c;
-                    int jl = b0 / p.H_f;
-                    int r = b0 - jl * p.H_f;
-                    const bool rowv = ho0 + q < p.H_o;
-                    const int rbase = (ho0 + q) * p.s_h;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int col = m * p.s_w + jl;
-                        const bool v = rowv && (b0 + e < p.S) && col < p.W_i;
-                        e16[e] = v ? (uint32_t)__ldg(xc + (int64_t)(rbase + r) * p.W_i + col) : 0u;
-                        if (++r == p.H_f) { r = 0; ++jl; }
-                    }
-                    *reinterpret_cast<uint4 *>(slab + (size_t)c * p.lbo + (size_t)(q * p.pitch + m) * 16) =
-                        make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
-                                   e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
+                if (pok) {
+                    fence_async_smem();
+                    mbar_arrive(full_b(sb));
                 }
-            } else {
-                // window rows of channel cc read from the window tensor:
-                // entry (c, q, m) = win[n][cc][ho0+q][m*S + 8c .. +8]
-                const int SC = 2 * p.U;
-                const int items = SC * p.Q * p.pitch;
-                const int64_t base_nc = ((int64_t)n * p.C_i + cc) * p.H_o;
-                for (int it = pt; it < items; it += NPT) {
-                    const int c = it % SC;
-                    const int t2 = it / SC;
-                    const int m = t2 % p.pitch;
-                    const int q = t2 / p.pitch;
-                    uint4 val = make_uint4(0, 0, 0, 0);
-                    if (ho0 + q < p.H_o) {
-                        const int64_t wo0 = (int64_t)m * p.S + 8 * c;   // within the window row
-                        const int64_t o = (base_nc + ho0 + q) * p.L + wo0;
-                        const int valid = (int)min((int64_t)min(8, p.S - 8 * c), p.L - wo0);
-                        if (valid == 8 && ((o >> 3) + 2) * 8 <= p.win_elems) {
-                            val = load8_unaligned(p.src, o);
-                        } else if (valid > 0) {
-                            uint32_t e16[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) e16[e] = (e < valid) ? (uint32_t)__ldg(p.src + o + e) : 0u;
-                            val = make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
-                                             e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
-                        }
-                    }
-                    *reinterpret_cast<uint4 *>(slab + (size_t)c * p.lbo + (size_t)(q * p.pitch + m) * 16) = val;
-                }
+                // the raw rows are consumed: they may be overwritten by the next chunk
+                if (MODE != TAP_CH) asm volatile("bar.sync 1, %0;" ::"r"(NPT) : "memory");
             }
-            fence_async_smem();
-            mbar_arrive(full_b(sb));
+            if (MODE == TAP_CH && !pok) break;
         }
-
+    } else {
         // ---------------- epilogue: TMEM -> registers -> smem transpose -> coalesced stores
-        const bool ok = warp_bar_wait(done, 0, ctl, SITE_DONE);
-        tc_fence_after();
-        if (ok) {
-            const int q4 = warp & 3;
-            const int hh = (warp - 2) >> 2;
-            const int co0 = mt * BM + q4 * 32;
-            const int64_t plane = (int64_t)p.H_o * p.W_o;
-            uint16_t *out_c = p.out + ((int64_t)n * p.C_o + co0) * plane;
-            drain_accumulator(tmem + ((uint32_t)(q4 * 32) << 16), hh, (p.NTp + 31) / 32, 2,
-                              reinterpret_cast<uint32_t *>(sB) + (warp - 2) * (32 * 17),
-                              min(32, p.C_o - co0), plane, p.bf16, [&](int pp) -> uint16_t * {
-                                  const int qrow = pp / p.pitch;
-                                  const int wo = pp - qrow * p.pitch;
-                                  const int ho = ho0 + qrow;
-                                  if (pp < p.NT && wo < p.W_o && ho < p.H_o)
-                                      return out_c + (int64_t)ho * p.W_o + wo;
-                                  return nullptr;
-                              });
+        const int ew = warp - 2 - TAP_PROD_WARPS;  // 0..7
+        const int q4 = warp & 3;                  // TMEM lane quarter this warp may read
+        const int hh = ew >> 2;                   // which half of the columns
+        uint32_t *stage = sE + ew * (32 * 33);
+        const int64_t plane = (int64_t)p.H_o * p.W_o;
+        int k = 0;
+        TapTile tl;
+        for (int64_t id = blockIdx.x; id < p.tiles_total; id += gridDim.x) {
+            tile_at(p, id, tl);
+            if (!warp_bar_wait(tmem_full, k & 1, ctl, SITE_DONE)) break;
+            tc_fence_after();
+            const int co0 = tl.mt * BM + q4 * 32;
+            const int NT = tl.Q * p.pitch;
+            const int NTp = (NT + 15) / 16 * 16;
+            // the two warps of a quarter split the columns in 64-column blocks
+            const int nb64 = (NTp + 63) / 64;
+            const int c_begin = hh == 0 ? 0 : ((nb64 + 1) / 2) * 64;
+            const int c_end = hh == 0 ? min(NTp, ((nb64 + 1) / 2) * 64) : NTp;
+            uint16_t *out_c = p.out + ((int64_t)tl.n * p.C_o + co0) * plane + (int64_t)tl.ho0 * p.W_o;
+            const int pitch = p.pitch, W_o = p.W_o;
+            drain_columns(tmem + ((uint32_t)(q4 * 32) << 16), c_begin, c_end, stage, min(32, p.C_o - co0),
+                          plane, p.bf16, out_c, [&](int pp) -> int {
+                              const int qrow = pp / pitch;
+                              const int wo = pp - qrow * pitch;
+                              return (pp < NT && wo < W_o) ? qrow * W_o + wo : -1;
+                          });
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tmem_empty);
+            ++k;
         }
     }
 
@@ -632,7 +726,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, p.tmem_cols);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -688,8 +782,34 @@ struct TapPlan {
     int64_t kslots;        // MMA K values per output pixel (cost model)
 };
 
-// Tiling of a tap kernel for a shape (mode TAP_CH / TAP_WX / TAP_WW), or !ok.
-TapPlan plan_tap(const Shape &s, int mode) {
+static int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+// Modelled time of one tile of NT positions: two MMAs of N = NTp/2 per K step,
+// at rates measured for tcgen05.mma M=128 with two accumulators (MAC/clk/SM:
+// N=64 1962, 128 2880, 224 3347, 256 3542), plus a fixed drain/restart cost.
+static double tile_cost(int64_t NT) {
+    const double n = (double)((NT + 15) / 16 * 16) / 2.0;
+    const double pts[5][2] = {{16, 600}, {64, 1962}, {128, 2880}, {224, 3347}, {256, 3542}};
+    double rate = pts[4][1];
+    for (int i = 0; i < 4; ++i)
+        if (n <= pts[i + 1][0]) {
+            const double f = (n - pts[i][0]) / (pts[i + 1][0] - pts[i][0]);
+            rate = pts[i][1] + (n < pts[i][0] ? 0.0 : f) * (pts[i + 1][1] - pts[i][1]);
+            break;
+        }
+    return 2.0 * n / rate + 0.15;  // relative units
+}
+
+// Tiling of a tap kernel for a shape (mode TAP_CH / TAP_WX / TAP_WW) on `sms`
+// SMs, or !ok: the tiling with the least modelled time among those whose slab
+// stages fit shared memory. Whether a plan exists, and its filter layout, do
+// not depend on `sms`.
+TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
     TapPlan pl{};
     pl.ok = false;
     pl.mode = mode;
@@ -708,16 +828,27 @@ TapPlan plan_tap(const Shape &s, int mode) {
         T = A * U;
         NCH = s.C_i;
         if (mode == TAP_WW && s.N * s.C_i * s.H_o * s.W_i * s.H_f >= (1ll << 40)) return pl;
+        if (s.H_o * s.W_i * s.H_f >= (1ll << 31)) return pl;
     }
-    if (pitch > TAP_MAX_NT) return pl;
-    for (int64_t Qmax = std::min<int64_t>(s.H_o, TAP_MAX_NT / pitch); Qmax >= 1; --Qmax) {
-        const int64_t tiles = (s.H_o + Qmax - 1) / Qmax;
-        const int64_t Q = (s.H_o + tiles - 1) / tiles;
-        const int64_t NT = Q * pitch;
-        const int64_t NTp = (NT + 15) / 16 * 16;
-        int64_t RR = 0, PB = 0, lbo, stage_b;
+    if (pitch > TAP_MAX_NT || T > 4096) return pl;
+    const int64_t Qcap = std::min<int64_t>(s.H_o, TAP_MAX_NT / pitch);
+    const int64_t MT = (s.C_o + BM - 1) / BM;
+    for (int64_t Qfit = Qcap; Qfit >= 1; --Qfit) {
+        // rows per tile: among tilings with at most Qfit rows, the one with the least
+        // modelled time = rounds of tiles over the SMs x time of one tile
+        int64_t Q = Qfit;
+        double best = 1e30;
+        for (int64_t tps = (s.H_o + Qfit - 1) / Qfit; tps <= (s.H_o + Qfit - 1) / Qfit + 4 && tps <= s.H_o; ++tps) {
+            const int64_t q = (s.H_o + tps - 1) / tps;
+            const int64_t tiles = s.N * MT * tps;
+            const int64_t rounds = (tiles + sms - 1) / sms;
+            const double t = (double)rounds * tile_cost(q * pitch);
+            if (t < best * 0.99) { best = t; Q = q; }
+        }
+        const int64_t NTp = (Q * pitch + 15) / 16 * 16;
+        const int64_t RR = (Q - 1) * s.s_h + s.H_f;  // input rows under a tile of Q rows
+        int64_t PB = 0, lbo, stage_b;
         if (mode == TAP_CH) {
-            RR = (Q - 1) * s.s_h + s.H_f;
             const int64_t HH = (RR + s.s_h - 1) / s.s_h;
             PB = HH * pitch * 16;
             lbo = s.s_h * s.s_w * PB;
@@ -734,34 +865,32 @@ TapPlan plan_tap(const Shape &s, int mode) {
             stage_b = std::max(2 * U * lbo, (2 * U - 1) * lbo + (A - 1 + NTp) * 16);
         }
         stage_b = (stage_b + 127) / 128 * 128;
-        if (stage_b < 8 * 32 * 17 * 4) stage_b = 8 * 32 * 17 * 4;  // epilogue staging reuses it
+        const int64_t raw = mode == TAP_CH ? 0
+                            : mode == TAP_WX ? (RR * s.W_i + 16) * 2
+                                             : (Q * s.W_i * s.H_f + 16) * 2;
         for (int BST : {3, 2}) {
             for (int TG : {9, 8, 6, 5, 4, 3, 2, 1}) {
                 const int tg = (int)std::min<int64_t>(TG, T);
                 if (TG > T && TG != 1) continue;
                 for (int AST : {4, 3, 2}) {
-                    int64_t total = (int64_t)AST * tg * TAP_A_BYTES + BST * stage_b + 256 + 4 * T;
+                    int64_t total = (int64_t)AST * tg * TAP_A_BYTES + BST * stage_b + (raw + 127) / 128 * 128 +
+                                    TAP_EPI_BYTES + 512 + 4 * T;
                     if (total > smem_max) continue;
-                    // a 512-column TMEM accumulator needs the SM to itself
-                    if (NTp > 256) total = std::max<int64_t>(total, 120 * 1024);
+                    // the 512-column TMEM accumulator needs the SM to itself
+                    total = std::max<int64_t>(total, 120 * 1024);
                     TapParams &p = pl.p;
                     p.C_i = (int)s.C_i; p.C_o = (int)s.C_o; p.H_i = (int)s.H_i; p.W_i = (int)s.W_i;
                     p.H_o = (int)s.H_o; p.W_o = (int)s.W_o; p.H_f = (int)s.H_f; p.W_f = (int)s.W_f;
                     p.s_h = (int)s.s_h; p.s_w = (int)s.s_w;
+                    p.MT = (int)((s.C_o + BM - 1) / BM);
                     p.NCH = (int)NCH;
                     p.T = (int)T;
                     p.TG = tg;
                     p.ntg = (int)((T + tg - 1) / tg);
-                    p.Q = (int)Q;
-                    p.tiles_h = (int)tiles;
+                    p.Qmax = (int)Q;
+                    p.tps = (int)((s.H_o + Q - 1) / Q);
+                    p.tiles_total = s.N * p.MT * p.tps;
                     p.pitch = (int)pitch;
-                    p.RR = (int)RR;
-                    p.NT = (int)NT;
-                    p.NTp = (int)NTp;
-                    // two accumulators (positions [0, N0) and [N0, NTp)) so that
-                    // consecutive MMAs never wait on each other's result
-                    p.N0 = NTp > 256 ? 256 : NTp >= 32 ? (int)((NTp / 2 + 15) / 16 * 16) : (int)NTp;
-                    p.N1 = (int)(NTp - p.N0);
                     p.lbo = (uint32_t)lbo;
                     p.PB = (uint32_t)PB;
                     p.U = (int)U;
@@ -769,14 +898,15 @@ TapPlan plan_tap(const Shape &s, int mode) {
                     p.A = (int)A;
                     p.L = s.W_i * s.H_f;
                     p.win_elems = s.N * s.C_i * s.H_o * s.W_i * s.H_f;
+                    p.N_img = (int)s.N;
+                    p.raw_elems = (int)(raw / 2);
                     p.stage_b = (uint32_t)stage_b;
                     p.BST = BST;
                     p.AST = AST;
-                    p.tmem_cols = NTp > 256 ? 512 : 256;
                     pl.smem = (size_t)total;
-                    pl.mtiles = (int)((s.C_o + BM - 1) / BM);
+                    pl.mtiles = p.MT;
                     pl.kslots = NCH * T * 16;
-                    pl.ok = tiles * s.N < (1ll << 31) && pl.mtiles < 65536;
+                    pl.ok = p.tiles_total < (1ll << 40) && s.N < (1ll << 31);
                     return pl;
                 }
             }
@@ -807,13 +937,13 @@ ExpandGeom expand_geom(const Shape &s) {
 // whichever needs fewer MMA K values per pixel; from the window tensor: the
 // window-row tap kernel. Either falls back to the expand kernel when its K
 // padding costs more than half again the expand kernel's K.
-static TapPlan choose_tap(const Shape &s, bool fused) {
+static TapPlan choose_tap(const Shape &s, bool fused, int64_t sms = 148) {
     const int64_t expand_k = s.C_i * ((s.H_f * s.W_f + 7) / 8 * 8);
     TapPlan best{};
     best.ok = false;
     for (int mode : {TAP_CH, TAP_WX, TAP_WW}) {
         if ((mode == TAP_WW) == fused) continue;
-        TapPlan pl = plan_tap(s, mode);
+        TapPlan pl = plan_tap(s, mode, sms);
         if (pl.ok && (!best.ok || pl.kslots < best.kslots)) best = pl;
     }
     if (best.ok && best.kslots * 2 > expand_k * 3) best.ok = false;
@@ -853,10 +983,8 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
     p.out = static_cast<uint16_t *>(out);
     p.status = status;
     p.vec = (s.W_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
-    p.idesc0 = make_idesc(bf16, BM, p.N0);
-    p.idesc1 = make_idesc(bf16, BM, p.N1 > 0 ? p.N1 : 16);
     p.bf16 = bf16 ? 1 : 0;
-    dim3 grid((unsigned)(p.tiles_h * s.N), (unsigned)pl.mtiles);
+    const unsigned grid = (unsigned)std::min<int64_t>(sm_count(), p.tiles_total);
     auto go = [&](auto kernel) -> cudaError_t {
         cudaError_t e2 = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (e2 != cudaSuccess) return e2;
@@ -870,7 +998,7 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
 
 cudaError_t launch_conv_tc(const void *src, const void *filt, void *out, void *ws, const Shape &s,
                            bool fused, bool bf16, cudaStream_t st) {
-    const TapPlan pl = choose_tap(s, fused);
+    const TapPlan pl = choose_tap(s, fused, sm_count());
     if (pl.ok) return launch_tap(pl, src, filt, out, ws, s, bf16, st);
     const ExpandGeom g = expand_geom(s);
     uint32_t *status = static_cast<uint32_t *>(ws);

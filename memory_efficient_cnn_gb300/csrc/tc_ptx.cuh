@@ -209,5 +209,57 @@ __device__ __forceinline__ void drain_accumulator(uint32_t taddr, int first_blk,
     }
 }
 
+// Faster drain for the tap kernels. The warp owns TMEM columns [c_begin,
+// c_end) of its 32 accumulator lanes (taddr = lane quarter base). Per block of
+// 64 columns: two 32-column TMEM loads (the next block's first load is in
+// flight while this block is stored), rounding to fp16/bf16, a transpose
+// through the warp's staging area (32 rows x 33 words), then lane l stores
+// positions 2l and 2l+1 of every row -- one 4-byte store when the two are
+// adjacent in the output and 4-byte aligned, else two 2-byte stores.
+// off_of(col) gives the output element offset of column col within a channel
+// plane (or -1 if the column is not an output); row r of the block lives at
+// out_c + r*row_stride.
+template <typename OffFn>
+__device__ __forceinline__ void drain_columns(uint32_t taddr, int c_begin, int c_end, uint32_t *stage,
+                                              int rows, int64_t row_stride, int bf16,
+                                              uint16_t *out_c, OffFn off_of) {
+    const int lane = threadIdx.x & 31;
+    if (c_begin >= c_end) return;
+    const bool stride_even = (row_stride & 1) == 0;
+    const int64_t base_par = (int64_t)(reinterpret_cast<uintptr_t>(out_c) >> 1);
+    uint32_t r[32];
+    tmem_ld32(taddr + (uint32_t)c_begin, r);
+    for (int c0 = c_begin; c0 < c_end; c0 += 64) {
+        // ---- columns c0..c0+31, then c0+32..c0+63 into the staging area (u16 [32][66])
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                stage[lane * 33 + half * 16 + i] = pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), bf16);
+            const int nxt = half == 0 ? c0 + 32 : c0 + 64;
+            if (nxt < c_end) tmem_ld32(taddr + (uint32_t)nxt, r);
+        }
+        __syncwarp();
+        // ---- lane l: positions c0 + 2l, c0 + 2l + 1 of every row
+        const int o0 = off_of(c0 + 2 * lane), o1 = off_of(c0 + 2 * lane + 1);
+        const bool pair = o0 >= 0 && o1 == o0 + 1;
+#pragma unroll 8
+        for (int row = 0; row < 32; ++row) {
+            if (row >= rows) break;
+            const uint32_t w = stage[row * 33 + lane];
+            uint16_t *d = out_c + (int64_t)row * row_stride;
+            const bool even = (((base_par + (stride_even ? 0 : row)) + o0) & 1) == 0;
+            if (pair && even) {
+                *reinterpret_cast<uint32_t *>(d + o0) = w;
+            } else {
+                if (o0 >= 0) d[o0] = (uint16_t)(w & 0xFFFFu);
+                if (o1 >= 0) d[o1] = (uint16_t)(w >> 16);
+            }
+        }
+        __syncwarp();
+    }
+}
+
 }  // namespace tc
 }  // namespace im2win
