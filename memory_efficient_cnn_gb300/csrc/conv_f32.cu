@@ -9,11 +9,12 @@
 // concatenation over ci of that pixel's contiguous window segments.
 //
 // Kernel: a CTA computes TM output channels x 128 pixels of one image.
-// The K dimension is walked in chunks of 16; each chunk's window segments
-// (16 x 128) and filter slice (16 x TM) are staged in shared memory, double
-// buffered through registers, and every thread accumulates an 8 x 4
-// (channels x pixels) register tile with FFMA. Warps are 4 channel-groups x
-// 8 pixel-groups so that the shared-memory operand reads are broadcasts.
+// The K dimension is walked in chunks of KC; each chunk's window segments
+// (KC x 128) and filter slice (KC x TM) are staged in shared memory, double
+// buffered through registers, and every thread accumulates an 8 x 8
+// (channels x pixels) register tile with FFMA (4 operand reads of 16 bytes
+// per 64 FFMA). Warps are 4 channel-groups x 8 pixel-groups so that every
+// shared-memory operand read is one conflict-free wavefront.
 // The fused variant (FROM_X) gathers the same matrix straight from the NCHW
 // input (x[n][ci][ho*s_h + r][wo*s_w + j] for k = j*H_f + r) and never
 // materialises the window tensor.
@@ -25,7 +26,6 @@ namespace im2win {
 namespace {
 
 constexpr int TP = 128;  // pixels per CTA
-constexpr int KC = 16;   // K per stage
 
 struct F32Params {
     const float *src;    // window tensor or NCHW input
@@ -43,13 +43,32 @@ struct F32Params {
     FastDiv div_KK, div_Wo, div_Hf;
 };
 
-template <int TM, bool FROM_X>
-__global__ void __launch_bounds__(TM * 4) conv_f32_kernel(F32Params p) {
-    constexpr int NT = TM * 4;
-    constexpr int A_PER = KC * TP / NT;   // window elements each thread stages
-    constexpr int B_PER = KC * TM / NT;   // filter elements each thread stages (4)
-    __shared__ __align__(16) float As[2][KC][TP + 4];
-    __shared__ __align__(16) float Bs[2][KC][TM + 4];
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// 4-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const float *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// TM output channels x 128 pixels per CTA, 8 x 8 register tile per thread
+// (channels ty*8..+7, pixels tx*4..+3 and 64 + tx*4..+3). K is staged KC at a
+// time through a 3-stage cp.async pipeline (gathers go straight to shared
+// memory, so no registers hold prefetched data).
+template <int TM, int KC, bool FROM_X>
+__global__ void __launch_bounds__(TM * 2, (TM >= 96 ? 2 : 4)) conv_f32_kernel(F32Params p) {
+    constexpr int NT = TM * 2;                 // (TM/8) x 16 threads
+    constexpr int A_PER = KC * TP / NT;        // window elements each thread stages
+    constexpr int B_PER = KC * TM / NT;        // filter elements each thread stages
+    constexpr int STAGES = 3;
+    static_assert(NT % KC == 0 && (KC * TP) % NT == 0 && (KC * TM) % NT == 0, "tile");
+    extern __shared__ __align__(16) float smem_f[];
+    float (*As)[KC][TP + 4] = reinterpret_cast<float (*)[KC][TP + 4]>(smem_f);
+    float (*Bs)[KC][TM + 4] = reinterpret_cast<float (*)[KC][TM + 4]>(smem_f + STAGES * KC * (TP + 4));
 
     const int tid = threadIdx.x;
     const int n = blockIdx.x / p.pos_tiles;
@@ -58,91 +77,89 @@ __global__ void __launch_bounds__(TM * 4) conv_f32_kernel(F32Params p) {
     const float *__restrict__ src = p.src + (int64_t)n * p.img_src;
     const float *__restrict__ filt = p.filt;
 
-    // ---- per-thread staging coordinates (k fixed, A_PER pixels)
+    // ---- staging coordinates: each thread stages one k of A_PER pixels and of B_PER channels
     const int ka = tid % KC;
     int pos_off[A_PER];
 #pragma unroll
     for (int i = 0; i < A_PER; ++i) {
-        int pl = tid / KC + i * (NT / KC);
-        int pg = p0 + pl;
+        const int pg = p0 + tid / KC + i * (NT / KC);
         if (pg < p.P) {
-            int ho = (int)fdiv((uint32_t)pg, p.div_Wo);
-            int wo = pg - ho * p.W_o;
+            const int ho = (int)fdiv((uint32_t)pg, p.div_Wo);
+            const int wo = pg - ho * p.W_o;
             pos_off[i] = FROM_X ? (ho * p.s_h * p.W_i + wo * p.s_w) : (ho * p.L + wo * p.S);
         } else {
             pos_off[i] = -1;
         }
     }
-    const int kb = tid % KC;
-    int co_b[B_PER];
-#pragma unroll
-    for (int i = 0; i < B_PER; ++i) co_b[i] = tid / KC + i * (NT / KC);
 
-    // ---- compute coordinates
-    const int warp = tid >> 5, lane = tid & 31;
-    const int ty = (warp >> 2) * 4 + (lane >> 3);  // channel group: 8 channels
-    const int tx = (warp & 3) * 8 + (lane & 7);     // pixel group: 4 pixels
-
-    float acc[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
-    float ra[A_PER], rb[B_PER];
-    auto load_chunk = [&](int kc0) {
-        const int kg = kc0 + ka;
+    auto issue_chunk = [&](int c) {
+        const int buf = c % STAGES;
+        const int kg = c * KC + ka;
         int coff = -1;
         if (kg < p.K) {
-            int ci = (int)fdiv((uint32_t)kg, p.div_KK);
-            int kk = kg - ci * p.KK;
+            const int ci = (int)fdiv((uint32_t)kg, p.div_KK);
+            const int kk = kg - ci * p.KK;
             if (FROM_X) {
-                int j = (int)fdiv((uint32_t)kk, p.div_Hf);
-                int r = kk - j * p.H_f;
+                const int j = (int)fdiv((uint32_t)kk, p.div_Hf);
+                const int r = kk - j * p.H_f;
                 coff = (ci * p.H_i + r) * p.W_i + j;
             } else {
                 coff = ci * p.H_o * p.L + kk;
             }
         }
 #pragma unroll
-        for (int i = 0; i < A_PER; ++i)
-            ra[i] = (coff >= 0 && pos_off[i] >= 0) ? __ldg(src + pos_off[i] + coff) : 0.f;
-        const int kgb = kc0 + kb;
+        for (int i = 0; i < A_PER; ++i) {
+            const bool v = coff >= 0 && pos_off[i] >= 0;
+            cp_async4(smem_addr(&As[buf][ka][tid / KC + i * (NT / KC)]), v ? src + pos_off[i] + coff : src,
+                      v ? 4u : 0u);
+        }
 #pragma unroll
         for (int i = 0; i < B_PER; ++i) {
-            int co = co0 + co_b[i];
-            rb[i] = (kgb < p.K && co < p.C_o) ? __ldg(filt + (int64_t)co * p.K + kgb) : 0.f;
+            const int co = co0 + tid / KC + i * (NT / KC);
+            const bool v = kg < p.K && co < p.C_o;
+            cp_async4(smem_addr(&Bs[buf][ka][tid / KC + i * (NT / KC)]), v ? filt + (int64_t)co * p.K + kg : filt,
+                      v ? 4u : 0u);
         }
     };
-    auto store_chunk = [&](int buf) {
+
+    // ---- compute coordinates: warps of 4 channel groups x 8 pixel groups
+    const int warp = tid >> 5, lane = tid & 31;
+    const int ty = (warp >> 1) * 4 + (lane >> 3);  // channel group (8 channels)
+    const int tx = (warp & 1) * 8 + (lane & 7);     // pixel group (2 x 4 pixels)
+
+    float acc[8][8];
 #pragma unroll
-        for (int i = 0; i < A_PER; ++i) As[buf][ka][tid / KC + i * (NT / KC)] = ra[i];
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int i = 0; i < B_PER; ++i) Bs[buf][kb][co_b[i]] = rb[i];
-    };
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
     const int nchunks = (p.K + KC - 1) / KC;
-    load_chunk(0);
-    store_chunk(0);
-    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < STAGES - 1; ++c) {
+        if (c < nchunks) issue_chunk(c);
+        cp_async_commit();
+    }
     for (int c = 0; c < nchunks; ++c) {
-        const int buf = c & 1;
-        if (c + 1 < nchunks) load_chunk((c + 1) * KC);
+        cp_async_wait<STAGES - 2>();  // chunk c has landed (this thread's copies)
+        __syncthreads();              // ... and every thread's; chunk c-1's buffer is free
+        if (c + STAGES - 1 < nchunks) issue_chunk(c + STAGES - 1);
+        cp_async_commit();
+        const int buf = c % STAGES;
 #pragma unroll
         for (int k = 0; k < KC; ++k) {
-            const float4 a = *reinterpret_cast<const float4 *>(&As[buf][k][tx * 4]);
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][k][tx * 4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][k][64 + tx * 4]);
             const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8]);
             const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8 + 4]);
-            const float av[4] = {a.x, a.y, a.z, a.w};
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(bv[i], av[j], acc[i][j]);
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(bv[i], av[j], acc[i][j]);
         }
-        if (c + 1 < nchunks) store_chunk(buf ^ 1);
-        __syncthreads();
     }
+    cp_async_wait<0>();
 
     // ---- epilogue: out[n][co][p]
 #pragma unroll
@@ -151,11 +168,16 @@ __global__ void __launch_bounds__(TM * 4) conv_f32_kernel(F32Params p) {
         if (co >= p.C_o) continue;
         float *orow = p.out + ((int64_t)n * p.C_o + co) * p.P;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int pg = p0 + tx * 4 + j;
+        for (int j = 0; j < 8; ++j) {
+            const int pg = p0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
             if (pg < p.P) orow[pg] = acc[i][j];
         }
     }
+}
+
+template <int TM, int KC>
+constexpr size_t f32_smem_bytes() {
+    return (size_t)3 * KC * ((TP + 4) + (TM + 4)) * sizeof(float);
 }
 
 // filt'[co][ci*KK + j*H_f + r] = filt[co][ci][r][j]; block 0 also clears the
@@ -174,10 +196,14 @@ __global__ void relayout_filter_f32(const float *__restrict__ filt, float *__res
     }
 }
 
-template <int TM, bool FROM_X>
+template <int TM, int KC, bool FROM_X>
 cudaError_t launch_tm(const F32Params &p, int N, cudaStream_t st) {
     dim3 grid((unsigned)(p.pos_tiles * N), (unsigned)((p.C_o + TM - 1) / TM));
-    conv_f32_kernel<TM, FROM_X><<<grid, TM * 4, 0, st>>>(p);
+    constexpr size_t smem = f32_smem_bytes<TM, KC>();
+    cudaError_t e = cudaFuncSetAttribute(conv_f32_kernel<TM, KC, FROM_X>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    conv_f32_kernel<TM, KC, FROM_X><<<grid, TM * 2, smem, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -233,19 +259,21 @@ cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *
     // channel tile with the least padding (ties: the larger tile)
     int best = 128;
     int64_t best_pad = (s.C_o + 127) / 128 * 128 - s.C_o;
-    for (int tm : {64, 32}) {
-        int64_t pad = (s.C_o + tm - 1) / tm * tm - s.C_o;
+    for (int tm : {96, 64, 32}) {
+        const int64_t pad = (s.C_o + tm - 1) / tm * tm - s.C_o;
         if (pad < best_pad) { best = tm; best_pad = pad; }
     }
     const int N = (int)s.N;
     if (from_x) {
-        if (best == 128) return launch_tm<128, true>(p, N, st);
-        if (best == 64) return launch_tm<64, true>(p, N, st);
-        return launch_tm<32, true>(p, N, st);
+        if (best == 128) return launch_tm<128, 16, true>(p, N, st);
+        if (best == 96) return launch_tm<96, 24, true>(p, N, st);
+        if (best == 64) return launch_tm<64, 16, true>(p, N, st);
+        return launch_tm<32, 16, true>(p, N, st);
     }
-    if (best == 128) return launch_tm<128, false>(p, N, st);
-    if (best == 64) return launch_tm<64, false>(p, N, st);
-    return launch_tm<32, false>(p, N, st);
+    if (best == 128) return launch_tm<128, 16, false>(p, N, st);
+    if (best == 96) return launch_tm<96, 24, false>(p, N, st);
+    if (best == 64) return launch_tm<64, 16, false>(p, N, st);
+    return launch_tm<32, 16, false>(p, N, st);
 }
 
 }  // namespace im2win
