@@ -133,6 +133,34 @@ const char *im2win_status_string(int status);
  */
 im2win_status im2win_device_status(const void *ws, size_t ws_bytes, void *stream);
 
+/* Size of the scratch array built into the library for im2win_conv_fused_noalloc. */
+#define IM2WIN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * im2win_conv_fused for callers that cannot allocate a workspace. The pages
+ * have no counterpart to this call: it exists for callers that only hold the
+ * input and output buffers -- a plugin slot that is handed tensor pointers and
+ * nothing else, or code that must not call cudaMalloc because it may
+ * synchronise the device. Same arguments and result as im2win_conv_fused,
+ * minus ws/ws_bytes: the scratch lives in one array of
+ * IM2WIN_NOALLOC_SCRATCH_BYTES compiled into the library (device memory of
+ * every GPU that loads it, held until the process exits). A problem whose
+ * fused workspace (im2win_workspace_size(IM2WIN_OP_CONV_FUSED, ...)) exceeds
+ * that size is rejected with IM2WIN_ERR_WORKSPACE before any work is queued.
+ * The first call on a device, with that device current, looks up the array's
+ * device address (cudaGetSymbolAddress); make it before any stream capture.
+ * All calls share the array and it keeps the last call's contents (each call
+ * re-lays the filter and clears the status word itself): calls whose work can
+ * overlap on the GPU race and may return wrong results. Calls no cudaMalloc,
+ * cudaFree or other allocating routine. An in-kernel wait that gives up is
+ * recorded in the shared array, which im2win_device_status cannot read; use
+ * im2win_conv_fused with a workspace when that check is needed.
+ */
+im2win_status im2win_conv_fused_noalloc(const void *x, const void *filt, void *out, int64_t N,
+                                        int64_t C_i, int64_t H_i, int64_t W_i, int64_t C_o,
+                                        int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w,
+                                        int dtype, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

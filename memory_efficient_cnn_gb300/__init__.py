@@ -9,6 +9,7 @@ a fused variant that never writes the window tensor. This package is the thin
 Python binding over it.
 """
 from ._binding import (  # noqa: F401
-    BF16, EXPORTS, F16, F32, OP_CONV, OP_CONV_FUSED, OP_TRANSFORM, Im2winError, conv, conv_fused,
-    im2win_conv, im2win_conv_fused, im2win_device_status, im2win_status_string, im2win_transform,
+    BF16, EXPORTS, F16, F32, NOALLOC_SCRATCH_BYTES, OP_CONV, OP_CONV_FUSED, OP_TRANSFORM, Im2winError,
+    conv, conv_fused, im2win_conv, im2win_conv_fused, im2win_conv_fused_noalloc, im2win_device_status,
+    im2win_status_string, im2win_transform,
     im2win_workspace_size, lib, library_path, out_hw, status_string, transform, workspace)

@@ -22,7 +22,8 @@ F32, F16, BF16 = 0, 1, 2
 _DTYPE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 
 EXPORTS = ("im2win_workspace_size", "im2win_transform", "im2win_conv", "im2win_conv_fused",
-           "im2win_status_string", "im2win_device_status")
+           "im2win_status_string", "im2win_device_status", "im2win_conv_fused_noalloc")
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -58,8 +59,9 @@ def lib() -> ctypes.CDLL:
             L.im2win_status_string.argtypes = [ctypes.c_int]
             L.im2win_status_string.restype = ctypes.c_char_p
             L.im2win_device_status.argtypes = [vp, sz, vp]
+            L.im2win_conv_fused_noalloc.argtypes = [vp, vp, vp] + shp + [ctypes.c_int, vp]
             for f in ("im2win_workspace_size", "im2win_transform", "im2win_conv",
-                      "im2win_conv_fused", "im2win_device_status"):
+                      "im2win_conv_fused", "im2win_device_status", "im2win_conv_fused_noalloc"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -145,6 +147,20 @@ def im2win_conv_fused(x: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws
            lib().im2win_conv_fused(x.data_ptr(), filt.data_ptr(), out.data_ptr(), ws.data_ptr(),
                                    ws.numel() * ws.element_size(), N, C_i, H_i, W_i, C_o, H_f,
                                    W_f, s_h, s_w, _dtype_code(x), _stream(x)))
+
+
+def im2win_conv_fused_noalloc(x: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, s_h, s_w) -> None:
+    """Fused convolution for callers that cannot allocate a workspace: the
+    scratch is the library's built-in array (see include/im2win.h)."""
+    _cuda(x, filt, out)
+    if not (x.dtype == filt.dtype == out.dtype):
+        raise TypeError("x, filt and out must share a dtype")
+    N, C_i, H_i, W_i = x.shape
+    C_o, _, H_f, W_f = filt.shape
+    _check("im2win_conv_fused_noalloc",
+           lib().im2win_conv_fused_noalloc(x.data_ptr(), filt.data_ptr(), out.data_ptr(), N, C_i,
+                                           H_i, W_i, C_o, H_f, W_f, s_h, s_w, _dtype_code(x),
+                                           _stream(x)))
 
 
 def im2win_device_status(ws: torch.Tensor) -> int:
