@@ -30,6 +30,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -122,58 +124,71 @@ def conv_flops(layer) -> float:
     return 2.0 * layer.N * layer.C_o * ho * wo * layer.C_i * layer.H_f * layer.W_f
 
 
-def cpu_oracle_rate(layer, budget_s: float, max_images: int | None = None):
-    """The oracle as it stands (fp64 direct conv) on the first images of the
-    batch, fp16-rounded inputs then fp32 inputs, until `budget_s` is spent."""
-    import oracle
-    from memory_efficient_cnn_gb300 import workloads as wl
+def workload_str(layer) -> str:
+    return (f"{layer.name}: N={layer.N}, C_i={layer.C_i}, {layer.H_i}x{layer.W_i}, C_o={layer.C_o}, "
+            f"{layer.H_f}x{layer.W_f}, stride {layer.s_h}x{layer.s_w}; {' and '.join(layer.dtypes)}")
 
-    oracle.build()
-    d_lo, d_hi = layer.dtypes[0], layer.dtypes[-1]
-    x16, w16 = wl.make_inputs(layer, d_lo, n_images=8)
-    x32, w32 = wl.make_inputs(layer, d_hi, n_images=8)
-    per_img = conv_flops(layer) / layer.N
-    done_imgs, t_total = 0, 0.0
-    limit = max_images if max_images is not None else 10 ** 9
-    i = 0
-    while (t_total < budget_s or done_imgs == 0) and done_imgs < limit:
-        x, w = (x16, w16) if i % 2 == 0 else (x32, w32)
-        n = (i // 2) % x.shape[0]
-        xd, wd = x[n:n + 1].double().numpy(), w.double().numpy()
-        t0 = time.perf_counter()
-        oracle.im2win(xd, layer.H_f, layer.s_h)
-        oracle.conv_direct(xd, wd, (layer.s_h, layer.s_w))
-        t_total += time.perf_counter() - t0
-        done_imgs += 1
-        i += 1
-    return per_img * done_imgs / t_total / 1e12, done_imgs, t_total, oracle.num_threads()
+
+class OracleSampler:
+    """The oracle as it stands (im2win transform + fp64 direct conv), one image
+    at a time on the leading images of the batch, the layer's dtypes alternating
+    (each rounded to its dtype, then widened exactly). Inputs are drawn once."""
+
+    def __init__(self, layer, n_images=8):
+        import oracle
+        from memory_efficient_cnn_gb300 import workloads as wl
+
+        oracle.build()
+        self.oracle, self.layer = oracle, layer
+        self.inputs = []
+        for d in layer.dtypes:
+            x, w = wl.make_inputs(layer, d, n_images=n_images)
+            self.inputs.append((x.double().numpy(), w.double().numpy()))
+        self.i = 0
+        self.per_img = conv_flops(layer) / layer.N
+
+    def run(self, budget_s: float, max_images: int):
+        """Images until `budget_s` of oracle time is spent (at least one)."""
+        L, done, t_total = self.layer, 0, 0.0
+        while (t_total < budget_s or done == 0) and done < max_images:
+            x, w = self.inputs[self.i % len(self.inputs)]
+            n = (self.i // len(self.inputs)) % x.shape[0]
+            xd = np.ascontiguousarray(x[n:n + 1])
+            t0 = time.perf_counter()
+            self.oracle.im2win(xd, L.H_f, L.s_h)
+            self.oracle.conv_direct(xd, w, (L.s_h, L.s_w))
+            t_total += time.perf_counter() - t0
+            done += 1
+            self.i += 1
+        return done, t_total
+
+    def threads(self) -> int:
+        return self.oracle.num_threads()
 
 
 def run_reference(args, layer, rank, world):
     if rank != 0:
         return
     # each step: the oracle on a bounded sample of images of the workload
+    smp = OracleSampler(layer)
     steps = []
-    threads = 1
     for s in range(args.warmup + args.steps):
-        rate, imgs, t, threads = cpu_oracle_rate(layer, budget_s=0.0, max_images=2)
+        imgs, t = smp.run(budget_s=0.5, max_images=32)
         if s >= args.warmup:
-            steps.append((rate, imgs, t))
-    flops = conv_flops(layer) / layer.N
-    tot_t = sum(t for _, _, t in steps)
-    tot_imgs = sum(i for _, i, _ in steps)
-    value = flops * tot_imgs / tot_t / 1e12
-    sample = (f"{tot_imgs // len(steps)} images of {layer.name} per step (im2win transform + fp64 "
-              f"direct conv; fp16-rounded and fp32 inputs alternate)")
+            steps.append((imgs, t))
+    tot_t = sum(t for _, t in steps)
+    tot_imgs = sum(i for i, _ in steps)
+    value = smp.per_img * tot_imgs / tot_t / 1e12
+    sample = (f"{tot_imgs / len(steps):.1f} images of {layer.name} per step on average (im2win "
+              f"transform + fp64 direct conv per image; {'/'.join(layer.dtypes)}-rounded inputs "
+              f"alternate), a step ends after 32 images or 0.5 s of oracle time")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / len(steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{layer.name}: N={layer.N}, C_i={layer.C_i}, {layer.H_i}x{layer.W_i}, "
-                               f"C_o={layer.C_o}, {layer.H_f}x{layer.W_f}, stride {layer.s_h}",
-                   "sample": sample},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+        "config": {"workload": workload_str(layer), "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": smp.threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -221,8 +236,10 @@ def main():
     # cpu baseline first (rank 0, N=1 only): before any other GPU work is queued
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
-        rate, imgs, t, threads = cpu_oracle_rate(layer, args.cpu_budget)
-        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+        smp = OracleSampler(layer)
+        imgs, t = smp.run(budget_s=args.cpu_budget, max_images=10 ** 9)
+        cpu = {"value": smp.per_img * imgs / t / 1e12, "unit": UNIT, "cores": smp.threads(),
+               "kind": "oracle",
                "sample": f"{imgs} images of {layer.name} (im2win transform + fp64 direct conv of the "
                          f"{'/'.join(layer.dtypes)} inputs, alternating), {t:.1f} s"}
 
@@ -376,8 +393,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "+".join(layer.dtypes), "data": "synthetic",
-        "config": {"workload": f"{layer.name}: N={N}, C_i={C_i}, {H_i}x{W_i}, C_o={C_o}, "
-                               f"{H_f}x{W_f}, stride {s_h}x{s_w}; {' and '.join(layer.dtypes)}",
+        "config": {"workload": workload_str(layer),
                    "step": ", ".join(names),
                    "parallelism": f"replicas x{world}", "l2": "flushed between steps (512 MB write)"},
         "roofline": {"kernel": dom, "bound": dk["bound"], "achieved": dk["achieved"],

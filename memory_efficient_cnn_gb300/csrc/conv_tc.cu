@@ -376,29 +376,6 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// 8 consecutive 16-bit elements starting at element o of `base` (2-byte aligned),
-// from the two aligned 16-byte vectors that cover them.
-__device__ __forceinline__ uint4 load8_unaligned(const uint16_t *base, int64_t o) {
-    const int64_t vi = o >> 3;
-    const uint4 v0 = __ldg(reinterpret_cast<const uint4 *>(base) + vi);
-    const uint4 v1 = __ldg(reinterpret_cast<const uint4 *>(base) + vi + 1);
-    const int sh = (int)(o & 7);           // element shift 0..7
-    const int q = sh >> 1;                 // word shift 0..3
-    uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint32_t u[5];
-#pragma unroll
-    for (int m = 0; m < 5; ++m) {
-        uint32_t t = w[m];
-        t = (q == 1) ? w[m + 1] : t;
-        t = (q == 2) ? w[m + 2] : t;
-        t = (q == 3) ? w[(m + 3) & 7] : t;
-        u[m] = t;
-    }
-    const uint32_t sel = (sh & 1) ? 0x5432u : 0x3210u;
-    return make_uint4(__byte_perm(u[0], u[1], sel), __byte_perm(u[1], u[2], sel),
-                      __byte_perm(u[2], u[3], sel), __byte_perm(u[3], u[4], sel));
-}
-
 // Persistent: one CTA per SM, each owning an equal share of the output rows.
 // Warp 0 issues the MMAs, warp 1 streams filter tiles, warps 2..9 fill the
 // slabs and warps 10..17 drain the accumulators, so the epilogue of one tile
