@@ -395,10 +395,10 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     const int nb = 2 * p.AST + 2 * p.BST + 3;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + nb);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
-    uint32_t *toff = reinterpret_cast<uint32_t *>(bars + nb + 1);  // [T] tap offsets
+    uint32_t *toff = reinterpret_cast<uint32_t *>(bars + nb + 1);  // [T] tap offsets (16-byte units)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int t = threadIdx.x; t < p.T; t += blockDim.x) toff[t] = tap_offset<MODE>(p, t);
+    for (int t = threadIdx.x; t < p.T; t += blockDim.x) toff[t] = tap_offset<MODE>(p, t) >> 4;  // 16-byte units
 
     auto full_a = [&](int s) { return smem_u32(bars + s); };
     auto empty_a = [&](int s) { return smem_u32(bars + p.AST + s); };
@@ -432,13 +432,25 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
     const Ctl ctl{reinterpret_cast<volatile int *>(abort_word), p.status};
+    // the filter tiles and the cleared status word come from the re-layout kernel
+    grid_dependency_wait();
 
     if (warp == 0) {
         // ---------------- MMA issuer
+        // One thread issues every MMA, so its own instruction latency bounds the
+        // MMA rate: stage indices and phases are ring counters, descriptors are
+        // built in 32-bit halves from tap offsets pre-shifted to 16-byte units,
+        // and the next tap's offset is loaded while the current tap issues.
         if (lane == 0) {
             bool ok = true;
-            int gb = 0, ga = 0, k = 0;
+            int k = 0;
+            int sb = 0, sa = 0;
+            uint32_t phb = 0, pha = 0;
             const uint64_t adesc0 = smem_desc(0, 128, 256), bdesc0 = smem_desc(0, p.lbo, 128);
+            const uint32_t a_hi = (uint32_t)(adesc0 >> 32), b_hi = (uint32_t)(bdesc0 >> 32);
+            const uint32_t a_lo_base = (uint32_t)adesc0 + (smem_u32(sA) >> 4);
+            const uint32_t b_lo_base = (uint32_t)bdesc0 + (smem_u32(sB) >> 4);
+            const uint32_t a_stage16 = a_stage >> 4, b_stage16 = p.stage_b >> 4;
             TapTile tl;
             for (int64_t id = blockIdx.x; ok && id < p.tiles_total; id += gridDim.x) {
                 tile_at(p, id, tl);
@@ -451,26 +463,31 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 const int N0 = split_n0(NTp), N1 = NTp - N0;
                 const uint32_t idesc0 = make_idesc(p.bf16 != 0, BM, N0);
                 const uint32_t idesc1 = make_idesc(p.bf16 != 0, BM, N1 > 0 ? N1 : 16);
-                for (int cc = 0; cc < p.NCH && ok; ++cc, ++gb) {
-                    const int sb = gb % p.BST;
-                    if (!(ok = bar_wait(full_b(sb), (gb / p.BST) & 1, ctl, SITE_FULL_B))) break;
-                    const uint32_t slab = smem_u32(sB + (size_t)sb * p.stage_b);
-                    for (int tg = 0; tg < p.ntg && ok; ++tg, ++ga) {
-                        const int sa = ga % p.AST;
-                        if (!(ok = bar_wait(full_a(sa), (ga / p.AST) & 1, ctl, SITE_FULL_A))) break;
+                for (int cc = 0; cc < p.NCH && ok; ++cc) {
+                    if (!(ok = bar_wait(full_b(sb), phb, ctl, SITE_FULL_B))) break;
+                    const uint32_t b_lo_slab = b_lo_base + (uint32_t)sb * b_stage16;
+                    for (int t0 = 0; t0 < p.T && ok; t0 += p.TG) {
+                        if (!(ok = bar_wait(full_a(sa), pha, ctl, SITE_FULL_A))) break;
                         tc_fence_after();
-                        const int t0 = tg * p.TG;
                         const int t_end = min(p.T, t0 + p.TG);
-                        uint64_t ad = adesc0 + ((uint64_t)((smem_u32(sA + (size_t)sa * a_stage) & 0x3FFFFu) >> 4));
-                        for (int t = t0; t < t_end; ++t, ad += TAP_A_BYTES >> 4) {
-                            const uint64_t bd = bdesc0 + (uint64_t)(((slab + toff[t]) & 0x3FFFFu) >> 4);
+                        uint32_t a_lo = a_lo_base + (uint32_t)sa * a_stage16;
+                        uint32_t off = toff[t0];
+                        for (int t = t0; t < t_end; ++t, a_lo += TAP_A_BYTES >> 4) {
+                            const uint32_t off_next = toff[t + 1 < t_end ? t + 1 : t];
+                            const uint64_t ad = ((uint64_t)a_hi << 32) | a_lo;
+                            const uint32_t b_lo = b_lo_slab + off;
+                            const uint64_t bd0 = ((uint64_t)b_hi << 32) | b_lo;
+                            const uint64_t bd1 = ((uint64_t)b_hi << 32) | (b_lo + (uint32_t)N0);
                             const uint32_t acc = (cc | t) != 0;
-                            mma_f16(tmem, ad, bd, idesc0, acc);
-                            if (N1 > 0) mma_f16(tmem + N0, ad, bd + (uint64_t)N0, idesc1, acc);
+                            mma_f16(tmem, ad, bd0, idesc0, acc);
+                            if (N1 > 0) mma_f16(tmem + N0, ad, bd1, idesc1, acc);
+                            off = off_next;
                         }
                         mma_commit(empty_a(sa));
+                        if (++sa == p.AST) { sa = 0; pha ^= 1; }
                     }
                     if (ok) mma_commit(empty_b(sb));
+                    if (++sb == p.BST) { sb = 0; phb ^= 1; }
                 }
                 if (ok) mma_commit(tmem_full);
                 ++k;
@@ -711,42 +728,47 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
 // holds, for output channel mt*128 + g*8 + row and K index k = h*8 + e of tap t:
 //   TAP_CH: filt[co][cc*16 + k][r][j] with t = r*W_f + j;
 //   TAP_W*: filt[co][cc][r][a*s_w + jl] with t = a*U + u, b = 16u + k = jl*H_f + r (b < S);
-// zero outside the filter. Block 0 also clears the status word.
+// zero outside the filter. With win_hf > 0 (TAP_CH over the window tensor, see
+// window_as_input) tap t is window offset k = t of the re-laid filter
+// filt'[co][ci][k] = filt[co][ci][k % H_f][k / H_f], H_f = win_hf.
+// Block 0 also clears the status word.
 __global__ void relayout_filter_tap(const uint16_t *__restrict__ filt, uint16_t *__restrict__ fa,
-                                    uint32_t *status, int64_t total, int mode, int C_i, int C_o,
-                                    int H_f, int W_f, int s_w, int T, int NCH, int U, int S) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
+                                    uint32_t *status, int mode, int C_i, int C_o, int H_f, int W_f,
+                                    int s_w, int T, int NCH, int U, int S, int win_hf, int n_chunks) {
+    allow_dependents();  // the tap kernel may start its prologue meanwhile
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
         status[0] = 0;
         status[1] = 0;
         status[2] = 0;
     }
-    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int e = (int)(idx & 7), rw = (int)((idx >> 3) & 7), h = (int)((idx >> 6) & 1),
-                  g = (int)((idx >> 7) & 15);
-        const int64_t rest = idx >> 11;
-        const int t = (int)(rest % T);
-        const int64_t rest2 = rest / T;
-        const int cc = (int)(rest2 % NCH);
-        const int mt = (int)(rest2 / NCH);
-        const int co = mt * BM + g * 8 + rw;
-        const int k = h * 8 + e;
-        uint16_t v = 0;
-        if (co < C_o) {
-            if (mode == TAP_CH) {
-                const int ci = cc * 16 + k;
-                if (ci < C_i) v = filt[((int64_t)co * C_i + ci) * H_f * W_f + t];
-            } else {
-                const int a = t / U, u = t - a * U;
-                const int b = 16 * u + k;
-                if (b < S) {
-                    const int jl = b / H_f, r = b - jl * H_f;
-                    const int j = a * s_w + jl;
-                    if (j < W_f) v = filt[(((int64_t)co * C_i + cc) * H_f + r) * W_f + j];
+    const int per_chunk = T * (TAP_A_BYTES / 2);  // elements of one (mt, cc) chunk: T taps x 2048
+    const int HW = H_f * W_f;
+    for (int chunk = blockIdx.y; chunk < n_chunks; chunk += gridDim.y) {
+        const int cc = chunk % NCH, mt = chunk / NCH;
+        uint16_t *dst = fa + (int64_t)chunk * per_chunk;
+        for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < per_chunk; idx += gridDim.x * blockDim.x) {
+            const int e = idx & 7, rw = (idx >> 3) & 7, h = (idx >> 6) & 1, g = (idx >> 7) & 15;
+            const int t = idx >> 11;
+            const int co = mt * BM + g * 8 + rw;
+            const int k = h * 8 + e;
+            uint16_t v = 0;
+            if (co < C_o) {
+                if (mode == TAP_CH) {
+                    const int ci = cc * 16 + k;
+                    const int ts = win_hf > 0 ? (t % win_hf) * (T / win_hf) + t / win_hf : t;
+                    if (ci < C_i) v = filt[((int64_t)co * C_i + ci) * HW + ts];
+                } else {
+                    const int a = t / U, u = t - a * U;
+                    const int b = 16 * u + k;
+                    if (b < S) {
+                        const int jl = b / H_f, r = b - jl * H_f;
+                        const int j = a * s_w + jl;
+                        if (j < W_f) v = filt[(((int64_t)co * C_i + cc) * H_f + r) * W_f + j];
+                    }
                 }
             }
+            dst[idx] = v;
         }
-        fa[idx] = v;
     }
 }
 
@@ -757,6 +779,7 @@ struct TapPlan {
     size_t smem;
     int mtiles;
     int64_t kslots;        // MMA K values per output pixel (cost model)
+    int win_hf;            // > 0: TAP_CH over the window tensor (filter taps permuted)
 };
 
 static int sm_count() {
@@ -910,17 +933,39 @@ ExpandGeom expand_geom(const Shape &s) {
 
 }  // namespace
 
-// Kernel choice. Fused: the tap kernel over channels or over window rows,
-// whichever needs fewer MMA K values per pixel; from the window tensor: the
-// window-row tap kernel. Either falls back to the expand kernel when its K
-// padding costs more than half again the expand kernel's K.
+// The convolution from the window tensor is itself a valid convolution: each
+// window row win[n][ci][ho][:] (W_i*H_f elements) is an input row, the filter is
+// the re-laid filter as one row of W_f*H_f taps, and output pixel wo starts at
+// window offset wo*s_w*H_f (the dot product of the im2win convolution). So the
+// window tensor is an input of H_o x W_i*H_f, filtered by 1 x W_f*H_f at stride
+// (1, s_w*H_f); the output extents are unchanged.
+static Shape window_as_input(const Shape &s) {
+    Shape v = s;
+    v.H_i = s.H_o;
+    v.W_i = s.W_i * s.H_f;
+    v.H_f = 1;
+    v.W_f = s.W_f * s.H_f;
+    v.s_h = 1;
+    v.s_w = s.s_w * s.H_f;
+    return v;
+}
+
+// Kernel choice: among the tap kernels that apply -- fused: over channels
+// (TAP_CH) or over window rows (TAP_WX); from the window tensor: over channels
+// of the window tensor seen as an input (window_as_input) or over window rows
+// (TAP_WW) -- the one that needs the fewest MMA K values per pixel. It falls back
+// to the expand kernel when its K padding costs more than half again the expand
+// kernel's K.
 static TapPlan choose_tap(const Shape &s, bool fused, int64_t sms = 148) {
     const int64_t expand_k = s.C_i * ((s.H_f * s.W_f + 7) / 8 * 8);
     TapPlan best{};
     best.ok = false;
     for (int mode : {TAP_CH, TAP_WX, TAP_WW}) {
-        if ((mode == TAP_WW) == fused) continue;
-        TapPlan pl = plan_tap(s, mode, sms);
+        if (fused && mode == TAP_WW) continue;
+        if (!fused && mode == TAP_WX) continue;
+        TapPlan pl = (!fused && mode == TAP_CH) ? plan_tap(window_as_input(s), TAP_CH, sms)
+                                                : plan_tap(s, mode, sms);
+        pl.win_hf = (!fused && mode == TAP_CH) ? (int)s.H_f : 0;
         if (pl.ok && (!best.ok || pl.kslots < best.kslots)) best = pl;
     }
     if (best.ok && best.kslots * 2 > expand_k * 3) best.ok = false;
@@ -949,24 +994,38 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
     TapParams p = pl.p;
     uint32_t *status = static_cast<uint32_t *>(ws);
     uint16_t *fa = reinterpret_cast<uint16_t *>(static_cast<unsigned char *>(ws) + kStatusBytes);
-    const int64_t total = (int64_t)pl.mtiles * p.NCH * p.T * (TAP_A_BYTES / 2);
-    relayout_filter_tap<<<(unsigned)std::min<int64_t>((total + 255) / 256, 8192), 256, 0, st>>>(
-        static_cast<const uint16_t *>(filt), fa, status, total, pl.mode, p.C_i, p.C_o, p.H_f, p.W_f,
-        p.s_w, p.T, p.NCH, p.U, p.S);
+    const int n_chunks = pl.mtiles * p.NCH;
+    const int per_chunk = p.T * (int)(TAP_A_BYTES / 2);
+    const dim3 rgrid((unsigned)std::min(std::max(1, (per_chunk + 255) / 256), 64),
+                     (unsigned)std::min(n_chunks, 65535));
+    relayout_filter_tap<<<rgrid, 256, 0, st>>>(static_cast<const uint16_t *>(filt), fa, status, pl.mode, p.C_i,
+                                               p.C_o, p.H_f, p.W_f, p.s_w, p.T, p.NCH, p.U, p.S, pl.win_hf,
+                                               n_chunks);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     p.src = static_cast<const uint16_t *>(src);
     p.fa = fa;
     p.out = static_cast<uint16_t *>(out);
     p.status = status;
-    p.vec = (s.W_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
+    p.vec = (p.W_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
     p.bf16 = bf16 ? 1 : 0;
     const unsigned grid = (unsigned)std::min<int64_t>(sm_count(), p.tiles_total);
     auto go = [&](auto kernel) -> cudaError_t {
         cudaError_t e2 = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
         if (e2 != cudaSuccess) return e2;
-        kernel<<<grid, TAP_THREADS, pl.smem, st>>>(p);
-        return cudaGetLastError();
+        // launched as a programmatic dependent of the re-layout kernel: the prologue
+        // overlaps it, the kernel waits for it before touching its output
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(TAP_THREADS);
+        cfg.dynamicSmemBytes = pl.smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kernel, p);
     };
     if (pl.mode == TAP_CH) return go(conv_tc_tap_kernel<TAP_CH>);
     if (pl.mode == TAP_WX) return go(conv_tc_tap_kernel<TAP_WX>);

@@ -109,6 +109,18 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the previous kernel of the stream has
+// finished; grid_dependency_wait() returns once that kernel has completed and
+// its writes are visible (immediately when launched without the attribute).
+// allow_dependents() lets the next such kernel start launching early.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05): start address, leading- and
 // stride-dimension byte offsets (all >> 4), fixed version bits 46..48 = 1,
 // base offset 0, no swizzle.
@@ -214,19 +226,18 @@ __device__ __forceinline__ void drain_accumulator(uint32_t taddr, int first_blk,
 // 64 columns: two 32-column TMEM loads (the next block's first load is in
 // flight while this block is stored), rounding to fp16/bf16, a transpose
 // through the warp's staging area (32 rows x 33 words), then lane l stores
-// positions 2l and 2l+1 of every row -- one 4-byte store when the two are
-// adjacent in the output and 4-byte aligned, else two 2-byte stores.
-// off_of(col) gives the output element offset of column col within a channel
-// plane (or -1 if the column is not an output); row r of the block lives at
-// out_c + r*row_stride.
+// positions 2l and 2l+1 of every row. off_of(col) gives the output element
+// offset of column col within a channel plane (or -1 if the column is not an
+// output); row r of the block lives at out_c + r*row_stride. When, for every
+// lane, the two positions are adjacent outputs at a 4-byte aligned address in
+// every row, the block is stored as 4-byte pairs; otherwise as 2-byte
+// elements. Either way a lane's row loop is branch-free.
 template <typename OffFn>
 __device__ __forceinline__ void drain_columns(uint32_t taddr, int c_begin, int c_end, uint32_t *stage,
                                               int rows, int64_t row_stride, int bf16,
                                               uint16_t *out_c, OffFn off_of) {
     const int lane = threadIdx.x & 31;
     if (c_begin >= c_end) return;
-    const bool stride_even = (row_stride & 1) == 0;
-    const int64_t base_par = (int64_t)(reinterpret_cast<uintptr_t>(out_c) >> 1);
     uint32_t r[32];
     tmem_ld32(taddr + (uint32_t)c_begin, r);
     for (int c0 = c_begin; c0 < c_end; c0 += 64) {
@@ -243,18 +254,39 @@ __device__ __forceinline__ void drain_columns(uint32_t taddr, int c_begin, int c
         __syncwarp();
         // ---- lane l: positions c0 + 2l, c0 + 2l + 1 of every row
         const int o0 = off_of(c0 + 2 * lane), o1 = off_of(c0 + 2 * lane + 1);
-        const bool pair = o0 >= 0 && o1 == o0 + 1;
+        const bool pair_ok = o0 < 0 || (o1 == o0 + 1 && (reinterpret_cast<uintptr_t>(out_c + o0) & 3) == 0);
+        const bool pairs = (row_stride & 1) == 0 && __all_sync(0xffffffffu, pair_ok);
+        const uint32_t *src = stage + lane;
+        if (pairs) {
+            if (o0 >= 0) {
+                uint32_t *d = reinterpret_cast<uint32_t *>(out_c + o0);
+                const int64_t st = row_stride >> 1;
+                if (rows == 32) {
 #pragma unroll 8
-        for (int row = 0; row < 32; ++row) {
-            if (row >= rows) break;
-            const uint32_t w = stage[row * 33 + lane];
-            uint16_t *d = out_c + (int64_t)row * row_stride;
-            const bool even = (((base_par + (stride_even ? 0 : row)) + o0) & 1) == 0;
-            if (pair && even) {
-                *reinterpret_cast<uint32_t *>(d + o0) = w;
+                    for (int row = 0; row < 32; ++row, d += st) *d = src[row * 33];
+                } else {
+                    for (int row = 0; row < rows; ++row, d += st) *d = src[row * 33];
+                }
+            }
+        } else if (o0 >= 0 || o1 >= 0) {
+            // a lane whose first position is not an output stores through its second
+            // address for both (the store of the missing one is predicated off)
+            uint16_t *d0 = out_c + (o0 >= 0 ? o0 : o1);
+            uint16_t *d1 = out_c + (o1 >= 0 ? o1 : o0);
+            const bool v0 = o0 >= 0, v1 = o1 >= 0;
+            if (rows == 32) {
+#pragma unroll 8
+                for (int row = 0; row < 32; ++row, d0 += row_stride, d1 += row_stride) {
+                    const uint32_t w = src[row * 33];
+                    if (v0) *d0 = (uint16_t)(w & 0xFFFFu);
+                    if (v1) *d1 = (uint16_t)(w >> 16);
+                }
             } else {
-                if (o0 >= 0) d[o0] = (uint16_t)(w & 0xFFFFu);
-                if (o1 >= 0) d[o1] = (uint16_t)(w >> 16);
+                for (int row = 0; row < rows; ++row, d0 += row_stride, d1 += row_stride) {
+                    const uint32_t w = src[row * 33];
+                    if (v0) *d0 = (uint16_t)(w & 0xFFFFu);
+                    if (v1) *d1 = (uint16_t)(w >> 16);
+                }
             }
         }
         __syncwarp();

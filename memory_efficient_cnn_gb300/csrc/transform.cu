@@ -8,39 +8,44 @@
 //
 // The transform is pure data movement and HBM-bound: the window is
 // H_f/s_h times the input. Design:
-//  * one CTA per (plane = n*C_i + ci, band of T output rows); the input rows
-//    of the band form one contiguous range of x, staged once into shared
-//    memory with 16-byte loads (rows shared by neighbouring output rows are
-//    read from HBM once per band);
-//  * the band's window rows are assembled in shared memory: a thread takes one
-//    input column w of one output row and copies its H_f elements (one per
-//    staged row) to window positions w*H_f .. w*H_f + H_f - 1, so consecutive
-//    lanes read consecutive shared-memory elements;
-//  * the band's output is one contiguous range of win; it leaves shared
-//    memory as whole 16-byte vectors (coalesced 128-bit stores), the buffer
-//    being offset so that its vectors line up with the global ones; the
-//    unaligned head and tail are written element by element, so neighbouring
-//    CTAs never overlap.
+//  * a CTA owns a contiguous piece of the work: several whole planes
+//    (plane = n*C_i + ci) when a plane is small, else a band of T output rows
+//    of one plane, else (rows too wide) a column segment of one output row.
+//    The input rows under that piece form one contiguous range of x, staged
+//    once into shared memory with 16-byte loads (rows shared by neighbouring
+//    output rows are read from HBM once per piece);
+//  * the piece's output is one contiguous range of win. Each thread builds
+//    whole 16-byte output vectors, aligned to the global ones, in registers:
+//    it walks the window positions of its vector (window row, column w, row
+//    offset r), gathers each element from the staged rows and stores the
+//    vector straight to win (coalesced 128-bit stores across the warp). The
+//    unaligned head and tail of the range are written element by element, so
+//    neighbouring CTAs never overlap.
 // The element type is the raw bit pattern (uint16_t / uint32_t), so the copy
 // is bit-exact for every dtype.
+#include <algorithm>
+
 #include "im2win_internal.cuh"
 
 namespace im2win {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kSmemBudget = 40 * 1024;  // per CTA (input + output band), 5 CTAs/SM
+constexpr int kSmemBudget = 32 * 1024;  // staged input band per CTA (up to 7 CTAs/SM)
 
 struct TParams {
     const void *x;
     void *win;
     int64_t x_elems;      // total elements of x
+    int64_t n_planes;     // N * C_i
     int64_t H_i, W_i, H_f, s_h, H_o;
     int64_t tiles_per_plane;
-    int T;                // output rows per band
+    int PPC;              // planes per CTA (> 1 only when whole planes fit)
+    int T;                // output rows per band (H_o for whole planes)
+    int RP;               // output rows per staged plane (H_o for whole planes, else T)
     int Wt, ctiles;       // columns per tile and column tiles per band (1 unless a row is too wide)
-    int in_cap;           // elements reserved for the staged input band (multiple of 8)
     uint32_t L;           // W_i * H_f
+    FastDiv div_L, div_Hf, div_RP;
 };
 
 template <typename E>
@@ -48,30 +53,32 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     constexpr int V = 16 / sizeof(E);
     E *s_in = reinterpret_cast<E *>(smem_raw);
-    E *s_out = s_in + p.in_cap;
 
     const E *__restrict__ x = static_cast<const E *>(p.x);
     E *__restrict__ win = static_cast<E *>(p.win);
 
     const int64_t tile_id = blockIdx.x / p.ctiles;
     const int ct = (int)(blockIdx.x - tile_id * p.ctiles);
-    const int64_t plane = tile_id / p.tiles_per_plane;
-    const int64_t tile = tile_id - plane * p.tiles_per_plane;
+    const int64_t group = tile_id / p.tiles_per_plane;
+    const int64_t tile = tile_id - group * p.tiles_per_plane;
+    const int64_t plane0 = group * p.PPC;
+    const int nplanes = (int)min((int64_t)p.PPC, p.n_planes - plane0);
     const int64_t ho0 = tile * p.T;
     const int64_t ho1 = min(ho0 + (int64_t)p.T, p.H_o);
-    const int rows_out = (int)(ho1 - ho0);
+    const int rows_out = (int)(ho1 - ho0);               // output rows per plane of the piece
     const int rows_in = (int)((rows_out - 1) * p.s_h + p.H_f);
     const int W_i = (int)p.W_i, H_f = (int)p.H_f, s_h = (int)p.s_h;
     const int L = (int)p.L;
     const int w0 = ct * p.Wt;
     const int Wc = min(p.Wt, W_i - w0);  // columns of this tile
+    const int plane_in = (int)p.H_i * Wc;  // staged elements between planes (whole planes only)
 
-    // ---- stage the band's input rows (columns [w0, w0 + Wc)) in s_in, row pitch Wc
+    // ---- stage the piece's input rows (columns [w0, w0 + Wc)) in s_in, row pitch Wc
     int lead = 0;
     if (p.ctiles == 1) {
         // whole rows: one contiguous range of x, x[in0, in0 + cnt) -> s_in[lead, lead + cnt)
-        const int64_t in0 = (plane * p.H_i + ho0 * p.s_h) * p.W_i;
-        const int cnt = rows_in * W_i;
+        const int64_t in0 = (plane0 * p.H_i + ho0 * p.s_h) * p.W_i;
+        const int cnt = (nplanes - 1) * plane_in + rows_in * W_i;
         const int64_t base = in0 - (in0 % V);
         lead = (int)(in0 - base);
         const int nvec = (lead + cnt + V - 1) / V;
@@ -95,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
             if (base + e < p.x_elems) s_in[e] = x[base + e];
     } else {
         // a column segment of each input row (rows too wide for one band)
-        const int64_t row0 = (plane * p.H_i + ho0 * p.s_h) * p.W_i + w0;
+        const int64_t row0 = (plane0 * p.H_i + ho0 * p.s_h) * p.W_i + w0;
         for (int e = threadIdx.x; e < rows_in * Wc; e += kThreads) {
             const int lr = e / Wc, c = e - lr * Wc;
             s_in[e] = x[row0 + (int64_t)lr * p.W_i + c];
@@ -103,35 +110,71 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
     }
     __syncthreads();
 
-    // ---- assemble the window rows: s_out[olead + hl*L + (w-w0)*H_f + r] = s_in[lead + (hl*s_h + r)*Wc + w - w0]
-    // (a band of whole rows is one contiguous output range; a column tile is one output row)
-    const int64_t o0 = (plane * p.H_o + ho0) * (int64_t)L + (int64_t)w0 * H_f;
-    const int64_t o1 = o0 + (p.ctiles == 1 ? (int64_t)rows_out * L : (int64_t)Wc * H_f);
-    const int olead = (int)(o0 % V);
+    // ---- write win[o0, o1): the piece's window rows (a column tile: one row segment)
+    const int64_t o0 = (plane0 * p.H_o + ho0) * (int64_t)L + (int64_t)w0 * H_f;
+    const int64_t o1 = o0 + (p.ctiles == 1 ? (int64_t)nplanes * rows_out * L : (int64_t)Wc * H_f);
     const E *sl = s_in + lead;
-    E *so = s_out + olead;
-    const int items = rows_out * Wc;
-    for (int it = threadIdx.x; it < items; it += kThreads) {
-        const int hl = it / Wc;
-        const int w = it - hl * Wc;
-        const E *src = sl + hl * s_h * Wc + w;
-        E *dst = so + hl * L + w * H_f;
-        for (int r = 0; r < H_f; ++r) dst[r] = src[r * Wc];
-    }
-    __syncthreads();
-
-    // ---- write win[o0, o1): aligned 16-byte vectors, ragged head and tail by element
+    const int rstep = s_h * Wc;  // staged elements between consecutive window rows of a plane
+    // staged index of the first element of window row gh of the piece
+    auto row_base = [&](int gh) -> int {
+        const int pl = (int)fdiv((uint32_t)gh, p.div_RP);
+        return pl * plane_in + (gh - pl * p.RP) * rstep;
+    };
+    // position q of the range -> (window row gh, column w, row offset r) and staged index
+    int gh, w, r;
+    auto locate = [&](int q) -> int {
+        gh = p.ctiles == 1 ? (int)fdiv((uint32_t)q, p.div_L) : 0;
+        const int rem = q - gh * L;
+        w = (int)fdiv((uint32_t)rem, p.div_Hf);
+        r = rem - w * H_f;
+        return row_base(gh) + r * Wc + w;
+    };
     int64_t a0 = (o0 + V - 1) / V * V;
     int64_t a1 = o1 / V * V;
     if (a0 > o1) a0 = o1;
     if (a1 < a0) a1 = a0;
     const int head = (int)(a0 - o0), tail = (int)(o1 - a1);
-    if ((int)threadIdx.x < head) win[o0 + threadIdx.x] = so[threadIdx.x];
-    if ((int)threadIdx.x < tail) win[a1 + threadIdx.x] = so[(int)(a1 - o0) + threadIdx.x];
+    if ((int)threadIdx.x < head + tail) {
+        const int q = (int)threadIdx.x < head ? (int)threadIdx.x : (int)(a1 - o0) + (int)threadIdx.x - head;
+        win[o0 + q] = sl[locate(q)];
+    }
     const int nbody = (int)((a1 - a0) / V);
-    const uint4 *sv = reinterpret_cast<const uint4 *>(so + (a0 - o0));  // 16-byte aligned by olead
     uint4 *gv = reinterpret_cast<uint4 *>(win + a0);
-    for (int v = threadIdx.x; v < nbody; v += kThreads) gv[v] = sv[v];
+    const int q_body = (int)(a0 - o0);
+    for (int v = threadIdx.x; v < nbody; v += kThreads) {
+        int idx = locate(q_body + v * V);
+        uint32_t e[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            e[i] = (uint32_t)sl[idx];
+            // next window position: r + 1, else the next column, else the next window row
+            if (++r < H_f) {
+                idx += Wc;
+            } else if (++w < Wc) {
+                r = 0;
+                idx += 1 - (H_f - 1) * Wc;
+            } else if (i + 1 < V) {
+                r = 0;
+                w = 0;
+                idx = row_base(++gh);
+            }
+        }
+        uint4 out;
+        if (V == 8) {
+            out = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16),
+                             e[6] | (e[7] << 16));
+        } else {
+            out = make_uint4(e[0], e[1], e[2], e[3]);
+        }
+        gv[v] = out;
+    }
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
 }
 
 }  // namespace
@@ -139,42 +182,58 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
 cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, cudaStream_t st) {
     if (s.N == 0) return cudaSuccess;
     const int64_t L = s.W_i * s.H_f;
-    // bytes of a band of T output rows of Wt columns: staged input rows + assembled window rows
-    auto band_bytes = [&](int64_t T, int64_t Wt) {
-        const int64_t in_elems = ((T - 1) * s.s_h + s.H_f) * Wt + 16;
-        return (in_elems + 8) / 8 * 8 * esz + (T * Wt * s.H_f + 16) * esz;
-    };
-    int64_t T = 1, Wt = s.W_i;
-    if (band_bytes(1, Wt) > kSmemBudget) {
+    const int64_t NP = s.N * s.C_i;
+    const int64_t full_rows = (s.H_o - 1) * s.s_h + s.H_f;  // input rows a plane's windows use
+    // bytes staged for `planes` whole planes, or for a band of T output rows of Wt columns
+    auto stage_bytes = [&](int64_t elems) { return (elems + 16 + 8) / 8 * 8 * esz; };
+    auto band_bytes = [&](int64_t T, int64_t Wt) { return stage_bytes(((T - 1) * s.s_h + s.H_f) * Wt); };
+    auto planes_bytes = [&](int64_t P) { return stage_bytes((P - 1) * s.H_i * s.W_i + full_rows * s.W_i); };
+    int64_t PPC = 1, T = 1, Wt = s.W_i;
+    const bool whole = planes_bytes(1) <= kSmemBudget;
+    if (whole) {
+        // whole planes per CTA: as many as fit, but no more than ~16 output vectors a thread
+        // and enough CTAs to fill every SM several times
+        T = s.H_o;
+        const int64_t plane_out_vecs = std::max<int64_t>(1, s.H_o * L * esz / 16);
+        const int64_t by_work = std::max<int64_t>(1, 16 * kThreads / plane_out_vecs);
+        const int64_t by_grid = std::max<int64_t>(1, NP / (sm_count() * 8));
+        const int64_t cap = std::min(by_work, by_grid);
+        while (PPC < cap && planes_bytes(PPC + 1) <= kSmemBudget) ++PPC;
+    } else if (band_bytes(1, Wt) > kSmemBudget) {
         // rows too wide: one output row per band, split into column tiles
         while (Wt > 8 && band_bytes(1, Wt) > kSmemBudget) Wt = (Wt + 1) / 2;
     } else {
         while (T < s.H_o && band_bytes(T + 1, Wt) <= kSmemBudget) ++T;
+        // balance the bands of a plane
+        const int64_t tiles = (s.H_o + T - 1) / T;
+        T = (s.H_o + tiles - 1) / tiles;
     }
     const int64_t ctiles = (s.W_i + Wt - 1) / Wt;
-    // balance the bands of a plane
     const int64_t tiles = (s.H_o + T - 1) / T;
-    T = (s.H_o + tiles - 1) / tiles;
-    const int64_t in_elems = ((T - 1) * s.s_h + s.H_f) * Wt + 16;
+    const size_t smem = (size_t)(whole ? planes_bytes(PPC) : band_bytes(T, Wt));
 
     TParams p;
     p.x = x;
     p.win = win;
     p.x_elems = s.N * s.C_i * s.H_i * s.W_i;
+    p.n_planes = NP;
     p.H_i = s.H_i;
     p.W_i = s.W_i;
     p.H_f = s.H_f;
     p.s_h = s.s_h;
     p.H_o = s.H_o;
     p.tiles_per_plane = tiles;
+    p.PPC = (int)PPC;
     p.T = (int)T;
+    p.RP = (int)T;
     p.Wt = (int)Wt;
     p.ctiles = (int)ctiles;
-    p.in_cap = (int)((in_elems + 8) / 8 * 8);
     p.L = (uint32_t)L;
-    const size_t smem = (size_t)band_bytes(T, Wt);
+    p.div_L = make_fastdiv((uint32_t)L);
+    p.div_Hf = make_fastdiv((uint32_t)s.H_f);
+    p.div_RP = make_fastdiv((uint32_t)T);
 
-    const int64_t blocks = s.N * s.C_i * tiles * ctiles;
+    const int64_t blocks = (NP + PPC - 1) / PPC * tiles * ctiles;
     cudaError_t e;
     if (esz == 2) {
         e = cudaFuncSetAttribute(transform_kernel<uint16_t>,
@@ -194,7 +253,7 @@ cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, 
 // (plane, band, column tile).
 bool transform_supported(const Shape &s, int esz) {
     // the narrowest tile (8 columns of one output row) must fit in shared memory
-    const int64_t narrow = ((s.H_f * 8 + 24) + (8 * s.H_f + 16)) * esz;
+    const int64_t narrow = (s.H_f * 8 + 24) * esz;
     return narrow <= 200 * 1024 && s.W_i * s.H_f * s.H_o < (1ll << 31) &&
            s.N * s.C_i * s.H_o * ((s.W_i + 7) / 8) < (1ll << 31);
 }

@@ -31,6 +31,8 @@ CASES = [  # N, C_i, H_i, W_i, H_f, s_h
     (2, 3, 32, 32, 3, 1), (3, 5, 37, 227, 11, 4), (1, 7, 29, 231, 7, 2), (2, 2, 9, 13, 9, 1),
     (1, 3, 40, 5, 1, 1), (2, 4, 50, 17, 3, 5), (1, 1, 300, 3, 2, 1), (5, 3, 24, 24, 5, 1),
     (1, 2, 6, 12000, 3, 2),  # one output row of input exceeds the default band budget
+    # many small planes: several whole planes per CTA, the last group ragged
+    (64, 64, 11, 13, 3, 2), (27, 113, 7, 9, 2, 1),
 ]
 
 
