@@ -29,7 +29,7 @@ constexpr int TP = 128;  // pixels per CTA
 
 struct F32Params {
     const float *src;    // window tensor or NCHW input
-    const float *filt;   // filt' [C_o][K]
+    const float *filt;   // filt' transposed and zero padded: [K_pad][C_o_pad]
     float *out;
     uint32_t *status;
     int C_i, C_o, H_o, W_o, H_i, W_i, H_f, s_h, s_w;
@@ -40,8 +40,12 @@ struct F32Params {
     int L;               // W_i * H_f
     int S;               // s_w * H_f
     int64_t img_src;     // elements of src per image
+    int C_o_pad;         // row length of the transposed filter (a multiple of the channel tile)
     FastDiv div_KK, div_Wo, div_Hf;
 };
+
+// The filter is padded along K to a multiple of every chunk length (16, 24).
+constexpr int K_ALIGN = 48;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -50,6 +54,10 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 __device__ __forceinline__ void cp_async4(uint32_t dst, const float *src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                  : "memory");
+}
+// 16-byte asynchronous copy global -> shared (L2 only).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const float *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -63,9 +71,10 @@ template <int TM, int KC, bool FROM_X>
 __global__ void __launch_bounds__(TM * 2, (TM >= 96 ? 2 : 4)) conv_f32_kernel(F32Params p) {
     constexpr int NT = TM * 2;                 // (TM/8) x 16 threads
     constexpr int A_PER = KC * TP / NT;        // window elements each thread stages
-    constexpr int B_PER = KC * TM / NT;        // filter elements each thread stages
+    constexpr int B_VEC = KC * TM / 4 / NT;    // 16-byte filter vectors each thread stages
     constexpr int STAGES = 3;
-    static_assert(NT % KC == 0 && (KC * TP) % NT == 0 && (KC * TM) % NT == 0, "tile");
+    static_assert(NT % KC == 0 && (KC * TP) % NT == 0 && (KC * TM / 4) % NT == 0, "tile");
+    static_assert(K_ALIGN % KC == 0, "filter padding");
     extern __shared__ __align__(16) float smem_f[];
     float (*As)[KC][TP + 4] = reinterpret_cast<float (*)[KC][TP + 4]>(smem_f);
     float (*Bs)[KC][TM + 4] = reinterpret_cast<float (*)[KC][TM + 4]>(smem_f + STAGES * KC * (TP + 4));
@@ -77,25 +86,32 @@ __global__ void __launch_bounds__(TM * 2, (TM >= 96 ? 2 : 4)) conv_f32_kernel(F3
     const float *__restrict__ src = p.src + (int64_t)n * p.img_src;
     const float *__restrict__ filt = p.filt;
 
-    // ---- staging coordinates: each thread stages one k of A_PER pixels and of B_PER channels
+    // ---- staging coordinates: each thread stages one k of A_PER pixels (4-byte gathers)
+    // and B_VEC 16-byte vectors of the filter slice
     const int ka = tid % KC;
-    int pos_off[A_PER];
+    int pos_off[A_PER];   // offset of the pixel's window segment; pixels past P read offset 0, size 0
+    uint32_t pos_ok = 0;  // bit i: pixel i exists
 #pragma unroll
     for (int i = 0; i < A_PER; ++i) {
         const int pg = p0 + tid / KC + i * (NT / KC);
+        pos_off[i] = 0;
         if (pg < p.P) {
             const int ho = (int)fdiv((uint32_t)pg, p.div_Wo);
             const int wo = pg - ho * p.W_o;
             pos_off[i] = FROM_X ? (ho * p.s_h * p.W_i + wo * p.s_w) : (ho * p.L + wo * p.S);
-        } else {
-            pos_off[i] = -1;
+            pos_ok |= 1u << i;
         }
     }
+    const uint32_t a_dst0 = smem_addr(&As[0][ka][tid / KC]);
+    const uint32_t b_dst0 = smem_addr(&Bs[0][0][0]);
+    constexpr uint32_t A_BUF = KC * (TP + 4) * 4, B_BUF = KC * (TM + 4) * 4;
+    const float *__restrict__ fcol = filt + co0;
 
     auto issue_chunk = [&](int c) {
         const int buf = c % STAGES;
         const int kg = c * KC + ka;
-        int coff = -1;
+        int coff = 0;
+        uint32_t ok = 0;
         if (kg < p.K) {
             const int ci = (int)fdiv((uint32_t)kg, p.div_KK);
             const int kk = kg - ci * p.KK;
@@ -106,19 +122,19 @@ __global__ void __launch_bounds__(TM * 2, (TM >= 96 ? 2 : 4)) conv_f32_kernel(F3
             } else {
                 coff = ci * p.H_o * p.L + kk;
             }
+            ok = pos_ok;
         }
+        const uint32_t a_dst = a_dst0 + buf * A_BUF;
 #pragma unroll
-        for (int i = 0; i < A_PER; ++i) {
-            const bool v = coff >= 0 && pos_off[i] >= 0;
-            cp_async4(smem_addr(&As[buf][ka][tid / KC + i * (NT / KC)]), v ? src + pos_off[i] + coff : src,
-                      v ? 4u : 0u);
-        }
+        for (int i = 0; i < A_PER; ++i)
+            cp_async4(a_dst + i * (NT / KC) * 4, src + (pos_off[i] + coff), ((ok >> i) & 1u) * 4u);
+        // filter rows c*KC .. c*KC + KC - 1, channels co0 .. co0 + TM - 1 (zero padded in memory)
+        const uint32_t b_dst = b_dst0 + buf * B_BUF;
 #pragma unroll
-        for (int i = 0; i < B_PER; ++i) {
-            const int co = co0 + tid / KC + i * (NT / KC);
-            const bool v = kg < p.K && co < p.C_o;
-            cp_async4(smem_addr(&Bs[buf][ka][tid / KC + i * (NT / KC)]), v ? filt + (int64_t)co * p.K + kg : filt,
-                      v ? 4u : 0u);
+        for (int v = 0; v < B_VEC; ++v) {
+            const int q = tid + v * NT;            // vector index in the KC x TM/4 slice
+            const int kr = q / (TM / 4), cv = q - kr * (TM / 4);
+            cp_async16(b_dst + (kr * (TM + 4) + cv * 4) * 4, fcol + (int64_t)(c * KC + kr) * p.C_o_pad + cv * 4);
         }
     };
 
@@ -182,17 +198,23 @@ constexpr size_t f32_smem_bytes() {
 
 // filt'[co][ci*KK + j*H_f + r] = filt[co][ci][r][j]; block 0 also clears the
 // workspace status word for this call.
-__global__ void relayout_filter_f32(const float *__restrict__ filt, float *__restrict__ fp,
-                                    uint32_t *status, int64_t total, int C_i, int H_f, int W_f) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) status[0] = 0;
-    const int64_t KK = (int64_t)H_f * W_f;
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        int64_t j = e % W_f;
-        int64_t t = e / W_f;
-        int64_t r = t % H_f;
-        int64_t cc = t / H_f;  // co*C_i + ci
-        fp[cc * KK + j * H_f + r] = filt[e];
+// fT[k][co] = filt'[co][k] with filt'[co][ci*KK + j*H_f + r] = filt[co][ci][r][j],
+// zero for k >= K or co >= C_o; block 0 also clears the workspace status word
+// for this call.
+__global__ void relayout_filter_f32(const float *__restrict__ filt, float *__restrict__ fT,
+                                    uint32_t *status, int K, int K_pad, int C_o, int C_o_pad, int H_f,
+                                    int W_f) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) status[0] = 0;
+    const int KK = H_f * W_f;
+    for (int k = blockIdx.y; k < K_pad; k += gridDim.y) {
+        int src_k = -1;
+        if (k < K) {
+            const int ci = k / KK, kk = k - ci * KK;
+            const int j = kk / H_f, r = kk - j * H_f;
+            src_k = ci * KK + r * W_f + j;  // index of filt[co][ci][r][j] within filt[co]
+        }
+        for (int co = blockIdx.x * blockDim.x + threadIdx.x; co < C_o_pad; co += gridDim.x * blockDim.x)
+            fT[(int64_t)k * C_o_pad + co] = (src_k >= 0 && co < C_o) ? filt[(int64_t)co * K + src_k] : 0.f;
     }
 }
 
@@ -209,25 +231,48 @@ cudaError_t launch_tm(const F32Params &p, int N, cudaStream_t st) {
 
 }  // namespace
 
+// Channel tile with the least padding (ties: the larger tile).
+static int choose_tm(const Shape &s) {
+    int best = 128;
+    int64_t best_pad = (s.C_o + 127) / 128 * 128 - s.C_o;
+    for (int tm : {96, 64, 32}) {
+        const int64_t pad = (s.C_o + tm - 1) / tm * tm - s.C_o;
+        if (pad < best_pad) { best = tm; best_pad = pad; }
+    }
+    return best;
+}
+
+static int64_t k_pad(const Shape &s) {
+    const int64_t K = s.C_i * s.H_f * s.W_f;
+    return (K + K_ALIGN - 1) / K_ALIGN * K_ALIGN;
+}
+
+static int64_t c_o_pad(const Shape &s) {
+    const int tm = choose_tm(s);
+    return (s.C_o + tm - 1) / tm * tm;
+}
+
 size_t conv_f32_filter_bytes(const Shape &s) {
-    return round_up((size_t)(s.C_o * s.C_i * s.H_f * s.W_f) * 4, 256);
+    return round_up((size_t)(k_pad(s) * c_o_pad(s)) * 4, 256);
 }
 
 bool conv_f32_supported(const Shape &s, bool from_x) {
     const int64_t img = from_x ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * s.W_i * s.H_f;
     const int64_t P = s.H_o * s.W_o;
     const int64_t tiles = (P + TP - 1) / TP;
-    return img < (1ll << 31) && s.C_i * s.H_f * s.W_f < (1ll << 31) && tiles * s.N < (1ll << 31) &&
-           (s.C_o + 31) / 32 < 65536;
+    return img < (1ll << 31) && k_pad(s) < (1ll << 30) && tiles * s.N < (1ll << 31) &&
+           (s.C_o + 31) / 32 < 65536 && k_pad(s) * c_o_pad(s) < (1ll << 40);
 }
 
 cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *ws,
                             const Shape &s, bool from_x, cudaStream_t st) {
     uint32_t *status = static_cast<uint32_t *>(ws);
     float *fp = reinterpret_cast<float *>(static_cast<unsigned char *>(ws) + kStatusBytes);
-    const int64_t total = s.C_o * s.C_i * s.H_f * s.W_f;
-    relayout_filter_f32<<<(unsigned)std::min<int64_t>((total + 255) / 256, 4096), 256, 0, st>>>(
-        static_cast<const float *>(filt), fp, status, total, (int)s.C_i, (int)s.H_f, (int)s.W_f);
+    const int64_t Kp = k_pad(s), Cp = c_o_pad(s);
+    const dim3 rgrid((unsigned)std::min<int64_t>((Cp + 127) / 128, 8), (unsigned)std::min<int64_t>(Kp, 65535));
+    relayout_filter_f32<<<rgrid, 128, 0, st>>>(static_cast<const float *>(filt), fp, status,
+                                               (int)(s.C_i * s.H_f * s.W_f), (int)Kp, (int)s.C_o, (int)Cp,
+                                               (int)s.H_f, (int)s.W_f);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || s.N == 0) return e;
 
@@ -252,17 +297,12 @@ cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *
     p.L = (int)(s.W_i * s.H_f);
     p.S = (int)(s.s_w * s.H_f);
     p.img_src = from_x ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * s.W_i * s.H_f;
+    p.C_o_pad = (int)Cp;
     p.div_KK = make_fastdiv((uint32_t)(s.H_f * s.W_f));
     p.div_Wo = make_fastdiv((uint32_t)s.W_o);
     p.div_Hf = make_fastdiv((uint32_t)s.H_f);
 
-    // channel tile with the least padding (ties: the larger tile)
-    int best = 128;
-    int64_t best_pad = (s.C_o + 127) / 128 * 128 - s.C_o;
-    for (int tm : {96, 64, 32}) {
-        const int64_t pad = (s.C_o + tm - 1) / tm * tm - s.C_o;
-        if (pad < best_pad) { best = tm; best_pad = pad; }
-    }
+    const int best = choose_tm(s);
     const int N = (int)s.N;
     if (from_x) {
         if (best == 128) return launch_tm<128, 16, true>(p, N, st);

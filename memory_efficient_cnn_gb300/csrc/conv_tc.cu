@@ -335,6 +335,7 @@ struct TapParams {
     int BST, AST;          // slab stages, filter stages
     int vec;               // CH: 16-byte row loads possible
     int bf16;
+    FastDiv div_pitch;     // W*: positions -> (output row, column group)
 };
 
 // A tile: output rows [ho0, ho0 + Q) of image n, output channels [mt*128, mt*128 + 128).
@@ -639,37 +640,43 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     //   entry (c, q, m)[e] = window row q of the tile at m*S + 8c + e
                     // TAP_WX: that element is x[cc][(ho0+q)*s_h + r][m*s_w + jl] with 8c + e = jl*H_f + r
                     // TAP_WW: it is read straight from the staged window row
+                    // One K chunk c at a time, so that the 8 source offsets of an entry
+                    // (and which of them exist) stay in registers; per entry one division.
                     const int SC = 2 * p.U;
-                    const int items = SC * Q * p.pitch;
+                    const int per_c = Q * p.pitch;
                     const E16 *raw = sRaw + raw_lead;
-                    for (int it = pt; it < items; it += NPT) {
-                        const int m = it % p.pitch;
-                        const int t2 = it / p.pitch;
-                        const int q = t2 % Q;
-                        const int c = t2 / Q;
-                        uint32_t e16[8];
-                        const int b0 = 8 * c;
-                        if (MODE == TAP_WX) {
-                            int jl = b0 / p.H_f;
-                            int r = b0 - jl * p.H_f;
+                    const int qstride = MODE == TAP_WX ? p.s_h * p.W_i : (int)p.L;
+                    const int mstride = MODE == TAP_WX ? p.s_w : p.S;
+                    for (int c = 0; c < SC; ++c) {
+                        // element e of an entry: raw offset boff[e] from the entry's base, present
+                        // if b = 8c + e < S and its column (WX) / window index (WW) is < lim[e] - m*mstride
+                        int boff[8], lim[8];
+                        int jl = (8 * c) / p.H_f, r = 8 * c - jl * p.H_f;
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int col = m * p.s_w + jl;
-                                const bool v = (b0 + e < p.S) && col < p.W_i;
-                                e16[e] = v ? (uint32_t)raw[(q * p.s_h + r) * p.W_i + col] : 0u;
+                        for (int e = 0; e < 8; ++e) {
+                            const int b = 8 * c + e;
+                            if (MODE == TAP_WX) {
+                                boff[e] = r * p.W_i + jl;
+                                lim[e] = b < p.S ? p.W_i - jl : 0;  // column m*s_w + jl < W_i
                                 if (++r == p.H_f) { r = 0; ++jl; }
-                            }
-                        } else {
-                            const int idx0 = m * p.S + b0;
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const bool v = (b0 + e < p.S) && (idx0 + e < (int)p.L);
-                                e16[e] = v ? (uint32_t)raw[q * (int)p.L + idx0 + e] : 0u;
+                            } else {
+                                boff[e] = b;
+                                lim[e] = b < p.S ? (int)p.L - b : 0;  // window index m*S + b < L
                             }
                         }
-                        *reinterpret_cast<uint4 *>(slab + (size_t)c * p.lbo + (size_t)(q * p.pitch + m) * 16) =
-                            make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
-                                       e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
+                        uint8_t *slab_c = slab + (size_t)c * p.lbo;
+                        for (int i = pt; i < per_c; i += NPT) {
+                            const int q = (int)fdiv((uint32_t)i, p.div_pitch);
+                            const int m = i - q * p.pitch;
+                            const int base = q * qstride + m * mstride;
+                            const int mm = m * mstride;
+                            uint32_t e16[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) e16[e] = mm < lim[e] ? (uint32_t)raw[base + boff[e]] : 0u;
+                            *reinterpret_cast<uint4 *>(slab_c + (size_t)i * 16) =
+                                make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
+                                           e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
+                        }
                     }
                 }
                 if (pok) {
@@ -1008,6 +1015,7 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
     p.out = static_cast<uint16_t *>(out);
     p.status = status;
     p.vec = (p.W_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
+    p.div_pitch = make_fastdiv((uint32_t)p.pitch);
     p.bf16 = bf16 ? 1 : 0;
     const unsigned grid = (unsigned)std::min<int64_t>(sm_count(), p.tiles_total);
     auto go = [&](auto kernel) -> cudaError_t {
