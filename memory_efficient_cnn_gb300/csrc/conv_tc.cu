@@ -305,7 +305,8 @@ enum TapMode { TAP_CH = 0, TAP_WX = 1, TAP_WW = 2 };
 
 constexpr int TAP_PROD_WARPS = 8;
 constexpr int TAP_EPI_WARPS = 8;
-constexpr int TAP_THREADS = (2 + TAP_PROD_WARPS + TAP_EPI_WARPS) * 32;
+constexpr int TAP_ISSUER1_WARP = 2 + TAP_PROD_WARPS + TAP_EPI_WARPS;  // the second MMA issuer
+constexpr int TAP_THREADS = (3 + TAP_PROD_WARPS + TAP_EPI_WARPS) * 32;
 constexpr uint32_t TAP_A_BYTES = BM * 16 * 2;  // one K=16 tap of 128 channels: 4 KB
 constexpr int TAP_MAX_NT = 512;
 constexpr uint32_t TAP_EPI_BYTES = TAP_EPI_WARPS * 32 * 33 * 4;
@@ -412,15 +413,15 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.AST; ++s) {
             mbar_init(full_a(s), 1);
-            mbar_init(empty_a(s), 1);
+            mbar_init(empty_a(s), 2);  // both MMA issuers commit
         }
         for (int s = 0; s < p.BST; ++s) {
             mbar_init(full_b(s), TAP_PROD_WARPS * 32);
-            mbar_init(empty_b(s), 1);
+            mbar_init(empty_b(s), 2);
         }
-        mbar_init(tmem_full, 1);
+        mbar_init(tmem_full, 2);
         mbar_init(tmem_empty, TAP_EPI_WARPS);
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);
         *abort_word = 0;
         fence_mbar_init();
     }
@@ -436,13 +437,19 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     // the filter tiles and the cleared status word come from the re-layout kernel
     grid_dependency_wait();
 
-    if (warp == 0) {
-        // ---------------- MMA issuer
-        // One thread issues every MMA, so its own instruction latency bounds the
-        // MMA rate: stage indices and phases are ring counters, descriptors are
-        // built in 32-bit halves from tap offsets pre-shifted to 16-byte units,
-        // and the next tap's offset is loaded while the current tap issues.
+    if (warp == 0 || warp == TAP_ISSUER1_WARP) {
+        // ---------------- MMA issuers
+        // A tile's positions are split over two accumulators, TMEM columns [0, N0)
+        // and [N0, NTp); warp 0 issues the MMAs of the first, the last warp those of
+        // the second, in parallel. One thread issues each stream, so its own
+        // instruction latency bounds the rate: stage indices and phases are ring
+        // counters, descriptors are built in 32-bit halves from tap offsets
+        // pre-shifted to 16-byte units, and the next tap's offset is loaded while
+        // the current one issues. Both issuers wait on every stage and both commit
+        // (the stage, accumulator and teardown barriers count two arrivals); an
+        // issuer with no columns (a tile of one accumulator) commits without MMAs.
         if (lane == 0) {
+            const int which = warp == 0 ? 0 : 1;
             bool ok = true;
             int k = 0;
             int sb = 0, sa = 0;
@@ -461,28 +468,28 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     tc_fence_after();
                 }
                 const int NTp = (tl.Q * p.pitch + 15) / 16 * 16;
-                const int N0 = split_n0(NTp), N1 = NTp - N0;
-                const uint32_t idesc0 = make_idesc(p.bf16 != 0, BM, N0);
-                const uint32_t idesc1 = make_idesc(p.bf16 != 0, BM, N1 > 0 ? N1 : 16);
+                const int N0 = split_n0(NTp);
+                const int NW = which == 0 ? N0 : NTp - N0;          // this issuer's columns
+                const uint32_t col0 = which == 0 ? 0u : (uint32_t)N0;
+                const uint32_t idesc = make_idesc(p.bf16 != 0, BM, NW > 0 ? NW : 16);
+                const uint32_t d_tmem = tmem + col0;
                 for (int cc = 0; cc < p.NCH && ok; ++cc) {
                     if (!(ok = bar_wait(full_b(sb), phb, ctl, SITE_FULL_B))) break;
-                    const uint32_t b_lo_slab = b_lo_base + (uint32_t)sb * b_stage16;
+                    const uint32_t b_lo_slab = b_lo_base + (uint32_t)sb * b_stage16 + col0;
                     for (int t0 = 0; t0 < p.T && ok; t0 += p.TG) {
                         if (!(ok = bar_wait(full_a(sa), pha, ctl, SITE_FULL_A))) break;
                         tc_fence_after();
-                        const int t_end = min(p.T, t0 + p.TG);
-                        uint32_t a_lo = a_lo_base + (uint32_t)sa * a_stage16;
-                        uint32_t off = toff[t0];
-                        for (int t = t0; t < t_end; ++t, a_lo += TAP_A_BYTES >> 4) {
-                            const uint32_t off_next = toff[t + 1 < t_end ? t + 1 : t];
-                            const uint64_t ad = ((uint64_t)a_hi << 32) | a_lo;
-                            const uint32_t b_lo = b_lo_slab + off;
-                            const uint64_t bd0 = ((uint64_t)b_hi << 32) | b_lo;
-                            const uint64_t bd1 = ((uint64_t)b_hi << 32) | (b_lo + (uint32_t)N0);
-                            const uint32_t acc = (cc | t) != 0;
-                            mma_f16(tmem, ad, bd0, idesc0, acc);
-                            if (N1 > 0) mma_f16(tmem + N0, ad, bd1, idesc1, acc);
-                            off = off_next;
+                        if (NW > 0) {
+                            const int t_end = min(p.T, t0 + p.TG);
+                            uint32_t a_lo = a_lo_base + (uint32_t)sa * a_stage16;
+                            uint32_t off = toff[t0];
+                            for (int t = t0; t < t_end; ++t, a_lo += TAP_A_BYTES >> 4) {
+                                const uint32_t off_next = toff[t + 1 < t_end ? t + 1 : t];
+                                const uint64_t ad = ((uint64_t)a_hi << 32) | a_lo;
+                                const uint64_t bd = ((uint64_t)b_hi << 32) | (b_lo_slab + off);
+                                mma_f16(d_tmem, ad, bd, idesc, (cc | t) != 0);
+                                off = off_next;
+                            }
                         }
                         mma_commit(empty_a(sa));
                         if (++sa == p.AST) { sa = 0; pha ^= 1; }
