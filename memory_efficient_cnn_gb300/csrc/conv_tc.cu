@@ -331,12 +331,17 @@ struct TapParams {
     int64_t L;             // WW: window row length W_i*H_f
     int64_t win_elems;     // WW: elements of the window tensor
     int N_img;             // images (bound of the staged reads)
-    int raw_elems;         // W*: elements of the raw staging buffer
+    int raw_elems;         // elements of the raw staging area (all slots)
+    int ring;              // 1: raw chunks staged by cp.async two deep (next chunk in flight)
+    int raw_slot;          // elements of one raw slot (a multiple of 64)
+    int raw_ch;            // CH with ring: elements per channel in a slot (rows x W_i)
     uint32_t stage_b;      // bytes of one slab stage
     int BST, AST;          // slab stages, filter stages
     int vec;               // CH: 16-byte row loads possible
     int bf16;
     FastDiv div_pitch;     // W*: positions -> (output row, column group)
+    FastDiv div_cgs, div_sh, div_sw;  // CH: 8-column groups per row, strides
+    FastDiv div_vpc;       // CH with ring: 16-byte vectors per channel of a full tile's rows
 };
 
 // A tile: output rows [ho0, ho0 + Q) of image n, output channels [mt*128, mt*128 + 128).
@@ -373,6 +378,15 @@ __device__ __forceinline__ uint32_t tap_offset(const TapParams &p, int t) {
         return (uint32_t)(2 * u) * p.lbo + (uint32_t)a * 16u;
     }
 }
+
+// 16-byte asynchronous copy global -> shared; bytes past src_bytes (0..16) are zero.
+__device__ __forceinline__ void cp_async16z(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -536,165 +550,234 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         __syncwarp();
     } else if (warp < 2 + TAP_PROD_WARPS) {
         // ---------------- slab producers
+        // Chunks are walked in order (tile by tile, NCH per tile). Their source rows
+        // are contiguous in global memory; where a raw staging area exists they are
+        // copied there by cp.async -- with a ring of two slots the next chunk's copy
+        // is in flight while this chunk is re-laid -- and the slab is built from
+        // shared memory. Without one (TAP_CH whose rows are not 16-byte aligned, or
+        // whose staging does not fit) the slab is gathered straight from global memory.
         const int pt = threadIdx.x - 64;
         constexpr int NPT = TAP_PROD_WARPS * 32;
         typedef uint16_t E16;
+        const bool staged = MODE != TAP_CH || p.ring;
+        const int nslots = p.ring ? 2 : 1;
         bool pok = true;
-        int gb = 0;
-        TapTile tl;
-        for (int64_t id = blockIdx.x; id < p.tiles_total; id += gridDim.x) {
-            tile_at(p, id, tl);
-            const int n = tl.n, ho0 = tl.ho0, Q = tl.Q;
-            for (int cc = 0; cc < p.NCH; ++cc, ++gb) {
-                const int sb = gb % p.BST;
-                int raw_lead = 0;
-                if (MODE != TAP_CH) {
-                    // stage the chunk's source rows (contiguous in global memory) with 16-byte
-                    // loads while earlier chunks are still being multiplied
-                    int64_t g0, cnt, total;
-                    if (MODE == TAP_WX) {
-                        const int R0 = ho0 * p.s_h;
-                        const int rows = (Q - 1) * p.s_h + p.H_f;
-                        g0 = (((int64_t)n * p.C_i + cc) * p.H_i + R0) * p.W_i;
-                        cnt = (int64_t)rows * p.W_i;
-                        total = (int64_t)p.N_img * p.C_i * p.H_i * p.W_i;
-                    } else {
-                        g0 = (((int64_t)n * p.C_i + cc) * p.H_o + ho0) * p.L;
-                        cnt = (int64_t)Q * p.L;
-                        total = p.win_elems;
-                    }
-                    raw_lead = (int)(g0 & 7);
-                    if (pok) {
-                        const int64_t base = g0 - raw_lead;
-                        const int nvec = (int)((raw_lead + cnt + 7) / 8);
-                        for (int v = pt; v < nvec; v += NPT) {
-                            const int64_t gg = base + (int64_t)v * 8;
-                            if (gg + 8 <= total) {
-                                *reinterpret_cast<uint4 *>(sRaw + v * 8) =
-                                    __ldg(reinterpret_cast<const uint4 *>(p.src + gg));
-                            } else {
-                                for (int i = 0; i < 8; ++i)
-                                    sRaw[v * 8 + i] = gg + i < total ? p.src[gg + i] : (E16)0;
-                            }
-                        }
-                    }
-                    asm volatile("bar.sync 1, %0;" ::"r"(NPT) : "memory");
+        int sb = 0;
+        uint32_t phb = 0;
+        // source range of chunk (tile, cc) and its 16-byte aligned copy into raw slot `slot`
+        auto raw_lead_of = [&](const TapTile &t, int cc) -> int {
+            if (MODE == TAP_CH) return 0;
+            const int64_t g0 = MODE == TAP_WX ? (((int64_t)t.n * p.C_i + cc) * p.H_i + t.ho0 * p.s_h) * p.W_i
+                                              : (((int64_t)t.n * p.C_i + cc) * p.H_o + t.ho0) * p.L;
+            return (int)(g0 & 7);
+        };
+        auto issue_raw = [&](const TapTile &t, int cc, int slot) {
+            const uint32_t dst0 = smem_u32(sRaw + (size_t)slot * p.raw_slot);
+            if (MODE == TAP_CH) {
+                const int rows = (t.Q - 1) * p.s_h + p.H_f;
+                const int vpc = rows * p.W_i / 8;  // 16-byte vectors per channel
+                const int64_t plane = (int64_t)p.H_i * p.W_i;
+                const uint16_t *x0 = p.src + ((int64_t)t.n * p.C_i * p.H_i + (int64_t)t.ho0 * p.s_h) * p.W_i;
+                const bool full = t.Q == p.Qmax;
+                for (int v = pt; v < 16 * vpc; v += NPT) {
+                    const int k = full ? (int)fdiv((uint32_t)v, p.div_vpc) : v / vpc;
+                    const int i = v - k * vpc;
+                    const int ci = cc * 16 + k;
+                    const bool ok = ci < p.C_i;
+                    cp_async16z(dst0 + (uint32_t)(k * p.raw_ch + i * 8) * 2,
+                                ok ? (const void *)(x0 + (int64_t)ci * plane + (int64_t)i * 8) : (const void *)p.src,
+                                ok ? 16u : 0u);
                 }
-                if (pok) pok = warp_bar_wait(empty_b(sb), ((gb / p.BST) & 1) ^ 1, ctl, SITE_EMPTY_PROD);
-                uint8_t *slab = sB + (size_t)sb * p.stage_b;
-                if (!pok) {
-                    // aborted: keep meeting the producers' barrier, do no work
-                } else if (MODE == TAP_CH) {
-                    const int R0 = ho0 * p.s_h;
-                    const int rows = (Q - 1) * p.s_h + p.H_f;
-                    const int64_t plane = (int64_t)p.H_i * p.W_i;
-                    const uint16_t *__restrict__ xn = p.src + (int64_t)n * p.C_i * plane;
-                    if (p.vec) {
-                        // 8 channels x 8 columns per item: 8 16-byte loads, 8x8 transpose, 8 16-byte stores
-                        const int cgs = p.W_i / 8;
-                        const int items = 2 * rows * cgs;
-                        for (int it = pt; it < items; it += NPT) {
-                            const int cg = it % cgs;
-                            const int t2 = it / cgs;
-                            const int lr = t2 % rows;
-                            const int c8 = t2 / rows;
-                            const int ci0 = cc * 16 + c8 * 8;
-                            uint4 v[8];
+            } else {
+                int64_t g0, cnt, total;
+                if (MODE == TAP_WX) {
+                    g0 = (((int64_t)t.n * p.C_i + cc) * p.H_i + t.ho0 * p.s_h) * p.W_i;
+                    cnt = (int64_t)((t.Q - 1) * p.s_h + p.H_f) * p.W_i;
+                    total = (int64_t)p.N_img * p.C_i * p.H_i * p.W_i;
+                } else {
+                    g0 = (((int64_t)t.n * p.C_i + cc) * p.H_o + t.ho0) * p.L;
+                    cnt = (int64_t)t.Q * p.L;
+                    total = p.win_elems;
+                }
+                const int lead = (int)(g0 & 7);
+                const int64_t base = g0 - lead;
+                const int nvec = (int)((lead + cnt + 7) / 8);
+                for (int v = pt; v < nvec; v += NPT) {
+                    const int64_t gg = base + (int64_t)v * 8;
+                    const int64_t left = total - gg;
+                    const uint32_t bytes = left >= 8 ? 16u : left > 0 ? (uint32_t)left * 2u : 0u;
+                    cp_async16z(dst0 + (uint32_t)v * 16, bytes ? (const void *)(p.src + gg) : (const void *)p.src, bytes);
+                }
+            }
+        };
+        auto next_chunk = [&](int64_t &id, int &cc, TapTile &t) {
+            if (++cc == p.NCH) {
+                cc = 0;
+                id += gridDim.x;
+                if (id < p.tiles_total) tile_at(p, id, t);
+            }
+        };
+        int64_t id = blockIdx.x;
+        int cc = 0;
+        TapTile tl;
+        if (id < p.tiles_total) tile_at(p, id, tl);
+        if (staged && id < p.tiles_total) issue_raw(tl, cc, 0);
+        cp_async_commit_group();
+        for (int g = 0; id < p.tiles_total; ++g, next_chunk(id, cc, tl)) {
+            const int slot = nslots == 2 ? (g & 1) : 0;
+            if (staged) {
+                if (nslots == 2) {
+                    int64_t id2 = id;
+                    int cc2 = cc;
+                    TapTile t2 = tl;
+                    next_chunk(id2, cc2, t2);
+                    if (pok && id2 < p.tiles_total) issue_raw(t2, cc2, slot ^ 1);
+                    cp_async_commit_group();
+                    cp_async_wait_group<1>();
+                } else {
+                    cp_async_wait_group<0>();
+                }
+                asm volatile("bar.sync 1, %0;" ::"r"(NPT) : "memory");
+            }
+            const int n = tl.n, ho0 = tl.ho0, Q = tl.Q;
+            if (pok) pok = warp_bar_wait(empty_b(sb), phb ^ 1, ctl, SITE_EMPTY_PROD);
+            uint8_t *slab = sB + (size_t)sb * p.stage_b;
+            const E16 *raw_slot = sRaw + (size_t)slot * p.raw_slot;
+            if (!pok) {
+                // aborted: keep meeting the producers' barrier, do no work
+            } else if (MODE == TAP_CH) {
+                const int rows = (Q - 1) * p.s_h + p.H_f;
+                const int64_t plane = (int64_t)p.H_i * p.W_i;
+                const uint16_t *__restrict__ xn = p.src + (int64_t)n * p.C_i * plane;
+                const int R0 = ho0 * p.s_h;
+                if (p.vec) {
+                    // 8 channels x 8 columns per item: 8 16-byte loads (from the raw slot or
+                    // global memory), 8x8 transpose, 8 16-byte stores
+                    const int cgs = p.W_i / 8;
+                    const int items = 2 * rows * cgs;
+                    for (int it = pt; it < items; it += NPT) {
+                        const int t2 = (int)fdiv((uint32_t)it, p.div_cgs);
+                        const int cg = it - t2 * cgs;
+                        const int c8 = t2 >= rows ? 1 : 0;
+                        const int lr = t2 - c8 * rows;
+                        const int ci0 = cc * 16 + c8 * 8;
+                        uint4 v[8];
+                        if (p.ring) {
+                            const E16 *src = raw_slot + (size_t)(c8 * 8) * p.raw_ch + lr * p.W_i + cg * 8;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = *reinterpret_cast<const uint4 *>(src + (size_t)e * p.raw_ch);
+                        } else {
                             const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)(R0 + lr) * p.W_i + cg * 8;
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
                                 v[e] = (ci0 + e < p.C_i) ? __ldg(reinterpret_cast<const uint4 *>(src + e * plane))
                                                          : make_uint4(0, 0, 0, 0);
-                            uint8_t *rowp = slab + (size_t)c8 * p.lbo + (size_t)((lr % p.s_h) * p.s_w) * p.PB +
-                                            (size_t)((lr / p.s_h) * p.pitch) * 16;
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const int col = cg * 8 + kk;
-                                const uint32_t sel = (kk & 1) ? 0x7632u : 0x5410u;
-                                const int wd = kk >> 1;
-                                const uint32_t w0 = __byte_perm(word_of(v[0], wd), word_of(v[1], wd), sel);
-                                const uint32_t w1 = __byte_perm(word_of(v[2], wd), word_of(v[3], wd), sel);
-                                const uint32_t w2 = __byte_perm(word_of(v[4], wd), word_of(v[5], wd), sel);
-                                const uint32_t w3 = __byte_perm(word_of(v[6], wd), word_of(v[7], wd), sel);
-                                uint8_t *dst = rowp + (size_t)(col % p.s_w) * p.PB + (size_t)(col / p.s_w) * 16;
-                                *reinterpret_cast<uint4 *>(dst) = make_uint4(w0, w1, w2, w3);
-                            }
                         }
-                    } else {
-                        // one column of 8 channels per item
-                        const int items = 2 * rows * p.W_i;
-                        for (int it = pt; it < items; it += NPT) {
-                            const int col = it % p.W_i;
-                            const int t2 = it / p.W_i;
-                            const int lr = t2 % rows;
-                            const int c8 = t2 / rows;
-                            const int ci0 = cc * 16 + c8 * 8;
-                            const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)(R0 + lr) * p.W_i + col;
-                            uint32_t e16[8];
+                        const int lq = (int)fdiv((uint32_t)lr, p.div_sh);
+                        uint8_t *rowp = slab + (size_t)c8 * p.lbo + (size_t)((lr - lq * p.s_h) * p.s_w) * p.PB +
+                                        (size_t)(lq * p.pitch) * 16;
+                        // column cg*8 + kk lives in phase block (col % s_w) at entry col / s_w
+                        int cq = (int)fdiv((uint32_t)(cg * 8), p.div_sw);
+                        int cph = cg * 8 - cq * p.s_w;
 #pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                e16[e] = (ci0 + e < p.C_i) ? (uint32_t)__ldg(src + e * plane) : 0u;
-                            uint8_t *dst = slab + (size_t)c8 * p.lbo +
-                                           (size_t)((lr % p.s_h) * p.s_w + col % p.s_w) * p.PB +
-                                           (size_t)((lr / p.s_h) * p.pitch + col / p.s_w) * 16;
-                            *reinterpret_cast<uint4 *>(dst) =
-                                make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
-                                           e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t sel = (kk & 1) ? 0x7632u : 0x5410u;
+                            const int wd = kk >> 1;
+                            const uint32_t w0 = __byte_perm(word_of(v[0], wd), word_of(v[1], wd), sel);
+                            const uint32_t w1 = __byte_perm(word_of(v[2], wd), word_of(v[3], wd), sel);
+                            const uint32_t w2 = __byte_perm(word_of(v[4], wd), word_of(v[5], wd), sel);
+                            const uint32_t w3 = __byte_perm(word_of(v[6], wd), word_of(v[7], wd), sel);
+                            uint8_t *dst = rowp + (size_t)cph * p.PB + (size_t)cq * 16;
+                            *reinterpret_cast<uint4 *>(dst) = make_uint4(w0, w1, w2, w3);
+                            if (++cph == p.s_w) { cph = 0; ++cq; }
                         }
                     }
                 } else {
-                    // window rows of channel cc, re-laid from the staged raw rows:
-                    //   entry (c, q, m)[e] = window row q of the tile at m*S + 8c + e
-                    // TAP_WX: that element is x[cc][(ho0+q)*s_h + r][m*s_w + jl] with 8c + e = jl*H_f + r
-                    // TAP_WW: it is read straight from the staged window row
-                    // One K chunk c at a time, so that the 8 source offsets of an entry
-                    // (and which of them exist) stay in registers; per entry one division.
-                    const int SC = 2 * p.U;
-                    const int per_c = Q * p.pitch;
-                    const E16 *raw = sRaw + raw_lead;
-                    const int qstride = MODE == TAP_WX ? p.s_h * p.W_i : (int)p.L;
-                    const int mstride = MODE == TAP_WX ? p.s_w : p.S;
-                    for (int c = 0; c < SC; ++c) {
-                        // element e of an entry: raw offset boff[e] from the entry's base, present
-                        // if b = 8c + e < S and its column (WX) / window index (WW) is < lim[e] - m*mstride
-                        int boff[8], lim[8];
-                        int jl = (8 * c) / p.H_f, r = 8 * c - jl * p.H_f;
+                    // one column of 8 channels per item
+                    const int items = 2 * rows * p.W_i;
+                    for (int it = pt; it < items; it += NPT) {
+                        const int col = it % p.W_i;
+                        const int t2 = it / p.W_i;
+                        const int c8 = t2 >= rows ? 1 : 0;
+                        const int lr = t2 - c8 * rows;
+                        const int ci0 = cc * 16 + c8 * 8;
+                        const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)(R0 + lr) * p.W_i + col;
+                        uint32_t e16[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int b = 8 * c + e;
-                            if (MODE == TAP_WX) {
-                                boff[e] = r * p.W_i + jl;
-                                lim[e] = b < p.S ? p.W_i - jl : 0;  // column m*s_w + jl < W_i
-                                if (++r == p.H_f) { r = 0; ++jl; }
-                            } else {
-                                boff[e] = b;
-                                lim[e] = b < p.S ? (int)p.L - b : 0;  // window index m*S + b < L
-                            }
-                        }
-                        uint8_t *slab_c = slab + (size_t)c * p.lbo;
-                        for (int i = pt; i < per_c; i += NPT) {
-                            const int q = (int)fdiv((uint32_t)i, p.div_pitch);
-                            const int m = i - q * p.pitch;
-                            const int base = q * qstride + m * mstride;
-                            const int mm = m * mstride;
-                            uint32_t e16[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) e16[e] = mm < lim[e] ? (uint32_t)raw[base + boff[e]] : 0u;
-                            *reinterpret_cast<uint4 *>(slab_c + (size_t)i * 16) =
-                                make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
-                                           e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
-                        }
+                        for (int e = 0; e < 8; ++e)
+                            e16[e] = (ci0 + e < p.C_i) ? (uint32_t)__ldg(src + e * plane) : 0u;
+                        uint8_t *dst = slab + (size_t)c8 * p.lbo +
+                                       (size_t)((lr % p.s_h) * p.s_w + col % p.s_w) * p.PB +
+                                       (size_t)((lr / p.s_h) * p.pitch + col / p.s_w) * 16;
+                        *reinterpret_cast<uint4 *>(dst) =
+                            make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
+                                       e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
                     }
                 }
-                if (pok) {
-                    fence_async_smem();
-                    mbar_arrive(full_b(sb));
+            } else {
+                // window rows of channel cc, re-laid from the staged raw rows:
+                //   entry (c, q, m)[e] = window row q of the tile at m*S + 8c + e
+                // TAP_WX: that element is x[cc][(ho0+q)*s_h + r][m*s_w + jl] with 8c + e = jl*H_f + r
+                // TAP_WW: it is read straight from the staged window row
+                // One K chunk c at a time, so that the 8 source offsets of an entry
+                // (and which of them exist) stay in registers; per entry one division.
+                const int SC = 2 * p.U;
+                const int per_c = Q * p.pitch;
+                const E16 *raw = raw_slot + raw_lead_of(tl, cc);
+                const int qstride = MODE == TAP_WX ? p.s_h * p.W_i : (int)p.L;
+                const int mstride = MODE == TAP_WX ? p.s_w : p.S;
+                for (int c = 0; c < SC; ++c) {
+                    // element e of an entry: raw offset boff[e] from the entry's base, present
+                    // if b = 8c + e < S and its column (WX) / window index (WW) is < lim[e] - m*mstride
+                    int boff[8], lim[8];
+                    int jl = (8 * c) / p.H_f, r = 8 * c - jl * p.H_f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int b = 8 * c + e;
+                        if (MODE == TAP_WX) {
+                            boff[e] = r * p.W_i + jl;
+                            lim[e] = b < p.S ? p.W_i - jl : 0;  // column m*s_w + jl < W_i
+                            if (++r == p.H_f) { r = 0; ++jl; }
+                        } else {
+                            boff[e] = b;
+                            lim[e] = b < p.S ? (int)p.L - b : 0;  // window index m*S + b < L
+                        }
+                    }
+                    uint8_t *slab_c = slab + (size_t)c * p.lbo;
+                    for (int i = pt; i < per_c; i += NPT) {
+                        const int q = (int)fdiv((uint32_t)i, p.div_pitch);
+                        const int m = i - q * p.pitch;
+                        const int base = q * qstride + m * mstride;
+                        const int mm = m * mstride;
+                        uint32_t e16[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) e16[e] = mm < lim[e] ? (uint32_t)raw[base + boff[e]] : 0u;
+                        *reinterpret_cast<uint4 *>(slab_c + (size_t)i * 16) =
+                            make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
+                                       e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
+                    }
                 }
-                // the raw rows are consumed: they may be overwritten by the next chunk
-                if (MODE != TAP_CH) asm volatile("bar.sync 1, %0;" ::"r"(NPT) : "memory");
             }
-            if (MODE == TAP_CH && !pok) break;
+            if (pok) {
+                fence_async_smem();
+                mbar_arrive(full_b(sb));
+            }
+            if (++sb == p.BST) { sb = 0; phb ^= 1; }
+            if (staged) {
+                // the raw slot is consumed: the copy of a later chunk may overwrite it
+                asm volatile("bar.sync 1, %0;" ::"r"(NPT) : "memory");
+                if (nslots == 1) {
+                    int64_t id2 = id;
+                    int cc2 = cc;
+                    TapTile t2 = tl;
+                    next_chunk(id2, cc2, t2);
+                    if (pok && id2 < p.tiles_total) issue_raw(t2, cc2, 0);
+                    cp_async_commit_group();
+                }
+            }
+            if (MODE == TAP_CH && !staged && !pok) break;
         }
+        cp_async_wait_group<0>();
     } else {
         // ---------------- epilogue: TMEM -> registers -> smem transpose -> coalesced stores
         const int ew = warp - 2 - TAP_PROD_WARPS;  // 0..7
@@ -879,15 +962,29 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
             stage_b = std::max(2 * U * lbo, (2 * U - 1) * lbo + (A - 1 + NTp) * 16);
         }
         stage_b = (stage_b + 127) / 128 * 128;
-        const int64_t raw = mode == TAP_CH ? 0
-                            : mode == TAP_WX ? (RR * s.W_i + 16) * 2
-                                             : (Q * s.W_i * s.H_f + 16) * 2;
-        for (int BST : {3, 2}) {
-            for (int TG : {9, 8, 6, 5, 4, 3, 2, 1}) {
-                const int tg = (int)std::min<int64_t>(TG, T);
-                if (TG > T && TG != 1) continue;
-                for (int AST : {4, 3, 2}) {
-                    int64_t total = (int64_t)AST * tg * TAP_A_BYTES + BST * stage_b + (raw + 127) / 128 * 128 +
+        // raw staging slot (elements, a multiple of 64): TAP_CH 16 channels of the tile's
+        // input rows (only when rows are whole 16-byte vectors), TAP_WX one channel's
+        // input rows, TAP_WW its window rows, each with room for the alignment lead
+        const int64_t slot = mode == TAP_CH ? (s.W_i % 8 == 0 ? 16 * RR * s.W_i : 0)
+                             : mode == TAP_WX ? RR * s.W_i + 16
+                                              : Q * s.W_i * s.H_f + 16;
+        const int64_t slot_e = (slot + 63) / 64 * 64;
+        // search: filter stages of at least 8 taps (or all of them) first, since every
+        // stage costs the MMA issuers a fixed overhead; within that a ring of two raw
+        // slots (the next chunk's copy in flight) before one slot (TAP_W*) or none
+        // (TAP_CH); then larger filter stages, then three slab stages, then three
+        // filter stages
+        for (int pass = 0; pass < 2; ++pass)
+        for (int ring : {1, 0}) {
+          const int64_t raw_e = mode == TAP_CH ? (ring ? 2 * slot_e : 0) : (ring ? 2 : 1) * slot_e;
+          if (ring && slot_e == 0) continue;
+          for (int TG : {9, 8, 6, 5, 4, 3, 2, 1}) {
+            const int tg = (int)std::min<int64_t>(TG, T);
+            if (TG > T && TG != 1) continue;
+            if (pass == 0 && tg < std::min<int64_t>(T, 8)) continue;
+            for (int BST : {3, 2}) {
+              for (int AST : {3, 2, 4}) {
+                    int64_t total = (int64_t)AST * tg * TAP_A_BYTES + BST * stage_b + raw_e * 2 +
                                     TAP_EPI_BYTES + 512 + 4 * T;
                     if (total > smem_max) continue;
                     // the 512-column TMEM accumulator needs the SM to itself
@@ -913,17 +1010,21 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
                     p.L = s.W_i * s.H_f;
                     p.win_elems = s.N * s.C_i * s.H_o * s.W_i * s.H_f;
                     p.N_img = (int)s.N;
-                    p.raw_elems = (int)(raw / 2);
+                    p.raw_elems = (int)raw_e;
+                    p.ring = ring;
+                    p.raw_slot = (int)slot_e;
+                    p.raw_ch = (int)(RR * s.W_i);
                     p.stage_b = (uint32_t)stage_b;
                     p.BST = BST;
                     p.AST = AST;
                     pl.smem = (size_t)total;
                     pl.mtiles = p.MT;
                     pl.kslots = NCH * T * 16;
-                    pl.ok = p.tiles_total < (1ll << 40) && s.N < (1ll << 31);
+                    pl.ok = p.tiles_total < (1ll << 40) && s.N < (1ll << 31) && raw_e < (1ll << 30);
                     return pl;
-                }
+              }
             }
+          }
         }
     }
     return pl;
@@ -1022,7 +1123,12 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
     p.out = static_cast<uint16_t *>(out);
     p.status = status;
     p.vec = (p.W_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
+    if (pl.mode == TAP_CH && !p.vec) p.ring = 0;  // 16-byte copies need 16-byte rows
     p.div_pitch = make_fastdiv((uint32_t)p.pitch);
+    p.div_cgs = make_fastdiv((uint32_t)std::max(1, p.W_i / 8));
+    p.div_sh = make_fastdiv((uint32_t)p.s_h);
+    p.div_sw = make_fastdiv((uint32_t)p.s_w);
+    p.div_vpc = make_fastdiv((uint32_t)std::max(1, ((p.Qmax - 1) * p.s_h + p.H_f) * p.W_i / 8));
     p.bf16 = bf16 ? 1 : 0;
     const unsigned grid = (unsigned)std::min<int64_t>(sm_count(), p.tiles_total);
     auto go = [&](auto kernel) -> cudaError_t {
