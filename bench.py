@@ -40,7 +40,11 @@ if ROOT not in sys.path:
 # kernel on this workload, from one ncu capture of the current kernel source
 # (summaries under profiles/); a kernel absent here has no capture of its
 # current version.
-DRAM_TRAFFIC: dict = {}
+DRAM_TRAFFIC: dict = {
+    # conv_f32_kernel<96,24,3,2,0>, cv1: 211.1 MB read + 106.9 MB written
+    # (profiles/conv_f32_kernel_cv1.md)
+    ("cv1", "conv_f32_window_f32"): 318.0e6,
+}
 
 METRIC = "im2win conv TFLOPS and % of dense peak per layer shape; workspace bytes"
 UNIT = "TFLOP/s"
@@ -388,7 +392,7 @@ def main():
         workspace[f"im2col_{d}"] = col_b[d]
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     dk = kernels[dom]
-    traffic = DRAM_TRAFFIC.get(dom)
+    traffic = DRAM_TRAFFIC.get((layer.name, dom))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

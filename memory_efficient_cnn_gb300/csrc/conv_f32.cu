@@ -44,8 +44,23 @@ struct F32Params {
     FastDiv div_KK, div_Wo, div_Hf;
 };
 
-// The filter is padded along K to a multiple of every chunk length (16, 24).
+// The filter is padded along K to a multiple of every chunk length (16, 24, 48).
 constexpr int K_ALIGN = 48;
+
+// Kernel configurations per channel tile: TM, KC (k per chunk), pipeline stages,
+// CTAs per SM the registers are budgeted for.
+#ifndef F32_CFG_128
+#define F32_CFG_128 128, 16, 3, 2
+#endif
+#ifndef F32_CFG_96
+#define F32_CFG_96 96, 24, 3, 2
+#endif
+#ifndef F32_CFG_64
+#define F32_CFG_64 64, 16, 3, 4
+#endif
+#ifndef F32_CFG_32
+#define F32_CFG_32 32, 16, 3, 4
+#endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -65,15 +80,20 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 // TM output channels x 128 pixels per CTA, 8 x 8 register tile per thread
 // (channels ty*8..+7, pixels tx*4..+3 and 64 + tx*4..+3). K is staged KC at a
-// time through a 3-stage cp.async pipeline (gathers go straight to shared
-// memory, so no registers hold prefetched data).
-template <int TM, int KC, bool FROM_X>
-__global__ void __launch_bounds__(TM * 2, (TM >= 96 ? 2 : 4)) conv_f32_kernel(F32Params p) {
+// time through a STAGES-deep cp.async pipeline (gathers go straight to shared
+// memory, so no registers hold prefetched data). The filter slice arrives as
+// 16-byte vectors. The 4-byte gathers follow the contiguous direction of the
+// source: from the window tensor consecutive k of a pixel are consecutive
+// elements, so thread t gathers k = t % KC of pixels t / KC + i*(NT/KC); from the
+// NCHW input consecutive pixels of a row are (unit stride), so lane l of warp w
+// gathers pixels l + 32i at the KPT values of k w*KPT ...
+template <int TM, int KC, int STAGES, int MINB, bool FROM_X>
+__global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
     constexpr int NT = TM * 2;                 // (TM/8) x 16 threads
-    constexpr int A_PER = KC * TP / NT;        // window elements each thread stages
+    constexpr int PPT = FROM_X ? TP / 32 : KC * TP / NT;  // pixels each thread gathers
+    constexpr int KPT = FROM_X ? KC * 32 / NT : 1;        // k values each thread gathers
     constexpr int B_VEC = KC * TM / 4 / NT;    // 16-byte filter vectors each thread stages
-    constexpr int STAGES = 3;
-    static_assert(NT % KC == 0 && (KC * TP) % NT == 0 && (KC * TM / 4) % NT == 0, "tile");
+    static_assert((FROM_X ? KPT * (NT / 32) == KC : NT % KC == 0) && (KC * TM / 4) % NT == 0, "tile");
     static_assert(K_ALIGN % KC == 0, "filter padding");
     extern __shared__ __align__(16) float smem_f[];
     float (*As)[KC][TP + 4] = reinterpret_cast<float (*)[KC][TP + 4]>(smem_f);
@@ -86,14 +106,16 @@ __global__ void __launch_bounds__(TM * 2, (TM >= 96 ? 2 : 4)) conv_f32_kernel(F3
     const float *__restrict__ src = p.src + (int64_t)n * p.img_src;
     const float *__restrict__ filt = p.filt;
 
-    // ---- staging coordinates: each thread stages one k of A_PER pixels (4-byte gathers)
-    // and B_VEC 16-byte vectors of the filter slice
-    const int ka = tid % KC;
-    int pos_off[A_PER];   // offset of the pixel's window segment; pixels past P read offset 0, size 0
+    // ---- staging coordinates
+    // thread's first pixel, pixel step, first k and shared-memory row/column
+    const int px0 = FROM_X ? (tid & 31) : tid / KC;
+    constexpr int PXS = FROM_X ? 32 : NT / KC;
+    const int k0 = FROM_X ? (tid >> 5) * KPT : tid % KC;
+    int pos_off[PPT];     // offset of the pixel's window segment; pixels past P read offset 0, size 0
     uint32_t pos_ok = 0;  // bit i: pixel i exists
 #pragma unroll
-    for (int i = 0; i < A_PER; ++i) {
-        const int pg = p0 + tid / KC + i * (NT / KC);
+    for (int i = 0; i < PPT; ++i) {
+        const int pg = p0 + px0 + PXS * i;
         pos_off[i] = 0;
         if (pg < p.P) {
             const int ho = (int)fdiv((uint32_t)pg, p.div_Wo);
@@ -102,32 +124,35 @@ __global__ void __launch_bounds__(TM * 2, (TM >= 96 ? 2 : 4)) conv_f32_kernel(F3
             pos_ok |= 1u << i;
         }
     }
-    const uint32_t a_dst0 = smem_addr(&As[0][ka][tid / KC]);
+    const uint32_t a_dst0 = smem_addr(&As[0][k0][px0]);
     const uint32_t b_dst0 = smem_addr(&Bs[0][0][0]);
     constexpr uint32_t A_BUF = KC * (TP + 4) * 4, B_BUF = KC * (TM + 4) * 4;
     const float *__restrict__ fcol = filt + co0;
 
     auto issue_chunk = [&](int c) {
         const int buf = c % STAGES;
-        const int kg = c * KC + ka;
-        int coff = 0;
-        uint32_t ok = 0;
-        if (kg < p.K) {
-            const int ci = (int)fdiv((uint32_t)kg, p.div_KK);
-            const int kk = kg - ci * p.KK;
-            if (FROM_X) {
-                const int j = (int)fdiv((uint32_t)kk, p.div_Hf);
-                const int r = kk - j * p.H_f;
-                coff = (ci * p.H_i + r) * p.W_i + j;
-            } else {
-                coff = ci * p.H_o * p.L + kk;
-            }
-            ok = pos_ok;
-        }
         const uint32_t a_dst = a_dst0 + buf * A_BUF;
 #pragma unroll
-        for (int i = 0; i < A_PER; ++i)
-            cp_async4(a_dst + i * (NT / KC) * 4, src + (pos_off[i] + coff), ((ok >> i) & 1u) * 4u);
+        for (int j = 0; j < KPT; ++j) {
+            const int kg = c * KC + k0 + j;
+            int coff = 0;
+            uint32_t ok = 0;
+            if (kg < p.K) {
+                const int ci = (int)fdiv((uint32_t)kg, p.div_KK);
+                const int kk = kg - ci * p.KK;
+                if (FROM_X) {
+                    const int jj = (int)fdiv((uint32_t)kk, p.div_Hf);
+                    const int r = kk - jj * p.H_f;
+                    coff = (ci * p.H_i + r) * p.W_i + jj;
+                } else {
+                    coff = ci * p.H_o * p.L + kk;
+                }
+                ok = pos_ok;
+            }
+#pragma unroll
+            for (int i = 0; i < PPT; ++i)
+                cp_async4(a_dst + (j * (TP + 4) + PXS * i) * 4, src + (pos_off[i] + coff), ((ok >> i) & 1u) * 4u);
+        }
         // filter rows c*KC .. c*KC + KC - 1, channels co0 .. co0 + TM - 1 (zero padded in memory)
         const uint32_t b_dst = b_dst0 + buf * B_BUF;
 #pragma unroll
@@ -191,9 +216,9 @@ __global__ void __launch_bounds__(TM * 2, (TM >= 96 ? 2 : 4)) conv_f32_kernel(F3
     }
 }
 
-template <int TM, int KC>
+template <int TM, int KC, int STAGES>
 constexpr size_t f32_smem_bytes() {
-    return (size_t)3 * KC * ((TP + 4) + (TM + 4)) * sizeof(float);
+    return (size_t)STAGES * KC * ((TP + 4) + (TM + 4)) * sizeof(float);
 }
 
 // filt'[co][ci*KK + j*H_f + r] = filt[co][ci][r][j]; block 0 also clears the
@@ -218,14 +243,14 @@ __global__ void relayout_filter_f32(const float *__restrict__ filt, float *__res
     }
 }
 
-template <int TM, int KC, bool FROM_X>
+template <int TM, int KC, int STAGES, int MINB, bool FROM_X>
 cudaError_t launch_tm(const F32Params &p, int N, cudaStream_t st) {
     dim3 grid((unsigned)(p.pos_tiles * N), (unsigned)((p.C_o + TM - 1) / TM));
-    constexpr size_t smem = f32_smem_bytes<TM, KC>();
-    cudaError_t e = cudaFuncSetAttribute(conv_f32_kernel<TM, KC, FROM_X>,
+    constexpr size_t smem = f32_smem_bytes<TM, KC, STAGES>();
+    cudaError_t e = cudaFuncSetAttribute(conv_f32_kernel<TM, KC, STAGES, MINB, FROM_X>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    conv_f32_kernel<TM, KC, FROM_X><<<grid, TM * 2, smem, st>>>(p);
+    conv_f32_kernel<TM, KC, STAGES, MINB, FROM_X><<<grid, TM * 2, smem, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -305,15 +330,15 @@ cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *
     const int best = choose_tm(s);
     const int N = (int)s.N;
     if (from_x) {
-        if (best == 128) return launch_tm<128, 16, true>(p, N, st);
-        if (best == 96) return launch_tm<96, 24, true>(p, N, st);
-        if (best == 64) return launch_tm<64, 16, true>(p, N, st);
-        return launch_tm<32, 16, true>(p, N, st);
+        if (best == 128) return launch_tm<F32_CFG_128, true>(p, N, st);
+        if (best == 96) return launch_tm<F32_CFG_96, true>(p, N, st);
+        if (best == 64) return launch_tm<F32_CFG_64, true>(p, N, st);
+        return launch_tm<F32_CFG_32, true>(p, N, st);
     }
-    if (best == 128) return launch_tm<128, 16, false>(p, N, st);
-    if (best == 96) return launch_tm<96, 24, false>(p, N, st);
-    if (best == 64) return launch_tm<64, 16, false>(p, N, st);
-    return launch_tm<32, 16, false>(p, N, st);
+    if (best == 128) return launch_tm<F32_CFG_128, false>(p, N, st);
+    if (best == 96) return launch_tm<F32_CFG_96, false>(p, N, st);
+    if (best == 64) return launch_tm<F32_CFG_64, false>(p, N, st);
+    return launch_tm<F32_CFG_32, false>(p, N, st);
 }
 
 }  // namespace im2win
