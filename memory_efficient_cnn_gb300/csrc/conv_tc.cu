@@ -303,6 +303,19 @@ __global__ void relayout_filter_expand(const uint16_t *__restrict__ filt, uint16
 // =========================================================================
 enum TapMode { TAP_CH = 0, TAP_WX = 1, TAP_WW = 2 };
 
+// Tap stacking (TAP_CH with C_o <= 64, so half of M = 128 would be idle).
+// Taps (r, j) and (r, j + s_w) lie in the same polyphase block, one slab entry
+// apart. One MMA at the B offset of (r, j) with A rows 0..63 = filter of (r, j)
+// and rows 64..127 = filter of (r, j + s_w) leaves in accumulator rows 64..127
+// the contribution of (r, j + s_w) to the position one column to the left; the
+// epilogue adds D[co + 64][p + 1] to D[co][p]. Group k of a filter row has its
+// top tap at j = (k / s_w) * 2 s_w + k % s_w (every column whose j / s_w is
+// even) and its bottom tap at j + s_w when that is < W_f.
+__host__ __device__ inline int stacked_top_j(int k, int s_w) { return (k / s_w) * 2 * s_w + k % s_w; }
+__host__ __device__ inline int stacked_groups_per_row(int W_f, int s_w) {
+    return (W_f / (2 * s_w)) * s_w + (W_f % (2 * s_w) < s_w ? W_f % (2 * s_w) : s_w);
+}
+
 constexpr int TAP_PROD_WARPS = 8;
 constexpr int TAP_EPI_WARPS = 8;
 constexpr int TAP_ISSUER1_WARP = 2 + TAP_PROD_WARPS + TAP_EPI_WARPS;  // the second MMA issuer
@@ -342,6 +355,8 @@ struct TapParams {
     FastDiv div_pitch;     // W*: positions -> (output row, column group)
     FastDiv div_cgs, div_sh, div_sw;  // CH: 8-column groups per row, strides
     FastDiv div_vpc;       // CH with ring: 16-byte vectors per channel of a full tile's rows
+    int stack;             // CH, C_o <= 64: two taps per MMA, stacked along M (see below)
+    int Gr;                // stacked: tap groups per filter row
 };
 
 // A tile: output rows [ho0, ho0 + Q) of image n, output channels [mt*128, mt*128 + 128).
@@ -408,13 +423,18 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sE) + TAP_EPI_BYTES);
     // [A stages][slab stages][raw rows (W modes)][epilogue staging] then
     // bars: full_a[AST] | empty_a[AST] | full_b[BST] | empty_b[BST] | tmem_full | tmem_empty | drain
-    const int nb = 2 * p.AST + 2 * p.BST + 3;
+    //       | stacked hand-over: full[4] | empty[4]
+    const int nb = 2 * p.AST + 2 * p.BST + 3 + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + nb);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
     uint32_t *toff = reinterpret_cast<uint32_t *>(bars + nb + 1);  // [T] tap offsets (16-byte units)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int t = threadIdx.x; t < p.T; t += blockDim.x) toff[t] = tap_offset<MODE>(p, t) >> 4;  // 16-byte units
+    for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
+        // a stacked group is issued at its top tap
+        const int tap = p.stack ? (t / p.Gr) * p.W_f + stacked_top_j(t % p.Gr, p.s_w) : t;
+        toff[t] = tap_offset<MODE>(p, tap) >> 4;  // 16-byte units
+    }
 
     auto full_a = [&](int s) { return smem_u32(bars + s); };
     auto empty_a = [&](int s) { return smem_u32(bars + p.AST + s); };
@@ -423,6 +443,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     const uint32_t tmem_full = smem_u32(bars + 2 * p.AST + 2 * p.BST);
     const uint32_t tmem_empty = smem_u32(bars + 2 * p.AST + 2 * p.BST + 1);
     const uint32_t drain = smem_u32(bars + 2 * p.AST + 2 * p.BST + 2);
+    auto xfull = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 3 + i); };
+    auto xempty = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 7 + i); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.AST; ++s) {
@@ -436,6 +458,10 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         mbar_init(tmem_full, 2);
         mbar_init(tmem_empty, TAP_EPI_WARPS);
         mbar_init(drain, 2);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(xfull(i), 32);
+            mbar_init(xempty(i), 32);
+        }
         *abort_word = 0;
         fence_mbar_init();
     }
@@ -481,7 +507,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     if (!(ok = bar_wait(tmem_empty, (k - 1) & 1, ctl, SITE_EMPTY_MMA))) break;
                     tc_fence_after();
                 }
-                const int NTp = (tl.Q * p.pitch + 15) / 16 * 16;
+                // stacked: one more column, read by the epilogue for the shifted rows
+                const int NTp = (tl.Q * p.pitch + p.stack + 15) / 16 * 16;
                 const int N0 = split_n0(NTp);
                 const int NW = which == 0 ? N0 : NTp - N0;          // this issuer's columns
                 const uint32_t col0 = which == 0 ? 0u : (uint32_t)N0;
@@ -786,26 +813,48 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         uint32_t *stage = sE + ew * (32 * 33);
         const int64_t plane = (int64_t)p.H_o * p.W_o;
         int k = 0;
+        uint32_t xk = 0;  // stacked hand-overs so far (the same count in both warps of a pair)
         TapTile tl;
         for (int64_t id = blockIdx.x; id < p.tiles_total; id += gridDim.x) {
             tile_at(p, id, tl);
             if (!warp_bar_wait(tmem_full, k & 1, ctl, SITE_DONE)) break;
             tc_fence_after();
-            const int co0 = tl.mt * BM + q4 * 32;
             const int NT = tl.Q * p.pitch;
             const int NTp = (NT + 15) / 16 * 16;
             // the two warps of a quarter split the columns in 64-column blocks
             const int nb64 = (NTp + 63) / 64;
             const int c_begin = hh == 0 ? 0 : ((nb64 + 1) / 2) * 64;
             const int c_end = hh == 0 ? min(NTp, ((nb64 + 1) / 2) * 64) : NTp;
-            uint16_t *out_c = p.out + ((int64_t)tl.n * p.C_o + co0) * plane + (int64_t)tl.ho0 * p.W_o;
             const int pitch = p.pitch, W_o = p.W_o;
-            drain_columns(tmem + ((uint32_t)(q4 * 32) << 16), c_begin, c_end, stage, min(32, p.C_o - co0),
-                          plane, p.bf16, out_c, [&](int pp) -> int {
-                              const int qrow = pp / pitch;
-                              const int wo = pp - qrow * pitch;
-                              return (pp < NT && wo < W_o) ? qrow * W_o + wo : -1;
-                          });
+            auto off_of = [&](int pp) -> int {
+                const int qrow = pp / pitch;
+                const int wo = pp - qrow * pitch;
+                return (pp < NT && wo < W_o) ? qrow * W_o + wo : -1;
+            };
+            const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16);
+            if (!p.stack) {
+                const int co0 = tl.mt * BM + q4 * 32;
+                uint16_t *out_c = p.out + ((int64_t)tl.n * p.C_o + co0) * plane + (int64_t)tl.ho0 * p.W_o;
+                drain_columns(taddr, c_begin, c_end, stage, min(32, p.C_o - co0), plane, p.bf16, out_c, off_of);
+            } else {
+                // warps of quarters 2, 3 (rows 64..127) feed the warps of quarters 0, 1
+                // (same channels, rows 0..63) of the same column half through the
+                // lower warp's staging area and the pair's two mbarriers
+                const int pair = (q4 & 1) + 2 * hh;
+                bool dok;
+                if (q4 >= 2) {
+                    dok = drain_stacked_lower(taddr, c_begin, c_end, reinterpret_cast<float *>(stage), xfull(pair),
+                                              xempty(pair), &xk, ctl, SITE_STACK);
+                } else {
+                    const int co0 = q4 * 32;
+                    uint16_t *out_c = p.out + ((int64_t)tl.n * p.C_o + co0) * plane + (int64_t)tl.ho0 * p.W_o;
+                    const float *xbuf = reinterpret_cast<const float *>(sE + (ew - 2) * (32 * 33));
+                    dok = drain_stacked_upper(taddr, c_begin, c_end, stage, xbuf, xfull(pair), xempty(pair), &xk,
+                                              ctl, SITE_STACK, max(0, min(32, p.C_o - co0)), plane, p.bf16,
+                                              out_c, off_of);
+                }
+                if (!dok) break;
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tmem_empty);
@@ -831,7 +880,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
 // Block 0 also clears the status word.
 __global__ void relayout_filter_tap(const uint16_t *__restrict__ filt, uint16_t *__restrict__ fa,
                                     uint32_t *status, int mode, int C_i, int C_o, int H_f, int W_f,
-                                    int s_w, int T, int NCH, int U, int S, int win_hf, int n_chunks) {
+                                    int s_w, int T, int NCH, int U, int S, int win_hf, int n_chunks,
+                                    int stack, int Gr) {
     allow_dependents();  // the tap kernel may start its prologue meanwhile
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
         status[0] = 0;
@@ -846,14 +896,22 @@ __global__ void relayout_filter_tap(const uint16_t *__restrict__ filt, uint16_t 
         for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < per_chunk; idx += gridDim.x * blockDim.x) {
             const int e = idx & 7, rw = (idx >> 3) & 7, h = (idx >> 6) & 1, g = (idx >> 7) & 15;
             const int t = idx >> 11;
-            const int co = mt * BM + g * 8 + rw;
+            const int co = mt * BM + (stack ? (g & 7) : g) * 8 + rw;
             const int k = h * 8 + e;
             uint16_t v = 0;
             if (co < C_o) {
                 if (mode == TAP_CH) {
                     const int ci = cc * 16 + k;
-                    const int ts = win_hf > 0 ? (t % win_hf) * (T / win_hf) + t / win_hf : t;
-                    if (ci < C_i) v = filt[((int64_t)co * C_i + ci) * HW + ts];
+                    // tap of the (virtual) filter: t itself, or for a stacked group the top
+                    // tap (rows 0..63) or the bottom tap (rows 64..127, absent past W_f)
+                    int tap = t;
+                    if (stack) {
+                        const int r = t / Gr, jt = stacked_top_j(t % Gr, s_w);
+                        const int j = g < 8 ? jt : jt + s_w;
+                        tap = j < W_f ? r * W_f + j : -1;
+                    }
+                    const int ts = tap < 0 ? -1 : win_hf > 0 ? (tap % win_hf) * (HW / win_hf) + tap / win_hf : tap;
+                    if (ci < C_i && ts >= 0) v = filt[((int64_t)co * C_i + ci) * HW + ts];
                 } else {
                     const int a = t / U, u = t - a * U;
                     const int b = 16 * u + k;
@@ -913,9 +971,12 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
     const int64_t smem_max = 227 * 1024 - 1024;
     if (s.C_i * s.H_i * s.W_i >= (1ll << 31)) return pl;
     int64_t pitch, T, U = 0, S = 0, A = 0, NCH;
+    // stacking (TAP_CH, C_o <= 64, some tap has a partner): T counts tap groups
+    const int stack = (mode == TAP_CH && s.C_o <= 64 && s.W_f > s.s_w) ? 1 : 0;
+    const int Gr = stack ? stacked_groups_per_row((int)s.W_f, (int)s.s_w) : 0;
     if (mode == TAP_CH) {
         pitch = (s.W_i + s.s_w - 1) / s.s_w;
-        T = s.H_f * s.W_f;
+        T = stack ? s.H_f * Gr : s.H_f * s.W_f;
         NCH = (s.C_i + 15) / 16;
     } else {
         S = s.s_w * s.H_f;
@@ -927,8 +988,11 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
         if (mode == TAP_WW && s.N * s.C_i * s.H_o * s.W_i * s.H_f >= (1ll << 40)) return pl;
         if (s.H_o * s.W_i * s.H_f >= (1ll << 31)) return pl;
     }
-    if (pitch > TAP_MAX_NT || T > 4096) return pl;
-    const int64_t Qcap = std::min<int64_t>(s.H_o, TAP_MAX_NT / pitch);
+    // stacked tiles need one more accumulator column, and the epilogue reads one
+    // column past a 64-column block: at most 448 columns
+    const int64_t max_nt = stack ? 448 - 1 : TAP_MAX_NT;
+    if (pitch > max_nt || T > 4096) return pl;
+    const int64_t Qcap = std::min<int64_t>(s.H_o, max_nt / pitch);
     const int64_t MT = (s.C_o + BM - 1) / BM;
     for (int64_t Qfit = Qcap; Qfit >= 1; --Qfit) {
         // rows per tile: among tilings with at most Qfit rows, the one with the least
@@ -942,7 +1006,7 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
             const double t = (double)rounds * tile_cost(q * pitch);
             if (t < best * 0.99) { best = t; Q = q; }
         }
-        const int64_t NTp = (Q * pitch + 15) / 16 * 16;
+        const int64_t NTp = (Q * pitch + stack + 15) / 16 * 16;
         const int64_t RR = (Q - 1) * s.s_h + s.H_f;  // input rows under a tile of Q rows
         int64_t PB = 0, lbo, stage_b;
         if (mode == TAP_CH) {
@@ -996,6 +1060,8 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
                     p.MT = (int)((s.C_o + BM - 1) / BM);
                     p.NCH = (int)NCH;
                     p.T = (int)T;
+                    p.stack = stack;
+                    p.Gr = Gr;
                     p.TG = tg;
                     p.ntg = (int)((T + tg - 1) / tg);
                     p.Qmax = (int)Q;
@@ -1115,7 +1181,7 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
                      (unsigned)std::min(n_chunks, 65535));
     relayout_filter_tap<<<rgrid, 256, 0, st>>>(static_cast<const uint16_t *>(filt), fa, status, pl.mode, p.C_i,
                                                p.C_o, p.H_f, p.W_f, p.s_w, p.T, p.NCH, p.U, p.S, pl.win_hf,
-                                               n_chunks);
+                                               n_chunks, p.stack, p.Gr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     p.src = static_cast<const uint16_t *>(src);

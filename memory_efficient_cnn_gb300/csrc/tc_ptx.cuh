@@ -105,6 +105,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr)
         : "memory");
 }
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t &r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -137,7 +140,7 @@ __host__ __device__ inline uint32_t make_idesc(bool bf16, int M, int N) {
 }
 
 enum WaitSite : uint32_t { SITE_FULL_A = 1, SITE_FULL_B, SITE_EMPTY_MMA, SITE_EMPTY_LOAD,
-                           SITE_EMPTY_PROD, SITE_DONE, SITE_DRAIN };
+                           SITE_EMPTY_PROD, SITE_DONE, SITE_DRAIN, SITE_STACK };
 
 struct Ctl {
     volatile int *abort_flag;
@@ -221,17 +224,61 @@ __device__ __forceinline__ void drain_accumulator(uint32_t taddr, int first_blk,
     }
 }
 
+// Stores one staged block of the tap kernels' drain: the warp's staging area
+// holds 32 rows x 64 columns of rounded results (u16 pairs, row pitch 33
+// words); lane l stores positions 2l and 2l+1 of every row. off_of(col) gives
+// the output element offset of column col within a channel plane (or -1 if the
+// column is not an output); row r lives at out_c + r*row_stride. When, for
+// every lane, the two positions are adjacent outputs at a 4-byte aligned
+// address in every row, the block is stored as 4-byte pairs; otherwise as
+// 2-byte elements. Either way a lane's row loop is branch-free.
+template <typename OffFn>
+__device__ __forceinline__ void store_block(const uint32_t *stage, int c0, int rows, int64_t row_stride,
+                                            uint16_t *out_c, OffFn off_of) {
+    const int lane = threadIdx.x & 31;
+    const int o0 = off_of(c0 + 2 * lane), o1 = off_of(c0 + 2 * lane + 1);
+    const bool pair_ok = o0 < 0 || (o1 == o0 + 1 && (reinterpret_cast<uintptr_t>(out_c + o0) & 3) == 0);
+    const bool pairs = (row_stride & 1) == 0 && __all_sync(0xffffffffu, pair_ok);
+    const uint32_t *src = stage + lane;
+    if (pairs) {
+        if (o0 >= 0) {
+            uint32_t *d = reinterpret_cast<uint32_t *>(out_c + o0);
+            const int64_t st = row_stride >> 1;
+            if (rows == 32) {
+#pragma unroll 8
+                for (int row = 0; row < 32; ++row, d += st) *d = src[row * 33];
+            } else {
+                for (int row = 0; row < rows; ++row, d += st) *d = src[row * 33];
+            }
+        }
+    } else if (o0 >= 0 || o1 >= 0) {
+        // a lane whose first position is not an output stores through its second
+        // address for both (the store of the missing one is predicated off)
+        uint16_t *d0 = out_c + (o0 >= 0 ? o0 : o1);
+        uint16_t *d1 = out_c + (o1 >= 0 ? o1 : o0);
+        const bool v0 = o0 >= 0, v1 = o1 >= 0;
+        if (rows == 32) {
+#pragma unroll 8
+            for (int row = 0; row < 32; ++row, d0 += row_stride, d1 += row_stride) {
+                const uint32_t w = src[row * 33];
+                if (v0) *d0 = (uint16_t)(w & 0xFFFFu);
+                if (v1) *d1 = (uint16_t)(w >> 16);
+            }
+        } else {
+            for (int row = 0; row < rows; ++row, d0 += row_stride, d1 += row_stride) {
+                const uint32_t w = src[row * 33];
+                if (v0) *d0 = (uint16_t)(w & 0xFFFFu);
+                if (v1) *d1 = (uint16_t)(w >> 16);
+            }
+        }
+    }
+}
+
 // Faster drain for the tap kernels. The warp owns TMEM columns [c_begin,
 // c_end) of its 32 accumulator lanes (taddr = lane quarter base). Per block of
 // 64 columns: two 32-column TMEM loads (the next block's first load is in
 // flight while this block is stored), rounding to fp16/bf16, a transpose
-// through the warp's staging area (32 rows x 33 words), then lane l stores
-// positions 2l and 2l+1 of every row. off_of(col) gives the output element
-// offset of column col within a channel plane (or -1 if the column is not an
-// output); row r of the block lives at out_c + r*row_stride. When, for every
-// lane, the two positions are adjacent outputs at a 4-byte aligned address in
-// every row, the block is stored as 4-byte pairs; otherwise as 2-byte
-// elements. Either way a lane's row loop is branch-free.
+// through the warp's staging area (32 rows x 33 words), then store_block.
 template <typename OffFn>
 __device__ __forceinline__ void drain_columns(uint32_t taddr, int c_begin, int c_end, uint32_t *stage,
                                               int rows, int64_t row_stride, int bf16,
@@ -252,45 +299,67 @@ __device__ __forceinline__ void drain_columns(uint32_t taddr, int c_begin, int c
             if (nxt < c_end) tmem_ld32(taddr + (uint32_t)nxt, r);
         }
         __syncwarp();
-        // ---- lane l: positions c0 + 2l, c0 + 2l + 1 of every row
-        const int o0 = off_of(c0 + 2 * lane), o1 = off_of(c0 + 2 * lane + 1);
-        const bool pair_ok = o0 < 0 || (o1 == o0 + 1 && (reinterpret_cast<uintptr_t>(out_c + o0) & 3) == 0);
-        const bool pairs = (row_stride & 1) == 0 && __all_sync(0xffffffffu, pair_ok);
-        const uint32_t *src = stage + lane;
-        if (pairs) {
-            if (o0 >= 0) {
-                uint32_t *d = reinterpret_cast<uint32_t *>(out_c + o0);
-                const int64_t st = row_stride >> 1;
-                if (rows == 32) {
-#pragma unroll 8
-                    for (int row = 0; row < 32; ++row, d += st) *d = src[row * 33];
-                } else {
-                    for (int row = 0; row < rows; ++row, d += st) *d = src[row * 33];
-                }
-            }
-        } else if (o0 >= 0 || o1 >= 0) {
-            // a lane whose first position is not an output stores through its second
-            // address for both (the store of the missing one is predicated off)
-            uint16_t *d0 = out_c + (o0 >= 0 ? o0 : o1);
-            uint16_t *d1 = out_c + (o1 >= 0 ? o1 : o0);
-            const bool v0 = o0 >= 0, v1 = o1 >= 0;
-            if (rows == 32) {
-#pragma unroll 8
-                for (int row = 0; row < 32; ++row, d0 += row_stride, d1 += row_stride) {
-                    const uint32_t w = src[row * 33];
-                    if (v0) *d0 = (uint16_t)(w & 0xFFFFu);
-                    if (v1) *d1 = (uint16_t)(w >> 16);
-                }
-            } else {
-                for (int row = 0; row < rows; ++row, d0 += row_stride, d1 += row_stride) {
-                    const uint32_t w = src[row * 33];
-                    if (v0) *d0 = (uint16_t)(w & 0xFFFFu);
-                    if (v1) *d1 = (uint16_t)(w >> 16);
-                }
-            }
-        }
+        store_block(stage, c0, rows, row_stride, out_c, off_of);
         __syncwarp();
     }
+}
+
+// Stacked drain, lower half: the warp reads accumulator rows 64..95 or 96..127
+// (the second tap of each stacked group) and hands, per 32-column half block
+// starting at column c, the fp32 values of columns c+1 .. c+32 to its partner
+// through xbuf (32 rows x 33 words). Hand-over number k (counted over the whole
+// kernel in *k, identically by both warps) completes phase k of bar_full (32
+// arrivals: every lane releases its own writes); xbuf is reused once phase k-1
+// of bar_empty (the partner's 32 arrivals) has completed. Waits are bounded;
+// false means the CTA aborted.
+__device__ __forceinline__ bool drain_stacked_lower(uint32_t taddr, int c_begin, int c_end, float *xbuf,
+                                                    uint32_t bar_full, uint32_t bar_empty, uint32_t *k,
+                                                    const Ctl &ctl, uint32_t site) {
+    const int lane = threadIdx.x & 31;
+    for (int c0 = c_begin; c0 < c_end; c0 += 64) {
+        for (int half = 0; half < 2; ++half, ++*k) {
+            const int cc = c0 + 32 * half;
+            uint32_t r[32], extra;
+            tmem_ld32(taddr + (uint32_t)cc, r);
+            tmem_ld1(taddr + (uint32_t)(cc + 32), extra);
+            tmem_wait_ld();
+            if (*k > 0 && !warp_bar_wait(bar_empty, (*k - 1) & 1, ctl, site)) return false;
+#pragma unroll
+            for (int i = 0; i < 31; ++i) xbuf[lane * 33 + i] = __uint_as_float(r[i + 1]);
+            xbuf[lane * 33 + 31] = __uint_as_float(extra);
+            mbar_arrive(bar_full);
+        }
+    }
+    return true;
+}
+
+// Stacked drain, upper half: accumulator rows 0..63 plus the partner's shifted
+// values give the outputs; rounding, transpose and store as in drain_columns.
+template <typename OffFn>
+__device__ __forceinline__ bool drain_stacked_upper(uint32_t taddr, int c_begin, int c_end, uint32_t *stage,
+                                                    const float *xbuf, uint32_t bar_full, uint32_t bar_empty,
+                                                    uint32_t *k, const Ctl &ctl, uint32_t site, int rows,
+                                                    int64_t row_stride, int bf16, uint16_t *out_c, OffFn off_of) {
+    const int lane = threadIdx.x & 31;
+    for (int c0 = c_begin; c0 < c_end; c0 += 64) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half, ++*k) {
+            uint32_t r[32];
+            tmem_ld32(taddr + (uint32_t)(c0 + 32 * half), r);
+            tmem_wait_ld();
+            if (!warp_bar_wait(bar_full, *k & 1, ctl, site)) return false;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                stage[lane * 33 + half * 16 + i] =
+                    pack2(__uint_as_float(r[2 * i]) + xbuf[lane * 33 + 2 * i],
+                          __uint_as_float(r[2 * i + 1]) + xbuf[lane * 33 + 2 * i + 1], bf16);
+            mbar_arrive(bar_empty);
+        }
+        __syncwarp();
+        store_block(stage, c0, rows, row_stride, out_c, off_of);
+        __syncwarp();
+    }
+    return true;
 }
 
 }  // namespace tc

@@ -45,14 +45,20 @@ struct TParams {
     int RP;               // output rows per staged plane (H_o for whole planes, else T)
     int Wt, ctiles;       // columns per tile and column tiles per band (1 unless a row is too wide)
     uint32_t L;           // W_i * H_f
+    int in_cap;           // elements reserved for the staged input (the offset table follows)
     FastDiv div_L, div_Hf, div_RP;
 };
 
-template <typename E>
+constexpr int kMaxTableHf = 32;
+
+template <typename E, bool TABLE>
 __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     constexpr int V = 16 / sizeof(E);
     E *s_in = reinterpret_cast<E *>(smem_raw);
+    // offT[r0][i]: staged offset of element i of a vector whose first element is at
+    // row offset r0 of column w, from column w's top: ((r0 + i) % H_f) * Wc + (r0 + i) / H_f
+    int *offT = reinterpret_cast<int *>(smem_raw + (size_t)p.in_cap * sizeof(E));
 
     const E *__restrict__ x = static_cast<const E *>(p.x);
     E *__restrict__ win = static_cast<E *>(p.win);
@@ -108,6 +114,12 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
             s_in[e] = x[row0 + (int64_t)lr * p.W_i + c];
         }
     }
+    if (TABLE) {
+        for (int e = threadIdx.x; e < H_f * V; e += kThreads) {
+            const int r0 = e / V, i = e - r0 * V;
+            offT[e] = ((r0 + i) % H_f) * Wc + (r0 + i) / H_f;
+        }
+    }
     __syncthreads();
 
     // ---- write win[o0, o1): the piece's window rows (a column tile: one row segment)
@@ -141,22 +153,40 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
     const int nbody = (int)((a1 - a0) / V);
     uint4 *gv = reinterpret_cast<uint4 *>(win + a0);
     const int q_body = (int)(a0 - o0);
+    const int Lw = p.ctiles == 1 ? L : Wc * H_f;  // window row length within the piece
     for (int v = threadIdx.x; v < nbody; v += kThreads) {
         int idx = locate(q_body + v * V);
         uint32_t e[V];
+        if (TABLE && w * H_f + r + V <= Lw) {
+            // the vector stays in one window row: element i is at a fixed offset from
+            // the top of column w, given by the table row of r
+            const int top = idx - r * Wc;
+            int o[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-            e[i] = (uint32_t)sl[idx];
-            // next window position: r + 1, else the next column, else the next window row
-            if (++r < H_f) {
-                idx += Wc;
-            } else if (++w < Wc) {
-                r = 0;
-                idx += 1 - (H_f - 1) * Wc;
-            } else if (i + 1 < V) {
-                r = 0;
-                w = 0;
-                idx = row_base(++gh);
+            for (int j = 0; j < V / 4; ++j) {
+                const int4 t = reinterpret_cast<const int4 *>(offT + r * V)[j];
+                o[4 * j] = t.x;
+                o[4 * j + 1] = t.y;
+                o[4 * j + 2] = t.z;
+                o[4 * j + 3] = t.w;
+            }
+#pragma unroll
+            for (int i = 0; i < V; ++i) e[i] = (uint32_t)sl[top + o[i]];
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                e[i] = (uint32_t)sl[idx];
+                // next window position: r + 1, else the next column, else the next window row
+                if (++r < H_f) {
+                    idx += Wc;
+                } else if (++w < Wc) {
+                    r = 0;
+                    idx += 1 - (H_f - 1) * Wc;
+                } else if (i + 1 < V) {
+                    r = 0;
+                    w = 0;
+                    idx = row_base(++gh);
+                }
             }
         }
         uint4 out;
@@ -210,7 +240,13 @@ cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, 
     }
     const int64_t ctiles = (s.W_i + Wt - 1) / Wt;
     const int64_t tiles = (s.H_o + T - 1) / T;
-    const size_t smem = (size_t)(whole ? planes_bytes(PPC) : band_bytes(T, Wt));
+    const size_t staged = (size_t)(whole ? planes_bytes(PPC) : band_bytes(T, Wt));
+    const int V = 16 / esz;
+    // the table pays off when a vector spans several columns (H_f < V): there the
+    // stepping would wrap more than once per vector; otherwise its extra shared-memory
+    // loads cost more than the one wrap they save
+    const bool use_table = s.H_f < V && s.H_f <= kMaxTableHf;
+    const size_t smem = staged + (use_table ? (size_t)s.H_f * V * sizeof(int) : 0);
 
     TParams p;
     p.x = x;
@@ -229,23 +265,24 @@ cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, 
     p.Wt = (int)Wt;
     p.ctiles = (int)ctiles;
     p.L = (uint32_t)L;
+    p.in_cap = (int)(staged / esz);
     p.div_L = make_fastdiv((uint32_t)L);
     p.div_Hf = make_fastdiv((uint32_t)s.H_f);
     p.div_RP = make_fastdiv((uint32_t)T);
 
     const int64_t blocks = (NP + PPC - 1) / PPC * tiles * ctiles;
+    auto go = [&](auto kernel) -> cudaError_t {
+        const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        kernel<<<(unsigned)blocks, kThreads, smem, st>>>(p);
+        return cudaSuccess;
+    };
     cudaError_t e;
-    if (esz == 2) {
-        e = cudaFuncSetAttribute(transform_kernel<uint16_t>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        transform_kernel<uint16_t><<<(unsigned)blocks, kThreads, smem, st>>>(p);
-    } else {
-        e = cudaFuncSetAttribute(transform_kernel<uint32_t>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        transform_kernel<uint32_t><<<(unsigned)blocks, kThreads, smem, st>>>(p);
-    }
+    if (esz == 2)
+        e = use_table ? go(transform_kernel<uint16_t, true>) : go(transform_kernel<uint16_t, false>);
+    else
+        e = use_table ? go(transform_kernel<uint32_t, true>) : go(transform_kernel<uint32_t, false>);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -56,6 +56,40 @@ def test_conv_tc_exact_on_sparse_integers(dt, bound, fused):
     np.testing.assert_array_equal(to_f64(out), want)
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["window", "fused"])
+@pytest.mark.parametrize("case", [(2, 24, 30, 33, 40, 5, 3, 1, 2), (1, 40, 21, 29, 64, 7, 7, 2, 2),
+                                  (2, 17, 19, 40, 8, 3, 4, 1, 1)],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_conv_tc_stacked_taps_exact_on_integers(case, fused):
+    """Output channels <= 64: two filter taps share one MMA (the second tap's sum is
+    taken one column to the left and added back in the epilogue). On sparse integer
+    inputs every partial sum is exact, so the result must equal the oracle exactly."""
+    N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w = case
+    layer = wl.Layer("stk", N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, seed=8)
+    x, w = wl.make_int_inputs(layer, "f16", seed=23, x_range=1, w_range=1, density=0.5)
+    out = _run(x, w, (s_h, s_w), fused)
+    want, _ = oracle.conv_direct(to_f64(x), to_f64(w), (s_h, s_w))
+    assert np.abs(want).max() <= 2048
+    np.testing.assert_array_equal(to_f64(out), want)
+
+
+@pytest.mark.parametrize("r0,j0", [(3, 2), (5, 6), (0, 0), (6, 5)])
+def test_conv_tc_stacked_one_hot_is_exact_crop(r0, j0):
+    """A single non-zero filter tap with C_o <= 64 at a pair's top (j=0), bottom
+    (j=2: partner of 0 at stride 2), the last column's unpaired tap (j=6 at W_f=7,
+    s_w=2 pairs with nothing) and the other row/column phases."""
+    layer = wl.Layer("hot2", 2, 20, 33, 37, 48, 7, 7, 2, 2, seed=10)
+    x, _ = wl.make_inputs(layer, "bf16")
+    w = torch.zeros((48, 20, 7, 7), dtype=torch.bfloat16)
+    w[41, 13, r0, j0] = 1.0
+    for fused in (False, True):
+        out = _run(x, w, (2, 2), fused)
+        ho, wo = out.shape[2:]
+        crop = x[:, 13, r0:r0 + (ho - 1) * 2 + 1:2, j0:j0 + (wo - 1) * 2 + 1:2]
+        assert torch.equal(out[:, 41].cpu(), crop), f"fused={fused}"
+        assert not out[:, :41].any() and not out[:, 42:].any()
+
+
 def test_conv_tc_one_hot_filter_is_exact_crop():
     layer = wl.Layer("hot", 2, 20, 33, 37, 130, 4, 5, 2, 3, seed=9)
     x, _ = wl.make_inputs(layer, "bf16")
