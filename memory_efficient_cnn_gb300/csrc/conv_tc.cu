@@ -377,9 +377,17 @@ __device__ __forceinline__ void tile_at(const TapParams &p, int64_t id, TapTile 
 }
 
 // MMA split of a tile's NTp positions into two accumulators [0, N0) and
-// [N0, NTp) so that consecutive MMAs never wait on each other.
+// [N0, NTp) so that consecutive MMAs never wait on each other; N0 is a multiple
+// of 32 so that each accumulator's columns start on a 32-column TMEM load. The
+// boundary is the same for every tile of a launch (that of the widest tile):
+// an accumulator is released as soon as it is drained, so the next tile's MMAs
+// into it must not reach columns of the other, possibly still draining, one.
+// A narrower tile may leave the second accumulator empty.
 __device__ __forceinline__ int split_n0(int NTp) {
-    return NTp >= 32 ? (NTp / 2 + 15) / 16 * 16 : NTp;
+    return NTp >= 32 ? min(NTp, (NTp / 2 + 31) / 32 * 32) : NTp;
+}
+__device__ __forceinline__ int tile_n0(const TapParams &p, int NTp) {
+    return min(NTp, split_n0((p.Qmax * p.pitch + p.stack + 15) / 16 * 16));
 }
 
 template <int MODE>
@@ -422,9 +430,9 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                                                 ((size_t)p.raw_elems * 2 + 127) / 128 * 128);
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sE) + TAP_EPI_BYTES);
     // [A stages][slab stages][raw rows (W modes)][epilogue staging] then
-    // bars: full_a[AST] | empty_a[AST] | full_b[BST] | empty_b[BST] | tmem_full | tmem_empty | drain
-    //       | stacked hand-over: full[4] | empty[4]
-    const int nb = 2 * p.AST + 2 * p.BST + 3 + 8;
+    // bars: full_a[AST] | empty_a[AST] | full_b[BST] | empty_b[BST] | tmem_full[2] | tmem_empty[2]
+    //       | drain | stacked hand-over: full[4] | empty[4]
+    const int nb = 2 * p.AST + 2 * p.BST + 5 + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + nb);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
     uint32_t *toff = reinterpret_cast<uint32_t *>(bars + nb + 1);  // [T] tap offsets (16-byte units)
@@ -440,11 +448,13 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     auto empty_a = [&](int s) { return smem_u32(bars + p.AST + s); };
     auto full_b = [&](int s) { return smem_u32(bars + 2 * p.AST + s); };
     auto empty_b = [&](int s) { return smem_u32(bars + 2 * p.AST + p.BST + s); };
-    const uint32_t tmem_full = smem_u32(bars + 2 * p.AST + 2 * p.BST);
-    const uint32_t tmem_empty = smem_u32(bars + 2 * p.AST + 2 * p.BST + 1);
-    const uint32_t drain = smem_u32(bars + 2 * p.AST + 2 * p.BST + 2);
-    auto xfull = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 3 + i); };
-    auto xempty = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 7 + i); };
+    // one full / empty pair per accumulator: the epilogue drains accumulator 0 and
+    // then 1, so each issuer restarts as soon as its own accumulator is drained
+    auto tmem_full = [&](int a) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + a); };
+    auto tmem_empty = [&](int a) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 2 + a); };
+    const uint32_t drain = smem_u32(bars + 2 * p.AST + 2 * p.BST + 4);
+    auto xfull = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 5 + i); };
+    auto xempty = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 9 + i); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.AST; ++s) {
@@ -455,8 +465,10 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             mbar_init(full_b(s), TAP_PROD_WARPS * 32);
             mbar_init(empty_b(s), 2);
         }
-        mbar_init(tmem_full, 2);
-        mbar_init(tmem_empty, TAP_EPI_WARPS);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tmem_full(a), 1);
+            mbar_init(tmem_empty(a), TAP_EPI_WARPS);
+        }
         mbar_init(drain, 2);
         for (int i = 0; i < 4; ++i) {
             mbar_init(xfull(i), 32);
@@ -504,12 +516,12 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 tile_at(p, id, tl);
                 if (k > 0) {
                     // the previous tile's accumulators must be drained
-                    if (!(ok = bar_wait(tmem_empty, (k - 1) & 1, ctl, SITE_EMPTY_MMA))) break;
+                    if (!(ok = bar_wait(tmem_empty(which), (k - 1) & 1, ctl, SITE_EMPTY_MMA))) break;
                     tc_fence_after();
                 }
                 // stacked: one more column, read by the epilogue for the shifted rows
                 const int NTp = (tl.Q * p.pitch + p.stack + 15) / 16 * 16;
-                const int N0 = split_n0(NTp);
+                const int N0 = tile_n0(p, NTp);
                 const int NW = which == 0 ? N0 : NTp - N0;          // this issuer's columns
                 const uint32_t col0 = which == 0 ? 0u : (uint32_t)N0;
                 const uint32_t idesc = make_idesc(p.bf16 != 0, BM, NW > 0 ? NW : 16);
@@ -538,7 +550,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     if (ok) mma_commit(empty_b(sb));
                     if (++sb == p.BST) { sb = 0; phb ^= 1; }
                 }
-                if (ok) mma_commit(tmem_full);
+                if (ok) mma_commit(tmem_full(which));
                 ++k;
             }
             // let every MMA in flight finish before the CTA tears down
@@ -817,14 +829,9 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         TapTile tl;
         for (int64_t id = blockIdx.x; id < p.tiles_total; id += gridDim.x) {
             tile_at(p, id, tl);
-            if (!warp_bar_wait(tmem_full, k & 1, ctl, SITE_DONE)) break;
-            tc_fence_after();
             const int NT = tl.Q * p.pitch;
-            const int NTp = (NT + 15) / 16 * 16;
-            // the two warps of a quarter split the columns in 64-column blocks
-            const int nb64 = (NTp + 63) / 64;
-            const int c_begin = hh == 0 ? 0 : ((nb64 + 1) / 2) * 64;
-            const int c_end = hh == 0 ? min(NTp, ((nb64 + 1) / 2) * 64) : NTp;
+            const int NTp = (NT + p.stack + 15) / 16 * 16;  // the MMAs' columns
+            const int N0 = tile_n0(p, NTp);
             const int pitch = p.pitch, W_o = p.W_o;
             auto off_of = [&](int pp) -> int {
                 const int qrow = pp / pitch;
@@ -832,32 +839,65 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 return (pp < NT && wo < W_o) ? qrow * W_o + wo : -1;
             };
             const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16);
+            // the two warps of a quarter split a column range in 64-column blocks
+            auto half_range = [&](int a0, int a1, int &cb, int &ce) {
+                const int nb = (a1 - a0 + 63) / 64;
+                const int mid = a0 + ((nb + 1) / 2) * 64;
+                cb = hh == 0 ? a0 : mid;
+                ce = hh == 0 ? min(a1, mid) : a1;
+            };
+            bool ok = true;
             if (!p.stack) {
                 const int co0 = tl.mt * BM + q4 * 32;
                 uint16_t *out_c = p.out + ((int64_t)tl.n * p.C_o + co0) * plane + (int64_t)tl.ho0 * p.W_o;
-                drain_columns(taddr, c_begin, c_end, stage, min(32, p.C_o - co0), plane, p.bf16, out_c, off_of);
+                for (int a = 0; a < 2 && ok; ++a) {
+                    if (!(ok = warp_bar_wait(tmem_full(a), k & 1, ctl, SITE_DONE))) break;
+                    tc_fence_after();
+                    int cb, ce;
+                    half_range(a == 0 ? 0 : N0, a == 0 ? N0 : NTp, cb, ce);
+                    // a block may reach past the range (into the other accumulator, which
+                    // may still be accumulating): only columns of the range are stored
+                    drain_columns(taddr, cb, ce, stage, min(32, p.C_o - co0), plane, p.bf16, out_c,
+                                  [&](int pp) -> int { return pp < ce ? off_of(pp) : -1; });
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tmem_empty(a));
+                }
             } else {
-                // warps of quarters 2, 3 (rows 64..127) feed the warps of quarters 0, 1
+                // the shifted add reads one column across the accumulators' boundary:
+                // both accumulators are drained together.
+                // Warps of quarters 2, 3 (rows 64..127) feed the warps of quarters 0, 1
                 // (same channels, rows 0..63) of the same column half through the
                 // lower warp's staging area and the pair's two mbarriers
-                const int pair = (q4 & 1) + 2 * hh;
-                bool dok;
-                if (q4 >= 2) {
-                    dok = drain_stacked_lower(taddr, c_begin, c_end, reinterpret_cast<float *>(stage), xfull(pair),
-                                              xempty(pair), &xk, ctl, SITE_STACK);
-                } else {
-                    const int co0 = q4 * 32;
-                    uint16_t *out_c = p.out + ((int64_t)tl.n * p.C_o + co0) * plane + (int64_t)tl.ho0 * p.W_o;
-                    const float *xbuf = reinterpret_cast<const float *>(sE + (ew - 2) * (32 * 33));
-                    dok = drain_stacked_upper(taddr, c_begin, c_end, stage, xbuf, xfull(pair), xempty(pair), &xk,
-                                              ctl, SITE_STACK, max(0, min(32, p.C_o - co0)), plane, p.bf16,
-                                              out_c, off_of);
+                ok = warp_bar_wait(tmem_full(0), k & 1, ctl, SITE_DONE) &&
+                     warp_bar_wait(tmem_full(1), k & 1, ctl, SITE_DONE);
+                if (ok) {
+                    tc_fence_after();
+                    int cb, ce;
+                    half_range(0, (NT + 15) / 16 * 16, cb, ce);
+                    const int pair = (q4 & 1) + 2 * hh;
+                    if (q4 >= 2) {
+                        ok = drain_stacked_lower(taddr, cb, ce, reinterpret_cast<float *>(stage), xfull(pair),
+                                                 xempty(pair), &xk, ctl, SITE_STACK);
+                    } else {
+                        const int co0 = q4 * 32;
+                        uint16_t *out_c = p.out + ((int64_t)tl.n * p.C_o + co0) * plane + (int64_t)tl.ho0 * p.W_o;
+                        const float *xbuf = reinterpret_cast<const float *>(sE + (ew - 2) * (32 * 33));
+                        ok = drain_stacked_upper(taddr, cb, ce, stage, xbuf, xfull(pair), xempty(pair), &xk, ctl,
+                                                 SITE_STACK, max(0, min(32, p.C_o - co0)), plane, p.bf16, out_c,
+                                                 off_of);
+                    }
                 }
-                if (!dok) break;
+                if (ok) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(tmem_empty(0));
+                        mbar_arrive(tmem_empty(1));
+                    }
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tmem_empty);
+            if (!ok) break;
             ++k;
         }
     }

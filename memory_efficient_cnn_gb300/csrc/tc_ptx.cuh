@@ -279,6 +279,8 @@ __device__ __forceinline__ void store_block(const uint32_t *stage, int c0, int r
 // 64 columns: two 32-column TMEM loads (the next block's first load is in
 // flight while this block is stored), rounding to fp16/bf16, a transpose
 // through the warp's staging area (32 rows x 33 words), then store_block.
+// The last block may reach past c_end: off_of must return -1 for its columns
+// that are not the warp's to store.
 template <typename OffFn>
 __device__ __forceinline__ void drain_columns(uint32_t taddr, int c_begin, int c_end, uint32_t *stage,
                                               int rows, int64_t row_stride, int bf16,
