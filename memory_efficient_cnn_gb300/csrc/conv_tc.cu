@@ -438,6 +438,21 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     uint32_t *toff = reinterpret_cast<uint32_t *>(bars + nb + 1);  // [T] tap offsets (16-byte units)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // W modes: per K chunk row c and element e of a slab entry, the raw offset
+    // from the entry's base and the limit on m*mstride below which it exists
+    int *wtab = reinterpret_cast<int *>((reinterpret_cast<uintptr_t>(toff + p.T) + 15) & ~(uintptr_t)15);
+    if (MODE != TAP_CH) {
+        for (int b = threadIdx.x; b < 16 * p.U; b += blockDim.x) {
+            if (MODE == TAP_WX) {
+                const int jl = b / p.H_f, r = b - jl * p.H_f;
+                wtab[b] = r * p.W_i + jl;
+                wtab[16 * p.U + b] = b < p.S ? p.W_i - jl : 0;  // column m*s_w + jl < W_i
+            } else {
+                wtab[b] = b;
+                wtab[16 * p.U + b] = b < p.S ? (int)p.L - b : 0;  // window index m*S + b < L
+            }
+        }
+    }
     for (int t = threadIdx.x; t < p.T; t += blockDim.x) {
         // a stacked group is issued at its top tap
         const int tap = p.stack ? (t / p.Gr) * p.W_f + stacked_top_j(t % p.Gr, p.s_w) : t;
@@ -767,20 +782,16 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 const int mstride = MODE == TAP_WX ? p.s_w : p.S;
                 for (int c = 0; c < SC; ++c) {
                     // element e of an entry: raw offset boff[e] from the entry's base, present
-                    // if b = 8c + e < S and its column (WX) / window index (WW) is < lim[e] - m*mstride
+                    // if m*mstride < lim[e] (the per-CTA table of the prologue)
                     int boff[8], lim[8];
-                    int jl = (8 * c) / p.H_f, r = 8 * c - jl * p.H_f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int b = 8 * c + e;
-                        if (MODE == TAP_WX) {
-                            boff[e] = r * p.W_i + jl;
-                            lim[e] = b < p.S ? p.W_i - jl : 0;  // column m*s_w + jl < W_i
-                            if (++r == p.H_f) { r = 0; ++jl; }
-                        } else {
-                            boff[e] = b;
-                            lim[e] = b < p.S ? (int)p.L - b : 0;  // window index m*S + b < L
-                        }
+                    {
+                        const int4 *tb = reinterpret_cast<const int4 *>(wtab + 8 * c);
+                        const int4 *tl4 = reinterpret_cast<const int4 *>(wtab + 16 * p.U + 8 * c);
+                        const int4 b0 = tb[0], b1 = tb[1], l0 = tl4[0], l1 = tl4[1];
+                        boff[0] = b0.x; boff[1] = b0.y; boff[2] = b0.z; boff[3] = b0.w;
+                        boff[4] = b1.x; boff[5] = b1.y; boff[6] = b1.z; boff[7] = b1.w;
+                        lim[0] = l0.x; lim[1] = l0.y; lim[2] = l0.z; lim[3] = l0.w;
+                        lim[4] = l1.x; lim[5] = l1.y; lim[6] = l1.z; lim[7] = l1.w;
                     }
                     uint8_t *slab_c = slab + (size_t)c * p.lbo;
                     for (int i = pt; i < per_c; i += NPT) {
@@ -1089,7 +1100,7 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
             for (int BST : {3, 2}) {
               for (int AST : {3, 2, 4}) {
                     int64_t total = (int64_t)AST * tg * TAP_A_BYTES + BST * stage_b + raw_e * 2 +
-                                    TAP_EPI_BYTES + 512 + 4 * T;
+                                    TAP_EPI_BYTES + 512 + 4 * T + 16 + 128 * U;
                     if (total > smem_max) continue;
                     // the 512-column TMEM accumulator needs the SM to itself
                     total = std::max<int64_t>(total, 120 * 1024);
