@@ -56,10 +56,10 @@ constexpr int K_ALIGN = 48;
 #define F32_CFG_96 96, 24, 3, 2
 #endif
 #ifndef F32_CFG_64
-#define F32_CFG_64 64, 16, 3, 4
+#define F32_CFG_64 64, 16, 3, 3
 #endif
 #ifndef F32_CFG_32
-#define F32_CFG_32 32, 16, 3, 4
+#define F32_CFG_32 32, 8, 3, 4
 #endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -84,16 +84,23 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // memory, so no registers hold prefetched data). The filter slice arrives as
 // 16-byte vectors. The 4-byte gathers follow the contiguous direction of the
 // source: from the window tensor consecutive k of a pixel are consecutive
-// elements, so thread t gathers k = t % KC of pixels t / KC + i*(NT/KC); from the
-// NCHW input consecutive pixels of a row are (unit stride), so lane l of warp w
+// elements, so a warp's copy covers 8 consecutive k of 4 pixels (lane l: k
+// offset l % 8, pixel offset l / 8) -- 32-byte runs in global memory and, with
+// the 4-word padding of a shared row, 32 distinct banks; warp w keeps k group
+// w % (KC/8) and walks every (NW/(KC/8))-th group of 4 pixels. From the NCHW
+// input consecutive pixels of a row are (unit stride), so lane l of warp w
 // gathers pixels l + 32i at the KPT values of k w*KPT ...
 template <int TM, int KC, int STAGES, int MINB, bool FROM_X>
 __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
     constexpr int NT = TM * 2;                 // (TM/8) x 16 threads
-    constexpr int PPT = FROM_X ? TP / 32 : KC * TP / NT;  // pixels each thread gathers
+    constexpr int NW = NT / 32;                           // warps
+    constexpr int KG = KC / 8;                            // window path: 8-k groups per chunk
+    constexpr int PPT = FROM_X ? TP / 32 : TP * KG / (4 * NW);  // pixels each thread gathers
     constexpr int KPT = FROM_X ? KC * 32 / NT : 1;        // k values each thread gathers
     constexpr int B_VEC = KC * TM / 4 / NT;    // 16-byte filter vectors each thread stages
-    static_assert((FROM_X ? KPT * (NT / 32) == KC : NT % KC == 0) && (KC * TM / 4) % NT == 0, "tile");
+    static_assert((FROM_X ? KPT * NW == KC : (KC % 8 == 0 && NW % KG == 0 && PPT * 4 * NW == TP * KG)) &&
+                      (KC * TM / 4) % NT == 0 && (TP + 4) % 32 == 4,
+                  "tile");
     static_assert(K_ALIGN % KC == 0, "filter padding");
     extern __shared__ __align__(16) float smem_f[];
     float (*As)[KC][TP + 4] = reinterpret_cast<float (*)[KC][TP + 4]>(smem_f);
@@ -108,9 +115,9 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
 
     // ---- staging coordinates
     // thread's first pixel, pixel step, first k and shared-memory row/column
-    const int px0 = FROM_X ? (tid & 31) : tid / KC;
-    constexpr int PXS = FROM_X ? 32 : NT / KC;
-    const int k0 = FROM_X ? (tid >> 5) * KPT : tid % KC;
+    const int px0 = FROM_X ? (tid & 31) : ((tid >> 5) / KG) * 4 + ((tid & 31) >> 3);
+    constexpr int PXS = FROM_X ? 32 : 4 * (NW / KG);
+    const int k0 = FROM_X ? (tid >> 5) * KPT : ((tid >> 5) % KG) * 8 + (tid & 7);
     int pos_off[PPT];     // offset of the pixel's window segment; pixels past P read offset 0, size 0
     uint32_t pos_ok = 0;  // bit i: pixel i exists
 #pragma unroll
