@@ -476,8 +476,10 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             mbar_init(full_a(s), 1);
             mbar_init(empty_a(s), 2);  // both MMA issuers commit
         }
+        // a slab stage is filled by one producer group (all producers when there is one)
+        const bool one_group = !(MODE == TAP_CH && (p.ring || p.stack));
         for (int s = 0; s < p.BST; ++s) {
-            mbar_init(full_b(s), TAP_PROD_WARPS * 32);
+            mbar_init(full_b(s), one_group ? TAP_PROD_WARPS * 32 : TAP_PROD_WARPS * 16);
             mbar_init(empty_b(s), 2);
         }
         for (int a = 0; a < 2; ++a) {
@@ -606,15 +608,22 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         // ---------------- slab producers
         // Chunks are walked in order (tile by tile, NCH per tile). Their source rows
         // are contiguous in global memory; where a raw staging area exists they are
-        // copied there by cp.async -- with a ring of two slots the next chunk's copy
-        // is in flight while this chunk is re-laid -- and the slab is built from
-        // shared memory. Without one (TAP_CH whose rows are not 16-byte aligned, or
-        // whose staging does not fit) the slab is gathered straight from global memory.
-        const int pt = threadIdx.x - 64;
-        constexpr int NPT = TAP_PROD_WARPS * 32;
-        typedef uint16_t E16;
+        // copied there by cp.async and the slab is built from shared memory. Without
+        // one (TAP_CH whose rows are not 16-byte aligned, or whose staging does not
+        // fit) the slab is gathered straight from global memory. For TAP_CH with a raw
+        // ring or with tap stacking a chunk's fill is mostly latency (copy, barriers,
+        // shared-memory round trips), so the producers form two groups of four warps
+        // that fill alternate chunks at the same time, each with its own raw slot and
+        // named barrier. Otherwise all eight warps fill every chunk, and with two raw
+        // slots the next chunk's copy is in flight while this one is re-laid.
         const bool staged = MODE != TAP_CH || p.ring;
-        const int nslots = p.ring ? 2 : 1;
+        const int ngroups = (MODE == TAP_CH && (p.ring || p.stack)) ? 2 : 1;
+        const bool prefetch = ngroups == 1 && staged && p.ring;
+        const int grp = ngroups == 2 ? (warp - 2) / (TAP_PROD_WARPS / 2) : 0;
+        const int NPT = TAP_PROD_WARPS * 32 / ngroups;  // threads of the group
+        const int pt = (threadIdx.x - 64) % NPT;         // thread within the group
+        const int bar_id = 1 + grp;
+        typedef uint16_t E16;
         bool pok = true;
         int sb = 0;
         uint32_t phb = 0;
@@ -675,27 +684,34 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         int cc = 0;
         TapTile tl;
         if (id < p.tiles_total) tile_at(p, id, tl);
-        if (staged && id < p.tiles_total) issue_raw(tl, cc, 0);
+        if (prefetch && id < p.tiles_total) issue_raw(tl, cc, 0);
         cp_async_commit_group();
         for (int g = 0; id < p.tiles_total; ++g, next_chunk(id, cc, tl)) {
-            const int slot = nslots == 2 ? (g & 1) : 0;
-            if (staged) {
-                if (nslots == 2) {
-                    int64_t id2 = id;
-                    int cc2 = cc;
-                    TapTile t2 = tl;
-                    next_chunk(id2, cc2, t2);
-                    if (pok && id2 < p.tiles_total) issue_raw(t2, cc2, slot ^ 1);
-                    cp_async_commit_group();
-                    cp_async_wait_group<1>();
-                } else {
-                    cp_async_wait_group<0>();
-                }
-                asm volatile("bar.sync 1, %0;" ::"r"(NPT) : "memory");
+            // slab stage of chunk g, advanced for every chunk
+            const int sb_g = sb;
+            const uint32_t ph_g = phb;
+            if (++sb == p.BST) { sb = 0; phb ^= 1; }
+            if (ngroups == 2 && (g & 1) != grp) continue;  // the other group's chunk
+            const int slot = prefetch ? (g & 1) : grp;
+            if (prefetch) {
+                // the next chunk's copy into the other slot, then wait for this one
+                int64_t id2 = id;
+                int cc2 = cc;
+                TapTile t2 = tl;
+                next_chunk(id2, cc2, t2);
+                if (pok && id2 < p.tiles_total) issue_raw(t2, cc2, slot ^ 1);
+                cp_async_commit_group();
+                cp_async_wait_group<1>();
+                asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(NPT) : "memory");
+            } else if (staged) {
+                if (pok) issue_raw(tl, cc, slot);
+                cp_async_commit_group();
+                cp_async_wait_group<0>();
+                asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(NPT) : "memory");
             }
             const int n = tl.n, ho0 = tl.ho0, Q = tl.Q;
-            if (pok) pok = warp_bar_wait(empty_b(sb), phb ^ 1, ctl, SITE_EMPTY_PROD);
-            uint8_t *slab = sB + (size_t)sb * p.stage_b;
+            if (pok) pok = warp_bar_wait(empty_b(sb_g), ph_g ^ 1, ctl, SITE_EMPTY_PROD);
+            uint8_t *slab = sB + (size_t)sb_g * p.stage_b;
             const E16 *raw_slot = sRaw + (size_t)slot * p.raw_slot;
             if (!pok) {
                 // aborted: keep meeting the producers' barrier, do no work
@@ -810,20 +826,11 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             }
             if (pok) {
                 fence_async_smem();
-                mbar_arrive(full_b(sb));
+                mbar_arrive(full_b(sb_g));
             }
-            if (++sb == p.BST) { sb = 0; phb ^= 1; }
             if (staged) {
-                // the raw slot is consumed: the copy of a later chunk may overwrite it
-                asm volatile("bar.sync 1, %0;" ::"r"(NPT) : "memory");
-                if (nslots == 1) {
-                    int64_t id2 = id;
-                    int cc2 = cc;
-                    TapTile t2 = tl;
-                    next_chunk(id2, cc2, t2);
-                    if (pok && id2 < p.tiles_total) issue_raw(t2, cc2, 0);
-                    cp_async_commit_group();
-                }
+                // the raw slot is consumed: the group's next copy may overwrite it
+                asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(NPT) : "memory");
             }
             if (MODE == TAP_CH && !staged && !pok) break;
         }
