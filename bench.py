@@ -126,6 +126,24 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(values, dist_mod=None, device=None):
+    """Each value's maximum over the ranks of the process group (the values
+    themselves when there is no group): the job's time is its slowest rank's."""
+    if dist_mod is None:
+        return [float(v) for v in values]
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_tflops(world: int, flops_per_rank_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs its own batch (weak scaling), all in
+    the time of the slowest rank."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def conv_flops(layer) -> float:
     ho = (layer.H_i - layer.H_f) // layer.s_h + 1
     wo = (layer.W_i - layer.W_f) // layer.s_w + 1
@@ -383,17 +401,15 @@ def main():
     e2e_ms = e_start.elapsed_time(e_end)
 
     if dist:
-        t = torch.tensor([step_ms, e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, e2e_ms = float(t[0]), float(t[1])
+        step_ms, e2e_ms = max_over_ranks([step_ms, e2e_ms], dist, dev)
         dist.destroy_process_group()
     if rank != 0:
         return
 
     f = conv_flops(layer)
     ms = step_ms / args.steps
-    value = world * n_convs * f / (ms * 1e-3) / 1e12
-    e2e_value = world * n_convs * f / (e2e_ms / args.steps * 1e-3) / 1e12
+    value = job_tflops(world, n_convs * f, ms)
+    e2e_value = job_tflops(world, n_convs * f, e2e_ms / args.steps)
     pk = _peaks()
     fp32_peak = SMS * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12  # FFMA lanes x 2 flop x clock
     esz = {"f16": 2, "bf16": 2, "f32": 4}
