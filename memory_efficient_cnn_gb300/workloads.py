@@ -62,7 +62,7 @@ SWEEP = tuple(
 CV2 = Layer("cv2", 128, 3, 231, 231, 96, 11, 11, 4, 4, seed=5, dtypes=("f16", "f32"))
 CV3 = Layer("cv3", 128, 3, 227, 227, 64, 7, 7, 2, 2, seed=6, dtypes=("f16", "f32"))
 
-ALL = (TINY, CV1, CV4, CV5) + SWEEP
+ALL = (TINY, CV1, CV4, CV5) + SWEEP + (CV2, CV3)
 
 
 def make_inputs(layer: Layer, dtype: str, seed: int | None = None, n_images: int | None = None):

@@ -55,7 +55,7 @@ def test_conv_f32_tiny_config():
         check_full(out, x, w, (1, 1), f"tiny fused={fused}")
 
 
-@pytest.mark.parametrize("layer", [wl.CV1] + list(wl.SWEEP), ids=lambda l: l.name)
+@pytest.mark.parametrize("layer", [wl.CV1, wl.CV2, wl.CV3] + list(wl.SWEEP), ids=lambda l: l.name)
 def test_conv_f32_full_size_sampled(layer):
     x, w = wl.make_inputs(layer, "f32")
     stride = (layer.s_h, layer.s_w)

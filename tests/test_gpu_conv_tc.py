@@ -103,7 +103,8 @@ def test_conv_tc_one_hot_filter_is_exact_crop():
         assert not out[:, :77].any() and not out[:, 78:].any()
 
 
-@pytest.mark.parametrize("layer,dt", [(wl.CV1, "f16"), (wl.CV4, "f16"), (wl.CV5, "bf16")]
+@pytest.mark.parametrize("layer,dt", [(wl.CV1, "f16"), (wl.CV2, "f16"), (wl.CV3, "f16"), (wl.CV4, "f16"),
+                                      (wl.CV5, "bf16")]
                          + [(l, "bf16") for l in wl.SWEEP], ids=lambda v: getattr(v, "name", v))
 def test_conv_tc_full_size_sampled(layer, dt):
     x, w = wl.make_inputs(layer, dt)

@@ -63,7 +63,8 @@ def test_transform_does_not_write_past_the_window():
     assert _raw(buf[:n]).tobytes() == oracle.im2win(_raw(x), H_f, s_h).tobytes()
 
 
-@pytest.mark.parametrize("layer,dt", [(wl.CV1, "f16"), (wl.CV1, "f32"), (wl.CV5, "bf16")]
+@pytest.mark.parametrize("layer,dt", [(wl.CV1, "f16"), (wl.CV1, "f32"), (wl.CV2, "f16"), (wl.CV3, "f32"),
+                                      (wl.CV5, "bf16")]
                          + [(l, "bf16") for l in wl.SWEEP], ids=lambda v: getattr(v, "name", v))
 def test_transform_full_size_bit_exact(layer, dt):
     x, _ = wl.make_inputs(layer, dt)
