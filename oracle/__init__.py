@@ -13,6 +13,12 @@ Each wrapper names the passage of the method it follows:
   Efficient Convolution On SIMD Architectures" and Fig. 1 middle column.
 * ``conv_im2win`` -- convolution as dot products over window segments (same).
 * ``conv_im2col`` -- im2col + GEMM, Fig. 1 right column.
+* ``im2win_nhwc`` / ``conv_im2win_nhwc`` -- the same two steps with channels
+  innermost (x[N][H_i][W_i][C_i], win[N][H_o][W_i*H_f][C_i],
+  out[N][H_o][W_o][C_o]); the [SIMD] page names a successor work on three
+  tensor layouts by title only, and this is the plainest reading of it.
+* ``conv_direct_nhwc`` / ``conv_points_nhwc`` -- the direct sums above on
+  channels-last tensors: a transpose to NCHW, the NCHW routine, a transpose back.
 
 Inputs are numpy arrays; floating inputs are widened to float64 exactly before
 the call (the caller has already rounded them to the dtype under test).
@@ -64,8 +70,11 @@ def _load():
             lib.oracle_conv_im2win.argtypes = [_PD, _PD, _PD] + shp
             lib.oracle_conv_im2col.argtypes = [_PD, _PD, _PD] + shp
             lib.oracle_im2win.argtypes = [ctypes.c_void_p, ctypes.c_void_p] + [_I64] * 6
+            lib.oracle_im2win_nhwc.argtypes = [ctypes.c_void_p, ctypes.c_void_p] + [_I64] * 6
+            lib.oracle_conv_im2win_nhwc.argtypes = [_PD, _PD, _PD] + shp
             for f in (lib.oracle_conv_direct, lib.oracle_conv_points, lib.oracle_conv_im2win,
-                      lib.oracle_conv_im2col, lib.oracle_im2win):
+                      lib.oracle_conv_im2col, lib.oracle_im2win, lib.oracle_im2win_nhwc,
+                      lib.oracle_conv_im2win_nhwc):
                 f.restype = ctypes.c_int
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -165,3 +174,58 @@ def workspace_elems(x_shape, w_shape, stride):
     _, _, hf, wf = w_shape
     _, _, ho, wo = out_shape(x_shape, w_shape, stride)
     return n * ci * hi * wi, n * ci * ho * wi * hf, n * ci * hf * wf * ho * wo
+
+
+# ---- channels-last (NHWC) layouts
+
+def _nchw(a):
+    return np.ascontiguousarray(np.transpose(a, (0, 3, 1, 2)))
+
+
+def _nhwc(a):
+    return np.ascontiguousarray(np.transpose(a, (0, 2, 3, 1)))
+
+
+def out_shape_nhwc(x_shape, w_shape, stride):
+    n, hi, wi, ci = x_shape
+    n2, co, ho, wo = out_shape((n, ci, hi, wi), w_shape, stride)
+    return (n2, ho, wo, co)
+
+
+def conv_direct_nhwc(x, w, stride=(1, 1)):
+    """conv_direct on x[N][H_i][W_i][C_i]; returns (out, S) as [N][H_o][W_o][C_o]."""
+    out, scale = conv_direct(_nchw(_f64(x)), w, stride)
+    return _nhwc(out), _nhwc(scale)
+
+
+def conv_points_nhwc(x, w, idx, stride=(1, 1)):
+    """conv_points on x[N][H_i][W_i][C_i] at coordinates idx[t] = (n, ho, wo, co)."""
+    idx = np.asarray(idx, dtype=np.int64).reshape(-1, 4)
+    return conv_points(_nchw(_f64(x)), w, idx[:, [0, 3, 1, 2]], stride)
+
+
+def im2win_nhwc(x, H_f, s_h):
+    """Window tensor win[n][ho][w*H_f + r][c] = x[n][ho*s_h + r][w][c], same dtype, byte copy."""
+    x = np.ascontiguousarray(x)
+    n, hi, wi, ci = x.shape
+    ho = (hi - H_f) // s_h + 1
+    win = np.empty((n, ho, wi * H_f, ci), dtype=x.dtype)
+    rc = _load().oracle_im2win_nhwc(x.ctypes.data, win.ctypes.data, x.dtype.itemsize,
+                                    n, ci, hi, wi, H_f, s_h)
+    if rc:
+        raise ValueError("oracle_im2win_nhwc: bad shape")
+    return win
+
+
+def conv_im2win_nhwc(x, w, stride=(1, 1)):
+    """Convolution through the fp64 channels-last window tensor; out[N][H_o][W_o][C_o]."""
+    x, w = _f64(x), _f64(w)
+    n, hi, wi, ci = x.shape
+    win = im2win_nhwc(x, w.shape[2], stride[0])
+    out = np.empty(out_shape_nhwc(x.shape, w.shape, stride), np.float64)
+    co, _, hf, wf = w.shape
+    rc = _load().oracle_conv_im2win_nhwc(_dp(win), _dp(w), _dp(out), n, ci, hi, wi, co, hf, wf,
+                                         stride[0], stride[1])
+    if rc:
+        raise ValueError("oracle_conv_im2win_nhwc: bad shape")
+    return out

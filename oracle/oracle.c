@@ -235,3 +235,73 @@ int oracle_conv_im2col(const double *x, const double *w, double *out,
     free(col);
     return 0;
 }
+
+/*
+ * Channels-last (NHWC) layouts. The successor work that carries im2win to
+ * several tensor layouts survives on the [SIMD] page as a title only
+ * ("... im2win and direct convolutions using three tensor layouts ..."), so
+ * the reading taken here is the plainest one: the NCHW window row keeps its
+ * order and every element of it becomes the C_i channels of that position,
+ * innermost:
+ *   x[N][H_i][W_i][C_i],  out[N][H_o][W_o][C_o],  filter w[C_o][C_i][H_f][W_f] as above,
+ *   win[n][ho][w*H_f + r][c] = x[n][ho*s_h + r][w][c].
+ * Byte copy of esz-byte elements, like oracle_im2win.
+ */
+int oracle_im2win_nhwc(const void *x, void *win, int64_t esz,
+                       int64_t N, int64_t C_i, int64_t H_i, int64_t W_i,
+                       int64_t H_f, int64_t s_h)
+{
+    if (esz <= 0 || N < 0 || C_i <= 0 || H_i <= 0 || W_i <= 0 || H_f <= 0 || s_h <= 0 || H_f > H_i)
+        return -1;
+    const unsigned char *src = (const unsigned char *)x;
+    unsigned char *dst = (unsigned char *)win;
+    int64_t H_o = (H_i - H_f) / s_h + 1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t ho = 0; ho < H_o; ++ho)
+            for (int64_t w = 0; w < W_i; ++w)
+                for (int64_t r = 0; r < H_f; ++r)
+                    for (int64_t c = 0; c < C_i; ++c) {
+                        int64_t d = ((n * H_o + ho) * W_i * H_f + w * H_f + r) * C_i + c;
+                        int64_t s = ((n * H_i + ho * s_h + r) * W_i + w) * C_i + c;
+                        memcpy(dst + d * esz, src + s * esz, (size_t)esz);
+                    }
+    return 0;
+}
+
+/*
+ * Convolution over the channels-last window tensor: the window row of output
+ * row ho is one contiguous run of W_i*H_f*C_i elements, and output pixel wo is
+ * the dot product of the segment that starts at wo*s_w*H_f*C_i with the filter
+ * re-laid in the same (column, row, channel) order,
+ *   filt''[co][(j*H_f + r)*C_i + c] = w[co][c][r][j],
+ *   out[n][ho][wo][co] = sum_{k < W_f*H_f*C_i} win[n][ho][wo*s_w*H_f*C_i + k] * filt''[co][k].
+ */
+int oracle_conv_im2win_nhwc(const double *win, const double *w, double *out,
+                            int64_t N, int64_t C_i, int64_t H_i, int64_t W_i, int64_t C_o,
+                            int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w)
+{
+    shape_t s;
+    if (make_shape(&s, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w)) return -1;
+    int64_t KK = s.W_f * s.H_f * s.C_i, L = s.W_i * s.H_f * s.C_i, step = s.s_w * s.H_f * s.C_i;
+    double *fp = (double *)malloc(sizeof(double) * (size_t)(s.C_o * KK));
+    if (!fp) return -1;
+    for (int64_t co = 0; co < s.C_o; ++co)
+        for (int64_t c = 0; c < s.C_i; ++c)
+            for (int64_t r = 0; r < s.H_f; ++r)
+                for (int64_t j = 0; j < s.W_f; ++j)
+                    fp[co * KK + (j * s.H_f + r) * s.C_i + c] = w[((co * s.C_i + c) * s.H_f + r) * s.W_f + j];
+    int64_t n, ho;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (n = 0; n < s.N; ++n)
+        for (ho = 0; ho < s.H_o; ++ho)
+            for (int64_t wo = 0; wo < s.W_o; ++wo)
+                for (int64_t co = 0; co < s.C_o; ++co) {
+                    const double *seg = win + (n * s.H_o + ho) * L + wo * step;
+                    const double *f = fp + co * KK;
+                    double acc = 0.0;
+                    for (int64_t k = 0; k < KK; ++k) acc += seg[k] * f[k];
+                    out[((n * s.H_o + ho) * s.W_o + wo) * s.C_o + co] = acc;
+                }
+    free(fp);
+    return 0;
+}

@@ -194,3 +194,74 @@ def test_bad_shapes_are_rejected():
         oracle.conv_direct(x, np.zeros((1, 2, 5, 1)))
     with pytest.raises(ValueError):
         oracle.conv_points(x, np.zeros((1, 2, 2, 2)), [[0, 1, 0, 0]])
+
+
+# ---- channels-last (NHWC) layouts: the same worked example and identities,
+# with channels innermost
+
+@pytest.mark.parametrize("rule", ["ones", "ramp"])
+def test_fig1_worked_example_nhwc(rule):
+    gold = json.load(open(GOLD))
+    x = np.transpose(_fig1_x(), (0, 2, 3, 1))           # x[0][h][w][c] = 9c + 3h + w
+    w = _fig1_filter(rule)
+    want = np.transpose(np.array(gold["filters"][rule]["out"], dtype=np.float64)[None], (0, 2, 3, 1))
+    out, scale = oracle.conv_direct_nhwc(x, w)
+    assert out.shape == (1, 2, 2, 2)
+    np.testing.assert_array_equal(out, want)
+    np.testing.assert_array_equal(oracle.conv_im2win_nhwc(x, w), want)
+    assert np.all(scale >= np.abs(out))
+    win = oracle.im2win_nhwc(x, 2, 1)
+    assert win.shape == (1, 2, 6, 3)
+    for c in range(3):
+        np.testing.assert_array_equal(win[0, 0, :, c], np.array(gold["window_rows_channel0"]["ho0"]) + 9 * c)
+        np.testing.assert_array_equal(win[0, 1, :, c], np.array(gold["window_rows_channel0"]["ho1"]) + 9 * c)
+
+
+def test_im2win_nhwc_is_a_byte_copy_for_every_element_size():
+    rng = np.random.default_rng(24)
+    for dt in (np.uint8, np.uint16, np.float32, np.float64):
+        x = rng.integers(0, 250, size=(2, 10, 11, 5)).astype(dt)
+        win = oracle.im2win_nhwc(x, 4, 3)
+        ho = (10 - 4) // 3 + 1
+        assert win.shape == (2, ho, 11 * 4, 5)
+        for h in range(ho):
+            for r in range(4):
+                np.testing.assert_array_equal(win[:, h, r::4, :], x[:, 3 * h + r, :, :])
+
+
+def test_nhwc_window_is_the_nchw_window_with_channels_innermost():
+    rng = np.random.default_rng(25)
+    x = rng.integers(-100, 100, size=(2, 6, 13, 9)).astype(np.int16)
+    for hf, sh in [(1, 1), (3, 1), (4, 3), (13, 2)]:
+        win_nchw = oracle.im2win(x, hf, sh)
+        win_nhwc = oracle.im2win_nhwc(np.transpose(x, (0, 2, 3, 1)), hf, sh)
+        np.testing.assert_array_equal(win_nhwc, np.transpose(win_nchw, (0, 2, 3, 1)))
+
+
+def test_nhwc_formulations_agree_exactly_on_integers():
+    """direct (NHWC) == im2win over the channels-last window, bit for bit."""
+    rng = np.random.default_rng(26)
+    for _ in range(200):
+        n, ci, hi, wi, co, hf, wf, sh, sw = _random_case(rng)
+        x = rng.integers(-3, 4, size=(n, hi, wi, ci)).astype(np.float64)
+        w = rng.integers(-3, 4, size=(co, ci, hf, wf)).astype(np.float64)
+        d, _ = oracle.conv_direct_nhwc(x, w, (sh, sw))
+        np.testing.assert_array_equal(oracle.conv_im2win_nhwc(x, w, (sh, sw)), d)
+        ref, _ = oracle.conv_direct(np.transpose(x, (0, 3, 1, 2)), w, (sh, sw))
+        np.testing.assert_array_equal(d, np.transpose(ref, (0, 2, 3, 1)))
+        idx = np.stack([rng.integers(0, s, 8) for s in d.shape], axis=1)
+        v, _ = oracle.conv_points_nhwc(x, w, idx, (sh, sw))
+        np.testing.assert_array_equal(v, d[tuple(idx.T)])
+
+
+def test_nhwc_one_hot_filter_is_strided_crop():
+    rng = np.random.default_rng(27)
+    x = rng.standard_normal((2, 23, 21, 6))
+    w = np.zeros((5, 6, 5, 4))
+    w[3, 4, 2, 3] = 1.0
+    sh, sw = 3, 2
+    out = oracle.conv_im2win_nhwc(x, w, (sh, sw))
+    ho, wo = out.shape[1:3]
+    crop = x[:, 2:2 + (ho - 1) * sh + 1:sh, 3:3 + (wo - 1) * sw + 1:sw, 4]
+    np.testing.assert_array_equal(out[..., 3], crop)
+    assert not out[..., [0, 1, 2, 4]].any()
