@@ -61,9 +61,12 @@ typedef enum {
 
 /* Which call a workspace size is asked for. */
 typedef enum {
-    IM2WIN_OP_TRANSFORM = 0,  /* bytes of the window tensor `win` that im2win_transform writes */
-    IM2WIN_OP_CONV = 1,       /* workspace of im2win_conv (status block + re-laid filter) */
-    IM2WIN_OP_CONV_FUSED = 2  /* workspace of im2win_conv_fused (status block + re-laid filter) */
+    IM2WIN_OP_TRANSFORM = 0,       /* bytes of the window tensor `win` that im2win_transform or
+                                      im2win_transform_nhwc writes (the same count) */
+    IM2WIN_OP_CONV = 1,            /* workspace of im2win_conv (status block + re-laid filter) */
+    IM2WIN_OP_CONV_FUSED = 2,      /* workspace of im2win_conv_fused (status block + re-laid filter) */
+    IM2WIN_OP_CONV_NHWC = 3,       /* workspace of im2win_conv_nhwc */
+    IM2WIN_OP_CONV_FUSED_NHWC = 4  /* workspace of im2win_conv_fused_nhwc */
 } im2win_op;
 
 /*
@@ -121,6 +124,55 @@ im2win_status im2win_conv_fused(const void *x, const void *filt, void *out, void
                                 size_t ws_bytes, int64_t N, int64_t C_i, int64_t H_i,
                                 int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f,
                                 int64_t s_h, int64_t s_w, int dtype, void *stream);
+
+/*
+ * Channels-last (NHWC) layouts
+ * ----------------------------
+ * [SIMD] names, as a title only, a successor work that carries im2win to three
+ * tensor layouts; these calls take its plainest reading: the NCHW window row
+ * keeps its order and each of its elements becomes the C_i channels of that
+ * position, innermost. Layouts:
+ *   x[N][H_i][W_i][C_i], win[N][H_o][W_i*H_f][C_i], out[N][H_o][W_o][C_o];
+ *   the filter keeps filt[C_o][C_i][H_f][W_f].
+ * Arguments, dtypes, alignment, streams, workspaces and errors are as for the
+ * NCHW calls above; each convolution's workspace is sized by its own op
+ * (IM2WIN_OP_CONV_NHWC, IM2WIN_OP_CONV_FUSED_NHWC). F16/BF16 convolutions need
+ * one of: C_i a multiple of 8 (16-byte channel groups), or a window step
+ * s_w*H_f*C_i (window tensor) / s_w*C_i (fused) that the tensor-core tiling
+ * accepts; otherwise they return IM2WIN_ERR_UNSUPPORTED.
+ */
+
+/*
+ * Channels-last im2win transformation:
+ *   win[n][ho][w*H_f + r][c] = x[n][ho*s_h + r][w][c]   for w < W_i, r < H_f, c < C_i.
+ * A bit-exact copy; writes exactly N*H_o*W_i*H_f*C_i elements at win.
+ */
+im2win_status im2win_transform_nhwc(const void *x, void *win, int64_t N, int64_t C_i, int64_t H_i,
+                                    int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f,
+                                    int64_t s_h, int64_t s_w, int dtype, void *stream);
+
+/*
+ * Convolution over the channels-last window tensor: the window row of (n, ho)
+ * is one run of W_i*H_f*C_i elements and
+ *   out[n][ho][wo][co] = sum_{k < W_f*H_f*C_i} win[n][ho][wo*s_w*H_f*C_i + k] * filt''[co][k],
+ *   filt''[co][(j*H_f + r)*C_i + c] = filt[co][c][r][j],
+ * which equals the direct valid cross-correlation of the NHWC input with filt.
+ * ws_bytes >= im2win_workspace_size(IM2WIN_OP_CONV_NHWC, ...).
+ */
+im2win_status im2win_conv_nhwc(const void *win, const void *filt, void *out, void *ws,
+                               size_t ws_bytes, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i,
+                               int64_t C_o, int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w,
+                               int dtype, void *stream);
+
+/*
+ * Fused channels-last convolution: the result of im2win_transform_nhwc followed
+ * by im2win_conv_nhwc, computed straight from the NHWC input without writing the
+ * window tensor. ws_bytes >= im2win_workspace_size(IM2WIN_OP_CONV_FUSED_NHWC, ...).
+ */
+im2win_status im2win_conv_fused_nhwc(const void *x, const void *filt, void *out, void *ws,
+                                     size_t ws_bytes, int64_t N, int64_t C_i, int64_t H_i,
+                                     int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f,
+                                     int64_t s_h, int64_t s_w, int dtype, void *stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *im2win_status_string(int status);

@@ -17,12 +17,13 @@ import torch
 from . import build as _build
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
-OP_TRANSFORM, OP_CONV, OP_CONV_FUSED = 0, 1, 2
+OP_TRANSFORM, OP_CONV, OP_CONV_FUSED, OP_CONV_NHWC, OP_CONV_FUSED_NHWC = 0, 1, 2, 3, 4
 F32, F16, BF16 = 0, 1, 2
 _DTYPE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 
 EXPORTS = ("im2win_workspace_size", "im2win_transform", "im2win_conv", "im2win_conv_fused",
-           "im2win_status_string", "im2win_device_status", "im2win_conv_fused_noalloc")
+           "im2win_status_string", "im2win_device_status", "im2win_conv_fused_noalloc",
+           "im2win_transform_nhwc", "im2win_conv_nhwc", "im2win_conv_fused_nhwc")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
@@ -60,8 +61,12 @@ def lib() -> ctypes.CDLL:
             L.im2win_status_string.restype = ctypes.c_char_p
             L.im2win_device_status.argtypes = [vp, sz, vp]
             L.im2win_conv_fused_noalloc.argtypes = [vp, vp, vp] + shp + [ctypes.c_int, vp]
+            L.im2win_transform_nhwc.argtypes = [vp, vp] + shp + [ctypes.c_int, vp]
+            L.im2win_conv_nhwc.argtypes = [vp, vp, vp, vp, sz] + shp + [ctypes.c_int, vp]
+            L.im2win_conv_fused_nhwc.argtypes = [vp, vp, vp, vp, sz] + shp + [ctypes.c_int, vp]
             for f in ("im2win_workspace_size", "im2win_transform", "im2win_conv",
-                      "im2win_conv_fused", "im2win_device_status", "im2win_conv_fused_noalloc"):
+                      "im2win_conv_fused", "im2win_device_status", "im2win_conv_fused_noalloc",
+                      "im2win_transform_nhwc", "im2win_conv_nhwc", "im2win_conv_fused_nhwc"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -163,6 +168,47 @@ def im2win_conv_fused_noalloc(x: torch.Tensor, filt: torch.Tensor, out: torch.Te
                                            _stream(x)))
 
 
+def im2win_transform_nhwc(x: torch.Tensor, win: torch.Tensor, C_o, H_f, W_f, s_h, s_w) -> None:
+    """Channels-last window transform: x[N][H_i][W_i][C_i] -> win[N][H_o][W_i*H_f][C_i]."""
+    _cuda(x, win)
+    N, H_i, W_i, C_i = x.shape
+    if win.dtype != x.dtype:
+        raise TypeError("win must have the dtype of x")
+    need = im2win_workspace_size(OP_TRANSFORM, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
+                                 _dtype_code(x))
+    if win.numel() * win.element_size() < need:
+        raise ValueError("win is smaller than the window tensor")
+    _check("im2win_transform_nhwc",
+           lib().im2win_transform_nhwc(x.data_ptr(), win.data_ptr(), N, C_i, H_i, W_i, C_o, H_f,
+                                       W_f, s_h, s_w, _dtype_code(x), _stream(x)))
+
+
+def im2win_conv_nhwc(win: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                     N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w) -> None:
+    """Convolution from the channels-last window tensor into out[N][H_o][W_o][C_o]."""
+    _cuda(win, filt, out, ws)
+    if not (win.dtype == filt.dtype == out.dtype):
+        raise TypeError("win, filt and out must share a dtype")
+    _check("im2win_conv_nhwc",
+           lib().im2win_conv_nhwc(win.data_ptr(), filt.data_ptr(), out.data_ptr(), ws.data_ptr(),
+                                  ws.numel() * ws.element_size(), N, C_i, H_i, W_i, C_o, H_f, W_f,
+                                  s_h, s_w, _dtype_code(win), _stream(win)))
+
+
+def im2win_conv_fused_nhwc(x: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                           s_h, s_w) -> None:
+    """Fused convolution of x[N][H_i][W_i][C_i] into out[N][H_o][W_o][C_o]."""
+    _cuda(x, filt, out, ws)
+    if not (x.dtype == filt.dtype == out.dtype):
+        raise TypeError("x, filt and out must share a dtype")
+    N, H_i, W_i, C_i = x.shape
+    C_o, _, H_f, W_f = filt.shape
+    _check("im2win_conv_fused_nhwc",
+           lib().im2win_conv_fused_nhwc(x.data_ptr(), filt.data_ptr(), out.data_ptr(), ws.data_ptr(),
+                                        ws.numel() * ws.element_size(), N, C_i, H_i, W_i, C_o, H_f,
+                                        W_f, s_h, s_w, _dtype_code(x), _stream(x)))
+
+
 def im2win_device_status(ws: torch.Tensor) -> int:
     """Synchronise the current stream and return the status word of `ws`."""
     _cuda(ws)
@@ -171,7 +217,8 @@ def im2win_device_status(ws: torch.Tensor) -> int:
 
 # ---------------------------------------------------------------- conveniences
 def workspace(op: int, x_shape, w_shape, stride, dtype: torch.dtype, device) -> torch.Tensor:
-    """Allocate (through torch) the workspace `op` needs."""
+    """Allocate (through torch) the workspace `op` needs; x_shape is given as
+    (N, C_i, H_i, W_i) in either layout."""
     N, C_i, H_i, W_i = x_shape
     C_o, _, H_f, W_f = w_shape
     b = im2win_workspace_size(op, N, C_i, H_i, W_i, C_o, H_f, W_f, stride[0], stride[1],
@@ -215,4 +262,43 @@ def conv_fused(x: torch.Tensor, filt: torch.Tensor, stride=(1, 1), ws: torch.Ten
     if out is None:
         out = torch.empty((N, C_o, H_o, W_o), dtype=x.dtype, device=x.device)
     im2win_conv_fused(x, filt, out, ws, stride[0], stride[1])
+    return out
+
+
+def transform_nhwc(x: torch.Tensor, H_f: int, s_h: int = 1) -> torch.Tensor:
+    """Channels-last window tensor win[N][H_o][W_i*H_f][C_i] of x[N][H_i][W_i][C_i]."""
+    N, H_i, W_i, C_i = x.shape
+    H_o = (H_i - H_f) // s_h + 1
+    win = torch.empty((N, H_o, W_i * H_f, C_i), dtype=x.dtype, device=x.device)
+    im2win_transform_nhwc(x, win, 1, H_f, 1, s_h, 1)
+    return win
+
+
+def conv_nhwc(win: torch.Tensor, filt: torch.Tensor, stride=(1, 1), ws: torch.Tensor | None = None,
+              out: torch.Tensor | None = None) -> torch.Tensor:
+    """Convolution from a channels-last window tensor produced by transform_nhwc()."""
+    N, H_o, L, C_i = win.shape
+    C_o, _, H_f, W_f = filt.shape
+    W_i = L // H_f
+    H_i = (H_o - 1) * stride[0] + H_f
+    _, W_o = out_hw(H_i, W_i, H_f, W_f, *stride)
+    if ws is None:
+        ws = workspace(OP_CONV_NHWC, (N, C_i, H_i, W_i), filt.shape, stride, win.dtype, win.device)
+    if out is None:
+        out = torch.empty((N, H_o, W_o, C_o), dtype=win.dtype, device=win.device)
+    im2win_conv_nhwc(win, filt, out, ws, N, C_i, H_i, W_i, C_o, H_f, W_f, stride[0], stride[1])
+    return out
+
+
+def conv_fused_nhwc(x: torch.Tensor, filt: torch.Tensor, stride=(1, 1), ws: torch.Tensor | None = None,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+    """Fused im2win convolution straight from the NHWC input; out[N][H_o][W_o][C_o]."""
+    N, H_i, W_i, C_i = x.shape
+    C_o, _, H_f, W_f = filt.shape
+    H_o, W_o = out_hw(H_i, W_i, H_f, W_f, *stride)
+    if ws is None:
+        ws = workspace(OP_CONV_FUSED_NHWC, (N, C_i, H_i, W_i), filt.shape, stride, x.dtype, x.device)
+    if out is None:
+        out = torch.empty((N, H_o, W_o, C_o), dtype=x.dtype, device=x.device)
+    im2win_conv_fused_nhwc(x, filt, out, ws, stride[0], stride[1])
     return out

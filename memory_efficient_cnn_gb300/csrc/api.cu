@@ -33,15 +33,16 @@ size_t window_bytes(const Shape &s, int esz) {
     return (size_t)(s.N * s.C_i * s.H_o * s.W_i * s.H_f) * (size_t)esz;
 }
 
-size_t conv_ws_bytes(const Shape &s, int dtype, bool fused) {
-    const size_t f = dtype == IM2WIN_F32 ? conv_f32_filter_bytes(s) : conv_tc_filter_bytes(s, fused);
+size_t conv_ws_bytes(const Shape &s, int dtype, bool fused, int layout) {
+    const size_t f = dtype == IM2WIN_F32 ? conv_f32_filter_bytes(s, fused, layout)
+                                         : conv_tc_filter_bytes(s, fused, layout);
     return kStatusBytes + round_up(f, 256);
 }
 
 im2win_status conv_common(const void *src, const void *filt, void *out, void *ws, size_t ws_bytes,
                           int64_t N, int64_t C_i, int64_t H_i, int64_t W_i, int64_t C_o,
                           int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w, int dtype,
-                          void *stream, bool fused) {
+                          void *stream, bool fused, int layout) {
     Shape s;
     im2win_status st = make_shape(s, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w);
     if (st != IM2WIN_OK) return st;
@@ -49,17 +50,33 @@ im2win_status conv_common(const void *src, const void *filt, void *out, void *ws
     if (s.N == 0) return IM2WIN_OK;  // empty batch: nothing to read or write
     if (!src || !filt || !out) return IM2WIN_ERR_INVALID_ARG;
     if (!aligned16(src) || !aligned16(filt) || !aligned16(out)) return IM2WIN_ERR_MISALIGNED;
-    if (!ws || ws_bytes < conv_ws_bytes(s, dtype, fused)) return IM2WIN_ERR_WORKSPACE;
+    if (!ws || ws_bytes < conv_ws_bytes(s, dtype, fused, layout)) return IM2WIN_ERR_WORKSPACE;
     if (!aligned16(ws)) return IM2WIN_ERR_MISALIGNED;
+    const bool ok = dtype == IM2WIN_F32 ? conv_f32_supported(s, fused, layout)
+                                        : conv_tc_supported(s, fused, layout);
+    if (!ok) return IM2WIN_ERR_UNSUPPORTED;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (dtype == IM2WIN_F32) {
-        if (!conv_f32_supported(s, fused)) return IM2WIN_ERR_UNSUPPORTED;
-        e = launch_conv_f32(src, filt, out, ws, s, fused, cs);
-    } else {
-        if (!conv_tc_supported(s, fused)) return IM2WIN_ERR_UNSUPPORTED;
-        e = launch_conv_tc(src, filt, out, ws, s, fused, dtype == IM2WIN_BF16, cs);
-    }
+    const cudaError_t e = dtype == IM2WIN_F32
+                              ? launch_conv_f32(src, filt, out, ws, s, fused, layout, cs)
+                              : launch_conv_tc(src, filt, out, ws, s, fused, layout, dtype == IM2WIN_BF16, cs);
+    return e == cudaSuccess ? IM2WIN_OK : IM2WIN_ERR_CUDA;
+}
+
+im2win_status transform_common(const void *x, void *win, int64_t N, int64_t C_i, int64_t H_i,
+                               int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f, int64_t s_h,
+                               int64_t s_w, int dtype, void *stream, int layout) {
+    Shape s;
+    im2win_status st = make_shape(s, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w);
+    if (st != IM2WIN_OK) return st;
+    const int esz = elem_size(dtype);
+    if (esz == 0) return IM2WIN_ERR_INVALID_ARG;
+    if (s.N == 0) return IM2WIN_OK;  // empty batch: nothing to read or write
+    if (!x || !win) return IM2WIN_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(win)) return IM2WIN_ERR_MISALIGNED;
+    const bool cl = layout == LAYOUT_NHWC;
+    if (!(cl ? transform_nhwc_supported(s, esz) : transform_supported(s, esz))) return IM2WIN_ERR_UNSUPPORTED;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = cl ? launch_transform_nhwc(x, win, s, esz, cs) : launch_transform(x, win, s, esz, cs);
     return e == cudaSuccess ? IM2WIN_OK : IM2WIN_ERR_CUDA;
 }
 
@@ -78,8 +95,10 @@ im2win_status im2win_workspace_size(int op, int64_t N, int64_t C_i, int64_t H_i,
     if (esz == 0) return IM2WIN_ERR_INVALID_ARG;
     switch (op) {
         case IM2WIN_OP_TRANSFORM: *bytes = window_bytes(s, esz); return IM2WIN_OK;
-        case IM2WIN_OP_CONV: *bytes = conv_ws_bytes(s, dtype, false); return IM2WIN_OK;
-        case IM2WIN_OP_CONV_FUSED: *bytes = conv_ws_bytes(s, dtype, true); return IM2WIN_OK;
+        case IM2WIN_OP_CONV: *bytes = conv_ws_bytes(s, dtype, false, LAYOUT_NCHW); return IM2WIN_OK;
+        case IM2WIN_OP_CONV_FUSED: *bytes = conv_ws_bytes(s, dtype, true, LAYOUT_NCHW); return IM2WIN_OK;
+        case IM2WIN_OP_CONV_NHWC: *bytes = conv_ws_bytes(s, dtype, false, LAYOUT_NHWC); return IM2WIN_OK;
+        case IM2WIN_OP_CONV_FUSED_NHWC: *bytes = conv_ws_bytes(s, dtype, true, LAYOUT_NHWC); return IM2WIN_OK;
         default: return IM2WIN_ERR_INVALID_ARG;
     }
 }
@@ -87,17 +106,13 @@ im2win_status im2win_workspace_size(int op, int64_t N, int64_t C_i, int64_t H_i,
 im2win_status im2win_transform(const void *x, void *win, int64_t N, int64_t C_i, int64_t H_i,
                                int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f,
                                int64_t s_h, int64_t s_w, int dtype, void *stream) {
-    Shape s;
-    im2win_status st = make_shape(s, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w);
-    if (st != IM2WIN_OK) return st;
-    const int esz = elem_size(dtype);
-    if (esz == 0) return IM2WIN_ERR_INVALID_ARG;
-    if (s.N == 0) return IM2WIN_OK;  // empty batch: nothing to read or write
-    if (!x || !win) return IM2WIN_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(win)) return IM2WIN_ERR_MISALIGNED;
-    if (!transform_supported(s, esz)) return IM2WIN_ERR_UNSUPPORTED;
-    cudaError_t e = launch_transform(x, win, s, esz, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? IM2WIN_OK : IM2WIN_ERR_CUDA;
+    return transform_common(x, win, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, dtype, stream, LAYOUT_NCHW);
+}
+
+im2win_status im2win_transform_nhwc(const void *x, void *win, int64_t N, int64_t C_i, int64_t H_i,
+                                    int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f,
+                                    int64_t s_h, int64_t s_w, int dtype, void *stream) {
+    return transform_common(x, win, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, dtype, stream, LAYOUT_NHWC);
 }
 
 im2win_status im2win_conv(const void *win, const void *filt, void *out, void *ws,
@@ -105,7 +120,7 @@ im2win_status im2win_conv(const void *win, const void *filt, void *out, void *ws
                           int64_t C_o, int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w,
                           int dtype, void *stream) {
     return conv_common(win, filt, out, ws, ws_bytes, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
-                       dtype, stream, false);
+                       dtype, stream, false, LAYOUT_NCHW);
 }
 
 im2win_status im2win_conv_fused(const void *x, const void *filt, void *out, void *ws,
@@ -113,7 +128,23 @@ im2win_status im2win_conv_fused(const void *x, const void *filt, void *out, void
                                 int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f,
                                 int64_t s_h, int64_t s_w, int dtype, void *stream) {
     return conv_common(x, filt, out, ws, ws_bytes, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
-                       dtype, stream, true);
+                       dtype, stream, true, LAYOUT_NCHW);
+}
+
+im2win_status im2win_conv_nhwc(const void *win, const void *filt, void *out, void *ws,
+                               size_t ws_bytes, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i,
+                               int64_t C_o, int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w,
+                               int dtype, void *stream) {
+    return conv_common(win, filt, out, ws, ws_bytes, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
+                       dtype, stream, false, LAYOUT_NHWC);
+}
+
+im2win_status im2win_conv_fused_nhwc(const void *x, const void *filt, void *out, void *ws,
+                                     size_t ws_bytes, int64_t N, int64_t C_i, int64_t H_i,
+                                     int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f,
+                                     int64_t s_h, int64_t s_w, int dtype, void *stream) {
+    return conv_common(x, filt, out, ws, ws_bytes, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
+                       dtype, stream, true, LAYOUT_NHWC);
 }
 
 const char *im2win_status_string(int status) {

@@ -18,6 +18,16 @@
 // The fused variant (FROM_X) gathers the same matrix straight from the NCHW
 // input (x[n][ci][ho*s_h + r][wo*s_w + j] for k = j*H_f + r) and never
 // materialises the window tensor.
+//
+// Channels-last tensors (NHWC) run the window path over a virtual shape:
+//  * from the channels-last window tensor, whose window row is one run of
+//    W_i*H_f*C_i elements: one channel, K = W_f*H_f*C_i contiguous elements per
+//    pixel starting at wo*s_w*H_f*C_i;
+//  * fused from the NHWC input: the H_f filter rows play the channels, each a
+//    contiguous run of W_f*C_i elements of input row ho*s_h + r starting at
+//    column wo*s_w (channel stride W_i*C_i, pixel stride s_w*C_i).
+// In both the filter is re-laid in the matching order and the epilogue writes
+// out[n][ho][wo][co].
 #include <algorithm>
 
 #include "im2win_internal.cuh"
@@ -40,6 +50,8 @@ struct F32Params {
     int L;               // W_i * H_f
     int S;               // s_w * H_f
     int64_t img_src;     // elements of src per image
+    int cs;              // window path: element stride between channels (H_o*L for the NCHW window)
+    int nhwc;            // output out[n][ho][wo][co] instead of out[n][co][ho][wo]
     int C_o_pad;         // row length of the transposed filter (a multiple of the channel tile)
     FastDiv div_KK, div_Wo, div_Hf;
 };
@@ -152,7 +164,7 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
                     const int r = kk - jj * p.H_f;
                     coff = (ci * p.H_i + r) * p.W_i + jj;
                 } else {
-                    coff = ci * p.H_o * p.L + kk;
+                    coff = ci * p.cs + kk;
                 }
                 ok = pos_ok;
             }
@@ -209,7 +221,26 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
     }
     cp_async_wait<0>();
 
-    // ---- epilogue: out[n][co][p]
+    // ---- epilogue: out[n][co][p], or out[n][p][co] (8 consecutive channels per pixel)
+    if (p.nhwc) {
+        const int cb = co0 + ty * 8;
+        const bool vec = (p.C_o & 3) == 0 && cb + 8 <= p.C_o;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int pg = p0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
+            if (pg >= p.P) continue;
+            float *d = p.out + ((int64_t)n * p.P + pg) * p.C_o + cb;
+            if (vec) {
+                reinterpret_cast<float4 *>(d)[0] = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
+                reinterpret_cast<float4 *>(d)[1] = make_float4(acc[4][j], acc[5][j], acc[6][j], acc[7][j]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (cb + i < p.C_o) d[i] = acc[i][j];
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int co = co0 + ty * 8 + i;
@@ -228,22 +259,21 @@ constexpr size_t f32_smem_bytes() {
     return (size_t)STAGES * KC * ((TP + 4) + (TM + 4)) * sizeof(float);
 }
 
-// filt'[co][ci*KK + j*H_f + r] = filt[co][ci][r][j]; block 0 also clears the
-// workspace status word for this call.
-// fT[k][co] = filt'[co][k] with filt'[co][ci*KK + j*H_f + r] = filt[co][ci][r][j],
-// zero for k >= K or co >= C_o; block 0 also clears the workspace status word
-// for this call.
+// fT[k][co] = filt'[co][k] with filt'[co][ci*KK + j*H_f + r] = filt[co][ci][r][j]
+// for the kernel's (virtual) shape, C_v x H_fv x W_fv; `view` maps that element
+// to the caller's filter, C x H_f x W_f (filter_src_offset). Zero for k >= K or
+// co >= C_o; block 0 also clears the workspace status word for this call.
 __global__ void relayout_filter_f32(const float *__restrict__ filt, float *__restrict__ fT,
-                                    uint32_t *status, int K, int K_pad, int C_o, int C_o_pad, int H_f,
-                                    int W_f) {
+                                    uint32_t *status, int K, int K_pad, int C_o, int C_o_pad, int H_fv,
+                                    int W_fv, int view, int C, int H_f, int W_f) {
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) status[0] = 0;
-    const int KK = H_f * W_f;
+    const int KK = H_fv * W_fv;
     for (int k = blockIdx.y; k < K_pad; k += gridDim.y) {
         int src_k = -1;
         if (k < K) {
             const int ci = k / KK, kk = k - ci * KK;
-            const int j = kk / H_f, r = kk - j * H_f;
-            src_k = ci * KK + r * W_f + j;  // index of filt[co][ci][r][j] within filt[co]
+            const int j = kk / H_fv, r = kk - j * H_fv;
+            src_k = (int)filter_src_offset(view, ci, r, j, C, H_f, W_f);  // within filt[co]
         }
         for (int co = blockIdx.x * blockDim.x + threadIdx.x; co < C_o_pad; co += gridDim.x * blockDim.x)
             fT[(int64_t)k * C_o_pad + co] = (src_k >= 0 && co < C_o) ? filt[(int64_t)co * K + src_k] : 0.f;
@@ -284,11 +314,13 @@ static int64_t c_o_pad(const Shape &s) {
     return (s.C_o + tm - 1) / tm * tm;
 }
 
-size_t conv_f32_filter_bytes(const Shape &s) {
+// The filter's K (C_i*H_f*W_f) and channel padding do not depend on the layout.
+size_t conv_f32_filter_bytes(const Shape &s, bool, int) {
     return round_up((size_t)(k_pad(s) * c_o_pad(s)) * 4, 256);
 }
 
-bool conv_f32_supported(const Shape &s, bool from_x) {
+bool conv_f32_supported(const Shape &s, bool from_x, int) {
+    // elements of one image of the source (the same count in either layout)
     const int64_t img = from_x ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * s.W_i * s.H_f;
     const int64_t P = s.H_o * s.W_o;
     const int64_t tiles = (P + TP - 1) / TP;
@@ -297,14 +329,20 @@ bool conv_f32_supported(const Shape &s, bool from_x) {
 }
 
 cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *ws,
-                            const Shape &s, bool from_x, cudaStream_t st) {
+                            const Shape &s, bool from_x, int layout, cudaStream_t st) {
     uint32_t *status = static_cast<uint32_t *>(ws);
     float *fp = reinterpret_cast<float *>(static_cast<unsigned char *>(ws) + kStatusBytes);
     const int64_t Kp = k_pad(s), Cp = c_o_pad(s);
+    const bool cl = layout == LAYOUT_NHWC;
+    // virtual filter extents and view (see the head of this file)
+    const int64_t H_fv = cl ? 1 : s.H_f;
+    const int64_t W_fv = !cl ? s.W_f : from_x ? s.W_f * s.C_i : s.W_f * s.H_f * s.C_i;
+    const int view = !cl ? VIEW_IDENT : from_x ? VIEW_CL_ROWS : VIEW_CL_WIN;
     const dim3 rgrid((unsigned)std::min<int64_t>((Cp + 127) / 128, 8), (unsigned)std::min<int64_t>(Kp, 65535));
     relayout_filter_f32<<<rgrid, 128, 0, st>>>(static_cast<const float *>(filt), fp, status,
                                                (int)(s.C_i * s.H_f * s.W_f), (int)Kp, (int)s.C_o, (int)Cp,
-                                               (int)s.H_f, (int)s.W_f);
+                                               (int)H_fv, (int)W_fv, view, (int)s.C_i, (int)s.H_f,
+                                               (int)s.W_f);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || s.N == 0) return e;
 
@@ -329,10 +367,27 @@ cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *
     p.L = (int)(s.W_i * s.H_f);
     p.S = (int)(s.s_w * s.H_f);
     p.img_src = from_x ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * s.W_i * s.H_f;
+    p.cs = (int)(s.H_o * s.W_i * s.H_f);
+    p.nhwc = cl ? 1 : 0;
     p.C_o_pad = (int)Cp;
     p.div_KK = make_fastdiv((uint32_t)(s.H_f * s.W_f));
     p.div_Wo = make_fastdiv((uint32_t)s.W_o);
     p.div_Hf = make_fastdiv((uint32_t)s.H_f);
+    if (cl) {
+        // the window path over the virtual shape: KK = H_fv*W_fv taps per channel
+        p.KK = (int)(H_fv * W_fv);
+        p.div_KK = make_fastdiv((uint32_t)p.KK);
+        if (from_x) {
+            p.L = (int)(s.s_h * s.W_i * s.C_i);  // output row step
+            p.S = (int)(s.s_w * s.C_i);          // pixel step
+            p.cs = (int)(s.W_i * s.C_i);         // filter row r = channel r
+        } else {
+            p.L = (int)(s.W_i * s.H_f * s.C_i);
+            p.S = (int)(s.s_w * s.H_f * s.C_i);
+            p.cs = (int)(s.H_o * p.L);           // one channel
+        }
+        from_x = false;
+    }
 
     const int best = choose_tm(s);
     const int N = (int)s.N;

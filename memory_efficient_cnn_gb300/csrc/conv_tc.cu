@@ -301,7 +301,13 @@ __global__ void relayout_filter_expand(const uint16_t *__restrict__ filt, uint16
 // computed and discarded. Filter tiles arrive per (chunk, group of taps) by
 // bulk copy, pre-laid by a re-layout kernel as [tap][co group][K half][8 co][8 K].
 // =========================================================================
-enum TapMode { TAP_CH = 0, TAP_WX = 1, TAP_WW = 2 };
+// TAP_CL (channels-last input, C_i a multiple of 8): the slab of TAP_CH, whose
+// 16-byte entries (8 channels of one input position) are 16 contiguous bytes of
+// an NHWC input. Producers copy each entry straight from global memory with
+// cp.async and never touch it; the copies' completion is tracked by the slab
+// barrier (cp.async.mbarrier.arrive.noinc), and the MMA issuers order the
+// copies before their reads with a proxy fence after the barrier wait.
+enum TapMode { TAP_CH = 0, TAP_WX = 1, TAP_WW = 2, TAP_CL = 3 };
 
 // Tap stacking (TAP_CH with C_o <= 64, so half of M = 128 would be idle).
 // Taps (r, j) and (r, j + s_w) lie in the same polyphase block, one slab entry
@@ -325,7 +331,7 @@ constexpr int TAP_MAX_NT = 512;
 constexpr uint32_t TAP_EPI_BYTES = TAP_EPI_WARPS * 32 * 33 * 4;
 
 struct TapParams {
-    const uint16_t *src;   // NCHW input (CH, WX) or window tensor (WW)
+    const uint16_t *src;   // NCHW input (CH, WX), window tensor (WW), NHWC input (CL)
     const uint16_t *fa;
     uint16_t *out;
     uint32_t *status;
@@ -357,6 +363,8 @@ struct TapParams {
     FastDiv div_vpc;       // CH with ring: 16-byte vectors per channel of a full tile's rows
     int stack;             // CH, C_o <= 64: two taps per MMA, stacked along M (see below)
     int Gr;                // stacked: tap groups per filter row
+    int nhwc;              // output out[n][ho][wo][co] (else out[n][co][ho][wo])
+    FastDiv div_wi;        // CL: positions of an input row
 };
 
 // A tile: output rows [ho0, ho0 + Q) of image n, output channels [mt*128, mt*128 + 128).
@@ -392,7 +400,7 @@ __device__ __forceinline__ int tile_n0(const TapParams &p, int NTp) {
 
 template <int MODE>
 __device__ __forceinline__ uint32_t tap_offset(const TapParams &p, int t) {
-    if (MODE == TAP_CH) {
+    if (MODE == TAP_CH || MODE == TAP_CL) {
         const int r = t / p.W_f, j = t - r * p.W_f;
         return (uint32_t)((((r % p.s_h) * p.s_w + (j % p.s_w)) * p.PB) +
                           (((r / p.s_h) * p.pitch + (j / p.s_w)) * 16));
@@ -421,6 +429,7 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
 // and the slab fill of the next overlap the MMAs.
 template <int MODE>
 __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __grid_constant__ TapParams p) {
+    constexpr bool CHAN = MODE == TAP_CH || MODE == TAP_CL;  // slab over channels
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t a_stage = (uint32_t)p.TG * TAP_A_BYTES;
     uint8_t *sA = smem;
@@ -441,7 +450,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     // W modes: per K chunk row c and element e of a slab entry, the raw offset
     // from the entry's base and the limit on m*mstride below which it exists
     int *wtab = reinterpret_cast<int *>((reinterpret_cast<uintptr_t>(toff + p.T) + 15) & ~(uintptr_t)15);
-    if (MODE != TAP_CH) {
+    if (!CHAN) {
         for (int b = threadIdx.x; b < 16 * p.U; b += blockDim.x) {
             if (MODE == TAP_WX) {
                 const int jl = b / p.H_f, r = b - jl * p.H_f;
@@ -545,6 +554,9 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 const uint32_t d_tmem = tmem + col0;
                 for (int cc = 0; cc < p.NCH && ok; ++cc) {
                     if (!(ok = bar_wait(full_b(sb), phb, ctl, SITE_FULL_B))) break;
+                    // CL: the slab was written by cp.async (generic proxy), the MMAs read
+                    // it through the async proxy
+                    if (MODE == TAP_CL) fence_async_smem();
                     const uint32_t b_lo_slab = b_lo_base + (uint32_t)sb * b_stage16 + col0;
                     for (int t0 = 0; t0 < p.T && ok; t0 += p.TG) {
                         if (!(ok = bar_wait(full_a(sa), pha, ctl, SITE_FULL_A))) break;
@@ -616,7 +628,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         // that fill alternate chunks at the same time, each with its own raw slot and
         // named barrier. Otherwise all eight warps fill every chunk, and with two raw
         // slots the next chunk's copy is in flight while this one is re-laid.
-        const bool staged = MODE != TAP_CH || p.ring;
+        const bool staged = !CHAN || (MODE == TAP_CH && p.ring);
         const int ngroups = (MODE == TAP_CH && (p.ring || p.stack)) ? 2 : 1;
         const bool prefetch = ngroups == 1 && staged && p.ring;
         const int grp = ngroups == 2 ? (warp - 2) / (TAP_PROD_WARPS / 2) : 0;
@@ -629,7 +641,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         uint32_t phb = 0;
         // source range of chunk (tile, cc) and its 16-byte aligned copy into raw slot `slot`
         auto raw_lead_of = [&](const TapTile &t, int cc) -> int {
-            if (MODE == TAP_CH) return 0;
+            if (CHAN) return 0;
             const int64_t g0 = MODE == TAP_WX ? (((int64_t)t.n * p.C_i + cc) * p.H_i + t.ho0 * p.s_h) * p.W_i
                                               : (((int64_t)t.n * p.C_i + cc) * p.H_o + t.ho0) * p.L;
             return (int)(g0 & 7);
@@ -715,6 +727,27 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             const E16 *raw_slot = sRaw + (size_t)slot * p.raw_slot;
             if (!pok) {
                 // aborted: keep meeting the producers' barrier, do no work
+            } else if (MODE == TAP_CL) {
+                // entry (8-channel half c8, tile row lr, column col) is x[n][R0 + lr][col][cc*16 + c8*8 ..
+                // + 8]: one 16-byte copy. Lane pairs take the two halves of a position (32
+                // contiguous bytes); halves past C_i (a multiple of 8) are zero-filled.
+                const int rows = (Q - 1) * p.s_h + p.H_f;
+                const int items = 2 * rows * p.W_i;
+                const uint16_t *xr = p.src + (((int64_t)n * p.H_i + (int64_t)ho0 * p.s_h) * p.W_i) * p.C_i + cc * 16;
+                for (int it = pt; it < items; it += NPT) {
+                    const int c8 = it & 1;
+                    const int pos = it >> 1;
+                    const int lr = (int)fdiv((uint32_t)pos, p.div_wi);
+                    const int col = pos - lr * p.W_i;
+                    const int lq = (int)fdiv((uint32_t)lr, p.div_sh);
+                    const int cq = (int)fdiv((uint32_t)col, p.div_sw);
+                    const uint32_t dst = smem_u32(slab + (size_t)c8 * p.lbo +
+                                                  (size_t)((lr - lq * p.s_h) * p.s_w + (col - cq * p.s_w)) * p.PB +
+                                                  (size_t)(lq * p.pitch + cq) * 16);
+                    const bool ok = cc * 16 + c8 * 8 < p.C_i;
+                    cp_async16z(dst, ok ? (const void *)(xr + (int64_t)pos * p.C_i + c8 * 8) : (const void *)p.src,
+                                ok ? 16u : 0u);
+                }
             } else if (MODE == TAP_CH) {
                 const int rows = (Q - 1) * p.s_h + p.H_f;
                 const int64_t plane = (int64_t)p.H_i * p.W_i;
@@ -825,15 +858,20 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 }
             }
             if (pok) {
-                fence_async_smem();
-                mbar_arrive(full_b(sb_g));
+                if (MODE == TAP_CL) {
+                    cp_async_mbar_arrive_noinc(full_b(sb_g));  // once this thread's copies land
+                } else {
+                    fence_async_smem();
+                    mbar_arrive(full_b(sb_g));
+                }
             }
             if (staged) {
                 // the raw slot is consumed: the group's next copy may overwrite it
                 asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(NPT) : "memory");
             }
-            if (MODE == TAP_CH && !staged && !pok) break;
+            if (CHAN && !staged && !pok) break;
         }
+        cp_async_commit_group();
         cp_async_wait_group<0>();
     } else {
         // ---------------- epilogue: TMEM -> registers -> smem transpose -> coalesced stores
@@ -865,9 +903,15 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 ce = hh == 0 ? min(a1, mid) : a1;
             };
             bool ok = true;
+            // channels-last: a position's channels are contiguous, positions C_o apart
+            auto out_at = [&](int co0) -> uint16_t * {
+                return p.nhwc ? p.out + (((int64_t)tl.n * p.H_o + tl.ho0) * p.W_o) * p.C_o + co0
+                              : p.out + ((int64_t)tl.n * p.C_o + co0) * plane + (int64_t)tl.ho0 * p.W_o;
+            };
+            const int64_t ostride = p.nhwc ? (int64_t)p.C_o : plane;
             if (!p.stack) {
                 const int co0 = tl.mt * BM + q4 * 32;
-                uint16_t *out_c = p.out + ((int64_t)tl.n * p.C_o + co0) * plane + (int64_t)tl.ho0 * p.W_o;
+                uint16_t *out_c = out_at(co0);
                 for (int a = 0; a < 2 && ok; ++a) {
                     if (!(ok = warp_bar_wait(tmem_full(a), k & 1, ctl, SITE_DONE))) break;
                     tc_fence_after();
@@ -875,8 +919,13 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     half_range(a == 0 ? 0 : N0, a == 0 ? N0 : NTp, cb, ce);
                     // a block may reach past the range (into the other accumulator, which
                     // may still be accumulating): only columns of the range are stored
-                    drain_columns(taddr, cb, ce, stage, min(32, p.C_o - co0), plane, p.bf16, out_c,
-                                  [&](int pp) -> int { return pp < ce ? off_of(pp) : -1; });
+                    auto off_in = [&](int pp) -> int { return pp < ce ? off_of(pp) : -1; };
+                    if (p.nhwc)
+                        drain_columns<true>(taddr, cb, ce, stage, min(32, p.C_o - co0), ostride, p.bf16, out_c,
+                                            off_in);
+                    else
+                        drain_columns<false>(taddr, cb, ce, stage, min(32, p.C_o - co0), ostride, p.bf16, out_c,
+                                             off_in);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(tmem_empty(a));
@@ -899,11 +948,17 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                                                  xempty(pair), &xk, ctl, SITE_STACK);
                     } else {
                         const int co0 = q4 * 32;
-                        uint16_t *out_c = p.out + ((int64_t)tl.n * p.C_o + co0) * plane + (int64_t)tl.ho0 * p.W_o;
+                        uint16_t *out_c = out_at(co0);
                         const float *xbuf = reinterpret_cast<const float *>(sE + (ew - 2) * (32 * 33));
-                        ok = drain_stacked_upper(taddr, cb, ce, stage, xbuf, xfull(pair), xempty(pair), &xk, ctl,
-                                                 SITE_STACK, max(0, min(32, p.C_o - co0)), plane, p.bf16, out_c,
-                                                 off_of);
+                        const int rows = max(0, min(32, p.C_o - co0));
+                        if (p.nhwc)
+                            ok = drain_stacked_upper<true>(taddr, cb, ce, stage, xbuf, xfull(pair), xempty(pair),
+                                                           &xk, ctl, SITE_STACK, rows, ostride, p.bf16, out_c,
+                                                           off_of);
+                        else
+                            ok = drain_stacked_upper<false>(taddr, cb, ce, stage, xbuf, xfull(pair), xempty(pair),
+                                                            &xk, ctl, SITE_STACK, rows, ostride, p.bf16, out_c,
+                                                            off_of);
                     }
                 }
                 if (ok) {
@@ -929,57 +984,64 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
 }
 
 // Filter tiles of the tap kernels: fa[mt][cc][t][g][h][row][e] (h = K half)
-// holds, for output channel mt*128 + g*8 + row and K index k = h*8 + e of tap t:
-//   TAP_CH: filt[co][cc*16 + k][r][j] with t = r*W_f + j;
-//   TAP_W*: filt[co][cc][r][a*s_w + jl] with t = a*U + u, b = 16u + k = jl*H_f + r (b < S);
-// zero outside the filter. With win_hf > 0 (TAP_CH over the window tensor, see
-// window_as_input) tap t is window offset k = t of the re-laid filter
-// filt'[co][ci][k] = filt[co][ci][k % H_f][k / H_f], H_f = win_hf.
-// Block 0 also clears the status word.
+// holds, for output channel mt*128 + g*8 + row and K index k = h*8 + e of tap t,
+// the element (ci, r, j) of the kernel's (virtual) filter C_v x H_fv x W_fv:
+//   TAP_CH, TAP_CL: ci = cc*16 + k, (r, j) = (t / W_fv, t % W_fv);
+//   TAP_W*: ci = cc, r = b % H_fv, j = a*s_wv + b / H_fv with t = a*U + u, b = 16u + k (b < S);
+// zero outside the filter. `view` maps that element to the caller's filter
+// C x H_f x W_f (filter_src_offset). Block 0 also clears the status word.
+struct TapRelayout {
+    int mode;
+    int C_v, H_fv, W_fv, s_wv;  // the kernel's shape
+    int view, C, H_f, W_f;      // the caller's filter and the view onto it
+    int C_o, T, NCH, U, S, n_chunks, stack, Gr;
+};
+
 __global__ void relayout_filter_tap(const uint16_t *__restrict__ filt, uint16_t *__restrict__ fa,
-                                    uint32_t *status, int mode, int C_i, int C_o, int H_f, int W_f,
-                                    int s_w, int T, int NCH, int U, int S, int win_hf, int n_chunks,
-                                    int stack, int Gr) {
+                                    uint32_t *status, const TapRelayout a) {
     allow_dependents();  // the tap kernel may start its prologue meanwhile
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
         status[0] = 0;
         status[1] = 0;
         status[2] = 0;
     }
-    const int per_chunk = T * (TAP_A_BYTES / 2);  // elements of one (mt, cc) chunk: T taps x 2048
-    const int HW = H_f * W_f;
-    for (int chunk = blockIdx.y; chunk < n_chunks; chunk += gridDim.y) {
-        const int cc = chunk % NCH, mt = chunk / NCH;
+    const int per_chunk = a.T * (TAP_A_BYTES / 2);  // elements of one (mt, cc) chunk: T taps x 2048
+    const int64_t frow = (int64_t)a.C * a.H_f * a.W_f;
+    for (int chunk = blockIdx.y; chunk < a.n_chunks; chunk += gridDim.y) {
+        const int cc = chunk % a.NCH, mt = chunk / a.NCH;
         uint16_t *dst = fa + (int64_t)chunk * per_chunk;
         for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < per_chunk; idx += gridDim.x * blockDim.x) {
             const int e = idx & 7, rw = (idx >> 3) & 7, h = (idx >> 6) & 1, g = (idx >> 7) & 15;
             const int t = idx >> 11;
-            const int co = mt * BM + (stack ? (g & 7) : g) * 8 + rw;
+            const int co = mt * BM + (a.stack ? (g & 7) : g) * 8 + rw;
             const int k = h * 8 + e;
-            uint16_t v = 0;
-            if (co < C_o) {
-                if (mode == TAP_CH) {
-                    const int ci = cc * 16 + k;
-                    // tap of the (virtual) filter: t itself, or for a stacked group the top
-                    // tap (rows 0..63) or the bottom tap (rows 64..127, absent past W_f)
-                    int tap = t;
-                    if (stack) {
-                        const int r = t / Gr, jt = stacked_top_j(t % Gr, s_w);
-                        const int j = g < 8 ? jt : jt + s_w;
-                        tap = j < W_f ? r * W_f + j : -1;
-                    }
-                    const int ts = tap < 0 ? -1 : win_hf > 0 ? (tap % win_hf) * (HW / win_hf) + tap / win_hf : tap;
-                    if (ci < C_i && ts >= 0) v = filt[((int64_t)co * C_i + ci) * HW + ts];
+            int ci = -1, r = 0, j = 0;
+            if (a.mode == TAP_CH || a.mode == TAP_CL) {
+                // tap of the filter: t itself, or for a stacked group the top tap (rows
+                // 0..63) or the bottom tap (rows 64..127, absent past W_fv)
+                if (a.stack) {
+                    r = t / a.Gr;
+                    const int jt = stacked_top_j(t % a.Gr, a.s_wv);
+                    j = g < 8 ? jt : jt + a.s_wv;
                 } else {
-                    const int a = t / U, u = t - a * U;
-                    const int b = 16 * u + k;
-                    if (b < S) {
-                        const int jl = b / H_f, r = b - jl * H_f;
-                        const int j = a * s_w + jl;
-                        if (j < W_f) v = filt[(((int64_t)co * C_i + cc) * H_f + r) * W_f + j];
-                    }
+                    r = t / a.W_fv;
+                    j = t - r * a.W_fv;
+                }
+                ci = cc * 16 + k;
+                if (ci >= a.C_v || j >= a.W_fv) ci = -1;
+            } else {
+                const int ta = t / a.U, u = t - ta * a.U;
+                const int b = 16 * u + k;
+                if (b < a.S) {
+                    const int jl = b / a.H_fv;
+                    r = b - jl * a.H_fv;
+                    j = ta * a.s_wv + jl;
+                    if (j < a.W_fv) ci = cc;
                 }
             }
+            uint16_t v = 0;
+            if (co < a.C_o && ci >= 0)
+                v = filt[(int64_t)co * frow + filter_src_offset(a.view, ci, r, j, a.C, a.H_f, a.W_f)];
             dst[idx] = v;
         }
     }
@@ -992,7 +1054,7 @@ struct TapPlan {
     size_t smem;
     int mtiles;
     int64_t kslots;        // MMA K values per output pixel (cost model)
-    int win_hf;            // > 0: TAP_CH over the window tensor (filter taps permuted)
+    int view;              // how the kernel's filter maps to the caller's (FilterView)
 };
 
 static int sm_count() {
@@ -1028,11 +1090,13 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
     pl.mode = mode;
     const int64_t smem_max = 227 * 1024 - 1024;
     if (s.C_i * s.H_i * s.W_i >= (1ll << 31)) return pl;
+    const bool chan = mode == TAP_CH || mode == TAP_CL;
+    if (mode == TAP_CL && s.C_i % 8 != 0) return pl;  // 16-byte entries of 8 channels
     int64_t pitch, T, U = 0, S = 0, A = 0, NCH;
-    // stacking (TAP_CH, C_o <= 64, some tap has a partner): T counts tap groups
-    const int stack = (mode == TAP_CH && s.C_o <= 64 && s.W_f > s.s_w) ? 1 : 0;
+    // stacking (TAP_CH / TAP_CL, C_o <= 64, some tap has a partner): T counts tap groups
+    const int stack = (chan && s.C_o <= 64 && s.W_f > s.s_w) ? 1 : 0;
     const int Gr = stack ? stacked_groups_per_row((int)s.W_f, (int)s.s_w) : 0;
-    if (mode == TAP_CH) {
+    if (chan) {
         pitch = (s.W_i + s.s_w - 1) / s.s_w;
         T = stack ? s.H_f * Gr : s.H_f * s.W_f;
         NCH = (s.C_i + 15) / 16;
@@ -1067,7 +1131,7 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
         const int64_t NTp = (Q * pitch + stack + 15) / 16 * 16;
         const int64_t RR = (Q - 1) * s.s_h + s.H_f;  // input rows under a tile of Q rows
         int64_t PB = 0, lbo, stage_b;
-        if (mode == TAP_CH) {
+        if (chan) {
             const int64_t HH = (RR + s.s_h - 1) / s.s_h;
             PB = HH * pitch * 16;
             lbo = s.s_h * s.s_w * PB;
@@ -1086,8 +1150,10 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
         stage_b = (stage_b + 127) / 128 * 128;
         // raw staging slot (elements, a multiple of 64): TAP_CH 16 channels of the tile's
         // input rows (only when rows are whole 16-byte vectors), TAP_WX one channel's
-        // input rows, TAP_WW its window rows, each with room for the alignment lead
-        const int64_t slot = mode == TAP_CH ? (s.W_i % 8 == 0 ? 16 * RR * s.W_i : 0)
+        // input rows, TAP_WW its window rows, each with room for the alignment lead;
+        // TAP_CL copies straight into the slab
+        const int64_t slot = mode == TAP_CL ? 0
+                             : mode == TAP_CH ? (s.W_i % 8 == 0 ? 16 * RR * s.W_i : 0)
                              : mode == TAP_WX ? RR * s.W_i + 16
                                               : Q * s.W_i * s.H_f + 16;
         const int64_t slot_e = (slot + 63) / 64 * 64;
@@ -1098,7 +1164,7 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
         // filter stages
         for (int pass = 0; pass < 2; ++pass)
         for (int ring : {1, 0}) {
-          const int64_t raw_e = mode == TAP_CH ? (ring ? 2 * slot_e : 0) : (ring ? 2 : 1) * slot_e;
+          const int64_t raw_e = chan ? (ring ? 2 * slot_e : 0) : (ring ? 2 : 1) * slot_e;
           if (ring && slot_e == 0) continue;
           for (int TG : {9, 8, 6, 5, 4, 3, 2, 1}) {
             const int tg = (int)std::min<int64_t>(TG, T);
@@ -1189,37 +1255,71 @@ static Shape window_as_input(const Shape &s) {
     return v;
 }
 
-// Kernel choice: among the tap kernels that apply -- fused: over channels
-// (TAP_CH) or over window rows (TAP_WX); from the window tensor: over channels
-// of the window tensor seen as an input (window_as_input) or over window rows
-// (TAP_WW) -- the one that needs the fewest MMA K values per pixel. It falls back
-// to the expand kernel when its K padding costs more than half again the expand
-// kernel's K.
-static TapPlan choose_tap(const Shape &s, bool fused, int64_t sms = 148) {
-    const int64_t expand_k = s.C_i * ((s.H_f * s.W_f + 7) / 8 * 8);
+// A channels-last tensor x[n][h][w][c] is, row by row, one channel of H x W*C
+// elements: the convolution with C_i channels is the one-channel convolution
+// of that image by the H_f x W_f*C_i filter whose column j*C_i + c is channel c
+// of filter column j, at stride (s_h, s_w*C_i). The output extents are unchanged.
+static Shape channels_as_columns(const Shape &s) {
+    Shape v = s;
+    v.C_i = 1;
+    v.W_i = s.W_i * s.C_i;
+    v.W_f = s.W_f * s.C_i;
+    v.s_w = s.s_w * s.C_i;
+    return v;
+}
+
+// Kernel choice: among the tap kernels that apply, the one that needs the
+// fewest MMA K values per pixel (ties: the first listed).
+//   NCHW fused:   TAP_CH over channels; TAP_WX over window rows.
+//   NCHW window:  TAP_CH over the channels of the window tensor seen as an input
+//                 (window_as_input); TAP_WW over window rows.
+//   NHWC fused:   TAP_CL over channels (C_i a multiple of 8); TAP_WX over the
+//                 input seen as one channel (channels_as_columns).
+//   NHWC window:  TAP_CL over the window tensor seen as an input; TAP_WW over it
+//                 seen as one channel.
+// NCHW falls back to the expand kernel when the choice's K padding costs more
+// than half again the expand kernel's K; NHWC has no fallback.
+static TapPlan choose_tap(const Shape &s, bool fused, int layout, int64_t sms = 148) {
+    struct Cand {
+        int mode;
+        Shape v;
+        int view;
+    };
+    Cand cand[2];
+    if (layout == LAYOUT_NHWC) {
+        const Shape base = fused ? s : window_as_input(s);
+        cand[0] = {TAP_CL, base, fused ? VIEW_IDENT : VIEW_WIN};
+        cand[1] = {fused ? TAP_WX : TAP_WW, channels_as_columns(base), fused ? VIEW_CL_X : VIEW_CL_WIN};
+    } else if (fused) {
+        cand[0] = {TAP_CH, s, VIEW_IDENT};
+        cand[1] = {TAP_WX, s, VIEW_IDENT};
+    } else {
+        cand[0] = {TAP_CH, window_as_input(s), VIEW_WIN};
+        cand[1] = {TAP_WW, s, VIEW_IDENT};
+    }
     TapPlan best{};
     best.ok = false;
-    for (int mode : {TAP_CH, TAP_WX, TAP_WW}) {
-        if (fused && mode == TAP_WW) continue;
-        if (!fused && mode == TAP_WX) continue;
-        TapPlan pl = (!fused && mode == TAP_CH) ? plan_tap(window_as_input(s), TAP_CH, sms)
-                                                : plan_tap(s, mode, sms);
-        pl.win_hf = (!fused && mode == TAP_CH) ? (int)s.H_f : 0;
+    for (const Cand &c : cand) {
+        TapPlan pl = plan_tap(c.v, c.mode, sms);
+        pl.view = c.view;
         if (pl.ok && (!best.ok || pl.kslots < best.kslots)) best = pl;
     }
-    if (best.ok && best.kslots * 2 > expand_k * 3) best.ok = false;
+    const int64_t expand_k = s.C_i * ((s.H_f * s.W_f + 7) / 8 * 8);
+    if (layout == LAYOUT_NCHW && best.ok && best.kslots * 2 > expand_k * 3) best.ok = false;
     return best;
 }
 
-size_t conv_tc_filter_bytes(const Shape &s, bool fused) {
-    const TapPlan pl = choose_tap(s, fused);
+size_t conv_tc_filter_bytes(const Shape &s, bool fused, int layout) {
+    const TapPlan pl = choose_tap(s, fused, layout);
     if (pl.ok) return round_up((size_t)pl.mtiles * pl.p.NCH * pl.p.T * TAP_A_BYTES, 256);
+    if (layout != LAYOUT_NCHW) return 0;
     const ExpandGeom g = expand_geom(s);
     return round_up((size_t)g.mtiles * BM * (size_t)g.K_pad * 2, 256);
 }
 
-bool conv_tc_supported(const Shape &s, bool fused) {
-    if (choose_tap(s, fused).ok) return true;
+bool conv_tc_supported(const Shape &s, bool fused, int layout) {
+    if (choose_tap(s, fused, layout).ok) return true;
+    if (layout != LAYOUT_NCHW) return false;
     const int64_t img = fused ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * s.W_i * s.H_f;
     const int64_t KKP = (s.H_f * s.W_f + 7) / 8 * 8;
     const int64_t P = s.H_o * s.W_o;
@@ -1229,7 +1329,7 @@ bool conv_tc_supported(const Shape &s, bool fused) {
 }
 
 static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *filt, void *out,
-                              void *ws, const Shape &s, bool bf16, cudaStream_t st) {
+                              void *ws, const Shape &s, int layout, bool bf16, cudaStream_t st) {
     TapParams p = pl.p;
     uint32_t *status = static_cast<uint32_t *>(ws);
     uint16_t *fa = reinterpret_cast<uint16_t *>(static_cast<unsigned char *>(ws) + kStatusBytes);
@@ -1237,9 +1337,13 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
     const int per_chunk = p.T * (int)(TAP_A_BYTES / 2);
     const dim3 rgrid((unsigned)std::min(std::max(1, (per_chunk + 255) / 256), 64),
                      (unsigned)std::min(n_chunks, 65535));
-    relayout_filter_tap<<<rgrid, 256, 0, st>>>(static_cast<const uint16_t *>(filt), fa, status, pl.mode, p.C_i,
-                                               p.C_o, p.H_f, p.W_f, p.s_w, p.T, p.NCH, p.U, p.S, pl.win_hf,
-                                               n_chunks, p.stack, p.Gr);
+    TapRelayout ra;
+    ra.mode = pl.mode;
+    ra.C_v = p.C_i; ra.H_fv = p.H_f; ra.W_fv = p.W_f; ra.s_wv = p.s_w;
+    ra.view = pl.view; ra.C = (int)s.C_i; ra.H_f = (int)s.H_f; ra.W_f = (int)s.W_f;
+    ra.C_o = p.C_o; ra.T = p.T; ra.NCH = p.NCH; ra.U = p.U; ra.S = p.S;
+    ra.n_chunks = n_chunks; ra.stack = p.stack; ra.Gr = p.Gr;
+    relayout_filter_tap<<<rgrid, 256, 0, st>>>(static_cast<const uint16_t *>(filt), fa, status, ra);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     p.src = static_cast<const uint16_t *>(src);
@@ -1253,6 +1357,8 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
     p.div_sh = make_fastdiv((uint32_t)p.s_h);
     p.div_sw = make_fastdiv((uint32_t)p.s_w);
     p.div_vpc = make_fastdiv((uint32_t)std::max(1, ((p.Qmax - 1) * p.s_h + p.H_f) * p.W_i / 8));
+    p.div_wi = make_fastdiv((uint32_t)p.W_i);
+    p.nhwc = layout == LAYOUT_NHWC ? 1 : 0;
     p.bf16 = bf16 ? 1 : 0;
     const unsigned grid = (unsigned)std::min<int64_t>(sm_count(), p.tiles_total);
     auto go = [&](auto kernel) -> cudaError_t {
@@ -1273,14 +1379,16 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
         return cudaLaunchKernelEx(&cfg, kernel, p);
     };
     if (pl.mode == TAP_CH) return go(conv_tc_tap_kernel<TAP_CH>);
+    if (pl.mode == TAP_CL) return go(conv_tc_tap_kernel<TAP_CL>);
     if (pl.mode == TAP_WX) return go(conv_tc_tap_kernel<TAP_WX>);
     return go(conv_tc_tap_kernel<TAP_WW>);
 }
 
 cudaError_t launch_conv_tc(const void *src, const void *filt, void *out, void *ws, const Shape &s,
-                           bool fused, bool bf16, cudaStream_t st) {
-    const TapPlan pl = choose_tap(s, fused, sm_count());
-    if (pl.ok) return launch_tap(pl, src, filt, out, ws, s, bf16, st);
+                           bool fused, int layout, bool bf16, cudaStream_t st) {
+    const TapPlan pl = choose_tap(s, fused, layout, sm_count());
+    if (pl.ok) return launch_tap(pl, src, filt, out, ws, s, layout, bf16, st);
+    if (layout != LAYOUT_NCHW) return cudaErrorNotSupported;
     const ExpandGeom g = expand_geom(s);
     uint32_t *status = static_cast<uint32_t *>(ws);
     uint16_t *fa = reinterpret_cast<uint16_t *>(static_cast<unsigned char *>(ws) + kStatusBytes);

@@ -53,25 +53,62 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
     return (__umulhi(n, f.m) + n) >> f.l;
 }
 
+// A kernel computes the convolution of a (virtual) shape whose filter is a
+// re-ordering of the caller's filter w[C_o][C][H_f][W_f]. The view names the
+// re-ordering: a virtual filter element (ci_v, r_v, j_v) is the caller's
+// element (c, r, j) with
+//   VIEW_IDENT     (ci_v, r_v, j_v)                              the shape itself
+//   VIEW_WIN       (ci_v, j_v % H_f, j_v / H_f)                  NCHW window tensor as the input,
+//                                                                 one row of W_f*H_f taps
+//   VIEW_CL_X      (j_v % C, r_v, j_v / C)                       NHWC input as one channel of
+//                                                                 H_i x W_i*C (columns (w, c))
+//   VIEW_CL_WIN    (j_v % C, (j_v / C) % H_f, j_v / C / H_f)     NHWC window tensor as one channel,
+//                                                                 one row of W_f*H_f*C taps
+//   VIEW_CL_ROWS   (j_v % C, ci_v, j_v / C)                      NHWC input, filter rows as channels,
+//                                                                 one row of W_f*C taps each
+enum FilterView { VIEW_IDENT = 0, VIEW_WIN = 1, VIEW_CL_X = 2, VIEW_CL_WIN = 3, VIEW_CL_ROWS = 4 };
+
+// Offset of virtual filter element (ci_v, r_v, j_v) within the caller's filter
+// row w[co][:][:][:] (C x H_f x W_f are the caller's extents).
+__host__ __device__ inline int64_t filter_src_offset(int view, int ci_v, int r_v, int j_v, int C, int H_f,
+                                                     int W_f) {
+    int c = ci_v, r = r_v, j = j_v;
+    switch (view) {
+        case VIEW_WIN: r = j_v % H_f; j = j_v / H_f; break;
+        case VIEW_CL_X: c = j_v % C; j = j_v / C; break;
+        case VIEW_CL_WIN: c = j_v % C; r = (j_v / C) % H_f; j = j_v / C / H_f; break;
+        case VIEW_CL_ROWS: c = j_v % C; r = ci_v; j = j_v / C; break;
+        default: break;
+    }
+    return ((int64_t)c * H_f + r) * W_f + j;
+}
+
+// Tensor layouts of the convolution entry points.
+enum Layout { LAYOUT_NCHW = 0, LAYOUT_NHWC = 1 };
+
 // ---- launchers (each returns cudaSuccess or the launch error) ----
 
-// Window transform of esz-byte elements.
+// Window transform of esz-byte elements (NCHW), and its channels-last form
+// win[n][ho][w*H_f + r][c] = x[n][ho*s_h + r][w][c].
 cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, cudaStream_t st);
 bool transform_supported(const Shape &s, int esz);
+cudaError_t launch_transform_nhwc(const void *x, void *win, const Shape &s, int esz, cudaStream_t st);
+bool transform_nhwc_supported(const Shape &s, int esz);
 
 // fp32 CUDA-core convolution; from_x selects the fused variant that gathers
-// from the NCHW input instead of the window tensor. ws holds the status block
-// followed by the re-laid filter.
-size_t conv_f32_filter_bytes(const Shape &s);
-bool conv_f32_supported(const Shape &s, bool from_x);
+// from the input instead of the window tensor; layout is NCHW or NHWC for the
+// input, window tensor and output alike. ws holds the status block followed
+// by the re-laid filter.
+size_t conv_f32_filter_bytes(const Shape &s, bool from_x, int layout);
+bool conv_f32_supported(const Shape &s, bool from_x, int layout);
 cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *ws,
-                            const Shape &s, bool from_x, cudaStream_t st);
+                            const Shape &s, bool from_x, int layout, cudaStream_t st);
 
-// fp16/bf16 tensor-core convolution (tcgen05). mode: 0 = from window tensor,
-// 1 = fused from NCHW input.
-size_t conv_tc_filter_bytes(const Shape &s, bool fused);
-bool conv_tc_supported(const Shape &s, bool fused);
+// fp16/bf16 tensor-core convolution (tcgen05): from the window tensor or fused
+// from the input, in either layout.
+size_t conv_tc_filter_bytes(const Shape &s, bool fused, int layout);
+bool conv_tc_supported(const Shape &s, bool fused, int layout);
 cudaError_t launch_conv_tc(const void *src, const void *filt, void *out, void *ws,
-                           const Shape &s, bool fused, bool bf16, cudaStream_t st);
+                           const Shape &s, bool fused, int layout, bool bf16, cudaStream_t st);
 
 }  // namespace im2win

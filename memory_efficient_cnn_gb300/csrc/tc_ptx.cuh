@@ -57,6 +57,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
+// cp.async 16-byte copies of this thread still in flight count towards one
+// arrival on `bar` when they complete (the barrier's expected count covers it).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -274,14 +279,63 @@ __device__ __forceinline__ void store_block(const uint32_t *stage, int c0, int r
     }
 }
 
+// Channels-last staging of 32 columns (half `half` of a 64-column block): lane
+// l holds channel l of columns half*32 + i in v[i]. Lane pairs swap values so
+// that each lane packs two adjacent channels of one column:
+//   stage[col*16 + l/2] = (channel 2(l/2), channel 2(l/2)+1) of column col,
+// i.e. a column's 32 channels are 64 contiguous bytes. Every store is one
+// conflict-free wavefront (32 consecutive words).
+__device__ __forceinline__ void stage_half_cl(uint32_t *stage, int half, const float (&v)[32], int bf16) {
+    const int lane = threadIdx.x & 31;
+    const bool odd = (lane & 1) != 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float a = v[2 * i], b = v[2 * i + 1];
+        const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+        const float lo = odd ? recv : a, hi = odd ? b : recv;
+        stage[(half * 32 + 2 * i + (odd ? 1 : 0)) * 16 + (lane >> 1)] = pack2(lo, hi, bf16);
+    }
+}
+
+// Stores a channels-last staged block of 64 columns: column col of the block
+// goes to out_c + off_of(c0 + col)*cstride (off_of < 0: not an output), its
+// channels 0..rows-1 contiguous. Four lanes cover a column's 32 channels with
+// 16-byte stores when cstride is a multiple of 8 (rows then is too), element
+// stores otherwise.
+template <typename OffFn>
+__device__ __forceinline__ void store_block_cl(const uint32_t *stage, int c0, int rows, int64_t cstride,
+                                               uint16_t *out_c, OffFn off_of) {
+    const int lane = threadIdx.x & 31;
+    const int oa = off_of(c0 + lane), ob = off_of(c0 + 32 + lane);
+    const bool vec = (cstride & 7) == 0;
+    const int q = lane & 3;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int col = it * 8 + (lane >> 2);
+        const int o = __shfl_sync(0xffffffffu, it < 4 ? oa : ob, col & 31);
+        if (o < 0 || q * 8 >= rows) continue;
+        const uint4 val = *reinterpret_cast<const uint4 *>(stage + col * 16 + q * 4);
+        uint16_t *d = out_c + (int64_t)o * cstride + q * 8;
+        if (vec) {
+            *reinterpret_cast<uint4 *>(d) = val;
+        } else {
+            const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (q * 8 + e < rows) d[e] = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
+        }
+    }
+}
+
 // Faster drain for the tap kernels. The warp owns TMEM columns [c_begin,
 // c_end) of its 32 accumulator lanes (taddr = lane quarter base). Per block of
 // 64 columns: two 32-column TMEM loads (the next block's first load is in
 // flight while this block is stored), rounding to fp16/bf16, a transpose
 // through the warp's staging area (32 rows x 33 words), then store_block.
 // The last block may reach past c_end: off_of must return -1 for its columns
-// that are not the warp's to store.
-template <typename OffFn>
+// that are not the warp's to store. CL: channels-last output (stage_half_cl,
+// store_block_cl; row_stride is then the stride between positions).
+template <bool CL, typename OffFn>
 __device__ __forceinline__ void drain_columns(uint32_t taddr, int c_begin, int c_end, uint32_t *stage,
                                               int rows, int64_t row_stride, int bf16,
                                               uint16_t *out_c, OffFn off_of) {
@@ -294,14 +348,25 @@ __device__ __forceinline__ void drain_columns(uint32_t taddr, int c_begin, int c
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             tmem_wait_ld();
+            if (CL) {
+                float v[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                stage[lane * 33 + half * 16 + i] = pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), bf16);
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                stage_half_cl(stage, half, v, bf16);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    stage[lane * 33 + half * 16 + i] =
+                        pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), bf16);
+            }
             const int nxt = half == 0 ? c0 + 32 : c0 + 64;
             if (nxt < c_end) tmem_ld32(taddr + (uint32_t)nxt, r);
         }
         __syncwarp();
-        store_block(stage, c0, rows, row_stride, out_c, off_of);
+        if (CL)
+            store_block_cl(stage, c0, rows, row_stride, out_c, off_of);
+        else
+            store_block(stage, c0, rows, row_stride, out_c, off_of);
         __syncwarp();
     }
 }
@@ -337,7 +402,7 @@ __device__ __forceinline__ bool drain_stacked_lower(uint32_t taddr, int c_begin,
 
 // Stacked drain, upper half: accumulator rows 0..63 plus the partner's shifted
 // values give the outputs; rounding, transpose and store as in drain_columns.
-template <typename OffFn>
+template <bool CL, typename OffFn>
 __device__ __forceinline__ bool drain_stacked_upper(uint32_t taddr, int c_begin, int c_end, uint32_t *stage,
                                                     const float *xbuf, uint32_t bar_full, uint32_t bar_empty,
                                                     uint32_t *k, const Ctl &ctl, uint32_t site, int rows,
@@ -350,15 +415,25 @@ __device__ __forceinline__ bool drain_stacked_upper(uint32_t taddr, int c_begin,
             tmem_ld32(taddr + (uint32_t)(c0 + 32 * half), r);
             tmem_wait_ld();
             if (!warp_bar_wait(bar_full, *k & 1, ctl, site)) return false;
+            if (CL) {
+                float v[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                stage[lane * 33 + half * 16 + i] =
-                    pack2(__uint_as_float(r[2 * i]) + xbuf[lane * 33 + 2 * i],
-                          __uint_as_float(r[2 * i + 1]) + xbuf[lane * 33 + 2 * i + 1], bf16);
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + xbuf[lane * 33 + i];
+                stage_half_cl(stage, half, v, bf16);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    stage[lane * 33 + half * 16 + i] =
+                        pack2(__uint_as_float(r[2 * i]) + xbuf[lane * 33 + 2 * i],
+                              __uint_as_float(r[2 * i + 1]) + xbuf[lane * 33 + 2 * i + 1], bf16);
+            }
             mbar_arrive(bar_empty);
         }
         __syncwarp();
-        store_block(stage, c0, rows, row_stride, out_c, off_of);
+        if (CL)
+            store_block_cl(stage, c0, rows, row_stride, out_c, off_of);
+        else
+            store_block(stage, c0, rows, row_stride, out_c, off_of);
         __syncwarp();
     }
     return true;

@@ -286,6 +286,146 @@ cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, 
     return cudaGetLastError();
 }
 
+// ---- channels-last window transform
+// win[n][ho][w*H_f + r][c] = x[n][ho*s_h + r][w][c]: the window row of (n, ho)
+// is W_i*H_f runs of C_i contiguous elements, run (w, r) being the C_i
+// channels of input position (ho*s_h + r, w). The output is written as whole
+// 16-byte vectors in order (coalesced stores); a grid-stride loop keeps four
+// vectors in flight per thread, and consecutive output rows, which share input
+// rows, are written at about the same time, so the rows are re-read from L2.
+namespace {
+
+struct TNParams {
+    const void *x;
+    void *win;
+    int64_t elems;        // window elements
+    int64_t vecs;         // 16-byte output vectors (the last may be partial)
+    int64_t Lp;           // window row length W_i*H_f*C_i
+    int C_i, H_i, W_i, H_f, s_h, H_o;
+    int VPR;              // vectors per run (vector path: C_i*esz / 16)
+    FastDiv div_vpr, div_wh, div_hf, div_ho;
+};
+
+// C_i*esz a multiple of 16: every run is whole, aligned 16-byte vectors.
+__global__ void __launch_bounds__(256) transform_nhwc_vec(TNParams p) {
+    const uint4 *__restrict__ x = static_cast<const uint4 *>(p.x);
+    uint4 *__restrict__ win = static_cast<uint4 *>(p.win);
+    const int WH = p.W_i * p.H_f;
+    const int G = gridDim.x * blockDim.x;
+    auto src_of = [&](int v) -> int64_t {
+        const int R = (int)fdiv((uint32_t)v, p.div_vpr);  // run: (n, ho, w, r)
+        const int k = v - R * p.VPR;
+        const int row = (int)fdiv((uint32_t)R, p.div_wh);  // n*H_o + ho
+        const int pp = R - row * WH;                      // w*H_f + r
+        const int w = (int)fdiv((uint32_t)pp, p.div_hf);
+        const int r = pp - w * p.H_f;
+        const int n = (int)fdiv((uint32_t)row, p.div_ho);
+        const int ho = row - n * p.H_o;
+        return (((int64_t)n * p.H_i + (int64_t)ho * p.s_h + r) * p.W_i + w) * p.VPR + k;
+    };
+    for (int v0 = blockIdx.x * blockDim.x + threadIdx.x; v0 < p.vecs; v0 += 4 * G) {
+        uint4 val[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int v = v0 + u * G;
+            if (v < p.vecs) val[u] = __ldg(x + src_of(v));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int v = v0 + u * G;
+            if (v < p.vecs) win[v] = val[u];
+        }
+    }
+}
+
+// Any C_i: each thread builds one 16-byte output vector element by element,
+// stepping (c, r, w, ho, n) from the vector's first element; a partial last
+// vector is stored element by element.
+template <typename E>
+__global__ void __launch_bounds__(256) transform_nhwc_elem(TNParams p) {
+    constexpr int V = 16 / sizeof(E);
+    const E *__restrict__ x = static_cast<const E *>(p.x);
+    E *__restrict__ win = static_cast<E *>(p.win);
+    for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < p.vecs;
+         v += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t f0 = v * V;
+        const int64_t row = f0 / p.Lp;
+        const int64_t off = f0 - row * p.Lp;
+        int n = (int)(row / p.H_o), ho = (int)(row - (int64_t)n * p.H_o);
+        const int64_t pos = off / p.C_i;
+        int c = (int)(off - pos * p.C_i);
+        int w = (int)(pos / p.H_f), r = (int)(pos - (int64_t)w * p.H_f);
+        union {
+            uint4 u;
+            E e[V];
+        } out;
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            out.e[e] = f0 + e < p.elems
+                           ? x[(((int64_t)n * p.H_i + (int64_t)ho * p.s_h + r) * p.W_i + w) * p.C_i + c]
+                           : E(0);
+            if (++c == p.C_i) {
+                c = 0;
+                if (++r == p.H_f) {
+                    r = 0;
+                    if (++w == p.W_i) {
+                        w = 0;
+                        if (++ho == p.H_o) { ho = 0; ++n; }
+                    }
+                }
+            }
+        }
+        if (f0 + V <= p.elems) {
+            *reinterpret_cast<uint4 *>(win + f0) = out.u;
+        } else {
+            for (int e = 0; f0 + e < p.elems; ++e) win[f0 + e] = out.e[e];
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_transform_nhwc(const void *x, void *win, const Shape &s, int esz, cudaStream_t st) {
+    TNParams p;
+    p.x = x;
+    p.win = win;
+    p.Lp = s.W_i * s.H_f * s.C_i;
+    p.elems = s.N * s.H_o * p.Lp;
+    p.vecs = (p.elems * esz + 15) / 16;
+    p.C_i = (int)s.C_i;
+    p.H_i = (int)s.H_i;
+    p.W_i = (int)s.W_i;
+    p.H_f = (int)s.H_f;
+    p.s_h = (int)s.s_h;
+    p.H_o = (int)s.H_o;
+    const bool vec = (s.C_i * esz) % 16 == 0;
+    p.VPR = vec ? (int)(s.C_i * esz / 16) : 1;
+    p.div_vpr = make_fastdiv((uint32_t)p.VPR);
+    p.div_wh = make_fastdiv((uint32_t)(s.W_i * s.H_f));
+    p.div_hf = make_fastdiv((uint32_t)s.H_f);
+    p.div_ho = make_fastdiv((uint32_t)s.H_o);
+    if (p.vecs == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t per_pass = vec ? 4 : 1;  // vectors per thread and grid pass
+    const int64_t need = (p.vecs + 256 * per_pass - 1) / (256 * per_pass);
+    const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)sms * 8));
+    if (vec)
+        transform_nhwc_vec<<<blocks, 256, 0, st>>>(p);
+    else if (esz == 2)
+        transform_nhwc_elem<uint16_t><<<blocks, 256, 0, st>>>(p);
+    else
+        transform_nhwc_elem<uint32_t><<<blocks, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+// The vector path indexes output vectors and runs with 32-bit arithmetic.
+bool transform_nhwc_supported(const Shape &s, int esz) {
+    const int64_t runs = s.N * s.H_o * s.W_i * s.H_f;
+    const int64_t bytes = runs * s.C_i * esz;
+    return bytes / 16 < (1ll << 30) && runs < (1ll << 31) && s.W_i * s.H_f * s.C_i < (1ll << 40);
+}
+
 // The transform indexes a band with 32-bit arithmetic and launches one CTA per
 // (plane, band, column tile).
 bool transform_supported(const Shape &s, int esz) {

@@ -55,7 +55,7 @@ def test_transform_size_is_the_window_tensor(lib, layer):
 @pytest.mark.parametrize("layer", wl.ALL, ids=lambda l: l.name)
 def test_conv_workspaces_hold_status_and_filter_only(lib, layer):
     for dt, esz in ((mec.F32, 4), (mec.F16, 2), (mec.BF16, 2)):
-        for op in (mec.OP_CONV, mec.OP_CONV_FUSED):
+        for op in (mec.OP_CONV, mec.OP_CONV_FUSED, mec.OP_CONV_NHWC, mec.OP_CONV_FUSED_NHWC):
             b = mec.im2win_workspace_size(op, *layer.shape_args, dt)
             filt = layer.C_o * layer.C_i * layer.H_f * layer.W_f * esz
             assert b % 256 == 0 and b >= 256 + filt
