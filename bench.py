@@ -21,6 +21,9 @@ e2e = the same FLOPs per step through the same API calls when every step also
 copies its inputs from pinned host memory and its outputs back; consecutive
 steps are pipelined over two device buffer sets and separate copy streams.
 
+`--layout nhwc` runs the same step on channels-last tensors (x[N][H_i][W_i][C_i],
+win[N][H_o][W_i*H_f][C_i], out[N][H_o][W_o][C_o]) through the *_nhwc calls.
+
 `--impl reference` times the CPU oracle (plain fp64 C, OpenMP) on a bounded
 sample of the same workload instead.
 """
@@ -45,9 +48,9 @@ if ROOT not in sys.path:
 # (summaries under profiles/); a kernel absent here has no capture of its
 # current version.
 DRAM_TRAFFIC: dict = {
-    # conv_f32_kernel<96,24,3,2,0>, cv1: 211.2 MB read + 106.9 MB written
+    # conv_f32_kernel<96,24,3,2,0,0>, cv1: 211.3 MB read + 106.5 MB written
     # (profiles/conv_f32_kernel_cv1.md)
-    ("cv1", "conv_f32_window_f32"): 318.1e6,
+    ("cv1", "conv_f32_window_f32"): 317.8e6,
 }
 
 METRIC = "im2win conv TFLOPS and % of dense peak per layer shape; workspace bytes"
@@ -231,6 +234,8 @@ def main():
                     help="workload: cv1 (default, the headline) or another layer of the parity set")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline (0 disables it)")
+    ap.add_argument("--layout", choices=["nchw", "nhwc"], default="nchw",
+                    help="tensor layout of input, window tensor and output")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -276,9 +281,12 @@ def main():
 
     # one step: per dtype, the transform, the conv from the window tensor and
     # (fp16/bf16) the fused conv; fp32 runs on the CUDA cores
+    cl = args.layout == "nhwc"
+    sfx = "_nhwc" if cl else ""
     host_in = []
     for d in layer.dtypes:
-        host_in += list(wl.make_inputs(layer, d))
+        xh, wh = wl.make_inputs(layer, d)
+        host_in += [xh.permute(0, 2, 3, 1).contiguous() if cl else xh, wh]
 
     def make_set():
         """Device buffers of one step (inputs, window tensors, outputs, workspaces)
@@ -292,22 +300,31 @@ def main():
         tdt = wl.DTYPES[d]
         x, w = xc.to(dev), wc.to(dev)
         dev_in += [x, w]
-        win = torch.empty((N, C_i, H_o, W_i * H_f), dtype=tdt, device=dev)
-        out_w = torch.empty((N, C_o, H_o, W_o), dtype=tdt, device=dev)
-        ws = mec.workspace(mec.OP_CONV, x.shape, w.shape, stride, tdt, dev)
-        ops.append((f"transform_{d}", d, "transform",
-                    lambda x=x, win=win: mec.im2win_transform(x, win, C_o, H_f, W_f, s_h, s_w),
+        nchw = (N, C_i, H_i, W_i)
+        if cl:
+            win = torch.empty((N, H_o, W_i * H_f, C_i), dtype=tdt, device=dev)
+            out_w = torch.empty((N, H_o, W_o, C_o), dtype=tdt, device=dev)
+            tr, cv, cvf = mec.im2win_transform_nhwc, mec.im2win_conv_nhwc, mec.im2win_conv_fused_nhwc
+            op_w, op_f = mec.OP_CONV_NHWC, mec.OP_CONV_FUSED_NHWC
+        else:
+            win = torch.empty((N, C_i, H_o, W_i * H_f), dtype=tdt, device=dev)
+            out_w = torch.empty((N, C_o, H_o, W_o), dtype=tdt, device=dev)
+            tr, cv, cvf = mec.im2win_transform, mec.im2win_conv, mec.im2win_conv_fused
+            op_w, op_f = mec.OP_CONV, mec.OP_CONV_FUSED
+        ws = mec.workspace(op_w, nchw, w.shape, stride, tdt, dev)
+        ops.append((f"transform_{d}{sfx}", d, "transform",
+                    lambda x=x, win=win: tr(x, win, C_o, H_f, W_f, s_h, s_w),
                     {"win_bytes": win.numel() * win.element_size()}))
         kind = "conv_f32" if d == "f32" else "conv_tc"
-        ops.append((f"{kind}_window_{d}", d, "window",
-                    lambda win=win, w=w, o=out_w, ws=ws: mec.im2win_conv(win, w, o, ws, *shp),
+        ops.append((f"{kind}_window_{d}{sfx}", d, "window",
+                    lambda win=win, w=w, o=out_w, ws=ws: cv(win, w, o, ws, *shp),
                     {"ws_bytes": ws.numel()}))
         outs.append(out_w)
         if d != "f32":
             out_f = torch.empty_like(out_w)
-            wsf = mec.workspace(mec.OP_CONV_FUSED, x.shape, w.shape, stride, tdt, dev)
-            ops.append((f"conv_tc_fused_{d}", d, "fused",
-                        lambda x=x, w=w, o=out_f, ws=wsf: mec.im2win_conv_fused(x, w, o, ws, s_h, s_w),
+            wsf = mec.workspace(op_f, nchw, w.shape, stride, tdt, dev)
+            ops.append((f"conv_tc_fused_{d}{sfx}", d, "fused",
+                        lambda x=x, w=w, o=out_f, ws=wsf: cvf(x, w, o, ws, s_h, s_w),
                         {"ws_bytes": wsf.numel()}))
             outs.append(out_f)
 
@@ -441,10 +458,10 @@ def main():
             kernels[name]["workspace_bytes"] = extra["ws_bytes"]
     workspace = {}
     for d in layer.dtypes:
-        ws_conv = kernels[f"{'conv_f32' if d == 'f32' else 'conv_tc'}_window_{d}"]["workspace_bytes"]
+        ws_conv = kernels[f"{'conv_f32' if d == 'f32' else 'conv_tc'}_window_{d}{sfx}"]["workspace_bytes"]
         workspace[f"two_step_{d}"] = win_b[d] + ws_conv
         if d != "f32":
-            workspace[f"fused_{d}"] = kernels[f"conv_tc_fused_{d}"]["workspace_bytes"]
+            workspace[f"fused_{d}"] = kernels[f"conv_tc_fused_{d}{sfx}"]["workspace_bytes"]
         workspace[f"im2col_{d}"] = col_b[d]
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     dk = kernels[dom]
@@ -453,7 +470,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "+".join(layer.dtypes), "data": "synthetic",
-        "config": {"workload": workload_str(layer),
+        "config": {"workload": workload_str(layer), "layout": "NHWC" if cl else "NCHW",
                    "step": ", ".join(names),
                    "parallelism": f"replicas x{world}", "l2": "flushed between steps (512 MB write)"},
         "roofline": {"kernel": dom, "bound": dk["bound"], "achieved": dk["achieved"],

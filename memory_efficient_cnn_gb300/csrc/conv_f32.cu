@@ -51,7 +51,6 @@ struct F32Params {
     int S;               // s_w * H_f
     int64_t img_src;     // elements of src per image
     int cs;              // window path: element stride between channels (H_o*L for the NCHW window)
-    int nhwc;            // output out[n][ho][wo][co] instead of out[n][co][ho][wo]
     int C_o_pad;         // row length of the transposed filter (a multiple of the channel tile)
     FastDiv div_KK, div_Wo, div_Hf;
 };
@@ -102,7 +101,7 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // w % (KC/8) and walks every (NW/(KC/8))-th group of 4 pixels. From the NCHW
 // input consecutive pixels of a row are (unit stride), so lane l of warp w
 // gathers pixels l + 32i at the KPT values of k w*KPT ...
-template <int TM, int KC, int STAGES, int MINB, bool FROM_X>
+template <int TM, int KC, int STAGES, int MINB, bool FROM_X, bool CL>
 __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
     constexpr int NT = TM * 2;                 // (TM/8) x 16 threads
     constexpr int NW = NT / 32;                           // warps
@@ -221,8 +220,8 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
     }
     cp_async_wait<0>();
 
-    // ---- epilogue: out[n][co][p], or out[n][p][co] (8 consecutive channels per pixel)
-    if (p.nhwc) {
+    // ---- epilogue: out[n][co][p], or (CL) out[n][p][co] (8 consecutive channels per pixel)
+    if (CL) {
         const int cb = co0 + ty * 8;
         const bool vec = (p.C_o & 3) == 0 && cb + 8 <= p.C_o;
 #pragma unroll
@@ -280,14 +279,14 @@ __global__ void relayout_filter_f32(const float *__restrict__ filt, float *__res
     }
 }
 
-template <int TM, int KC, int STAGES, int MINB, bool FROM_X>
+template <int TM, int KC, int STAGES, int MINB, bool FROM_X, bool CL = false>
 cudaError_t launch_tm(const F32Params &p, int N, cudaStream_t st) {
     dim3 grid((unsigned)(p.pos_tiles * N), (unsigned)((p.C_o + TM - 1) / TM));
     constexpr size_t smem = f32_smem_bytes<TM, KC, STAGES>();
-    cudaError_t e = cudaFuncSetAttribute(conv_f32_kernel<TM, KC, STAGES, MINB, FROM_X>,
+    cudaError_t e = cudaFuncSetAttribute(conv_f32_kernel<TM, KC, STAGES, MINB, FROM_X, CL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    conv_f32_kernel<TM, KC, STAGES, MINB, FROM_X><<<grid, TM * 2, smem, st>>>(p);
+    conv_f32_kernel<TM, KC, STAGES, MINB, FROM_X, CL><<<grid, TM * 2, smem, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -368,7 +367,6 @@ cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *
     p.S = (int)(s.s_w * s.H_f);
     p.img_src = from_x ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * s.W_i * s.H_f;
     p.cs = (int)(s.H_o * s.W_i * s.H_f);
-    p.nhwc = cl ? 1 : 0;
     p.C_o_pad = (int)Cp;
     p.div_KK = make_fastdiv((uint32_t)(s.H_f * s.W_f));
     p.div_Wo = make_fastdiv((uint32_t)s.W_o);
@@ -386,11 +384,16 @@ cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *
             p.S = (int)(s.s_w * s.H_f * s.C_i);
             p.cs = (int)(s.H_o * p.L);           // one channel
         }
-        from_x = false;
     }
 
     const int best = choose_tm(s);
     const int N = (int)s.N;
+    if (cl) {  // the window path with the channels-last epilogue
+        if (best == 128) return launch_tm<F32_CFG_128, false, true>(p, N, st);
+        if (best == 96) return launch_tm<F32_CFG_96, false, true>(p, N, st);
+        if (best == 64) return launch_tm<F32_CFG_64, false, true>(p, N, st);
+        return launch_tm<F32_CFG_32, false, true>(p, N, st);
+    }
     if (from_x) {
         if (best == 128) return launch_tm<F32_CFG_128, true>(p, N, st);
         if (best == 96) return launch_tm<F32_CFG_96, true>(p, N, st);

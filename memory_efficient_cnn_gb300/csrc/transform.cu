@@ -290,9 +290,16 @@ cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, 
 // win[n][ho][w*H_f + r][c] = x[n][ho*s_h + r][w][c]: the window row of (n, ho)
 // is W_i*H_f runs of C_i contiguous elements, run (w, r) being the C_i
 // channels of input position (ho*s_h + r, w). The output is written as whole
-// 16-byte vectors in order (coalesced stores); a grid-stride loop keeps four
-// vectors in flight per thread, and consecutive output rows, which share input
-// rows, are written at about the same time, so the rows are re-read from L2.
+// 16-byte vectors in order (coalesced stores).
+//  * C_i*esz a multiple of 16: every run is whole 16-byte vectors, copied one
+//    to one by a grid-stride loop that keeps four in flight per thread;
+//    consecutive output rows, which share input rows, are written at about the
+//    same time, so shared rows are re-read from L2.
+//  * otherwise, a CTA owns a band of output rows of one image: the input rows
+//    under it are one contiguous range of x (rows of W_i*C_i elements), staged
+//    once into shared memory with 16-byte loads; each thread builds 16-byte
+//    output vectors from it, stepping (c, r, w, row) element by element, and
+//    the band's unaligned head and tail are written element by element.
 namespace {
 
 struct TNParams {
@@ -304,6 +311,8 @@ struct TNParams {
     int C_i, H_i, W_i, H_f, s_h, H_o;
     int VPR;              // vectors per run (vector path: C_i*esz / 16)
     FastDiv div_vpr, div_wh, div_hf, div_ho;
+    int T, tiles;         // staged path: output rows per band, bands per image
+    int64_t x_elems;      // staged path: elements of x
 };
 
 // C_i*esz a multiple of 16: every run is whole, aligned 16-byte vectors.
@@ -383,6 +392,96 @@ __global__ void __launch_bounds__(256) transform_nhwc_elem(TNParams p) {
     }
 }
 
+template <typename E>
+__global__ void __launch_bounds__(256) transform_nhwc_staged(TNParams p) {
+    extern __shared__ __align__(16) unsigned char smem_nhwc[];
+    constexpr int V = 16 / sizeof(E);
+    E *s_in = reinterpret_cast<E *>(smem_nhwc);
+    const E *__restrict__ x = static_cast<const E *>(p.x);
+    E *__restrict__ win = static_cast<E *>(p.win);
+    const int n = blockIdx.x / p.tiles;
+    const int tile = blockIdx.x - n * p.tiles;
+    const int ho0 = tile * p.T;
+    const int rows_out = min(p.T, p.H_o - ho0);
+    const int rows_in = (rows_out - 1) * p.s_h + p.H_f;
+    const int C = p.C_i, H_f = p.H_f, W_i = p.W_i;
+    const int RL = W_i * C;  // elements of an input row
+
+    // ---- stage x[in0, in0 + cnt) at s_in[lead, lead + cnt)
+    const int64_t in0 = ((int64_t)n * p.H_i + (int64_t)ho0 * p.s_h) * RL;
+    const int cnt = rows_in * RL;
+    const int64_t base = in0 - (in0 % V);
+    const int lead = (int)(in0 - base);
+    const int nvec = (lead + cnt + V - 1) / V;
+    const int64_t inside = (p.x_elems - base) / V;  // vectors wholly inside x
+    const int nfull = inside < (int64_t)nvec ? (int)inside : nvec;
+    const uint4 *gx = reinterpret_cast<const uint4 *>(x + base);
+    uint4 *sx = reinterpret_cast<uint4 *>(s_in);
+    int v = threadIdx.x;
+    for (; v + 3 * 256 < nfull; v += 4 * 256) {
+        const uint4 r0 = __ldg(gx + v), r1 = __ldg(gx + v + 256);
+        const uint4 r2 = __ldg(gx + v + 512), r3 = __ldg(gx + v + 768);
+        sx[v] = r0;
+        sx[v + 256] = r1;
+        sx[v + 512] = r2;
+        sx[v + 768] = r3;
+    }
+    for (; v < nfull; v += 256) sx[v] = __ldg(gx + v);
+    for (int e = nfull * V + (int)threadIdx.x; e < nvec * V; e += 256)
+        if (base + e < p.x_elems) s_in[e] = x[base + e];
+    __syncthreads();
+
+    // staged index of band element g (g = t*Lp + (w*H_f + r)*C + c)
+    const int Lp = (int)p.Lp;
+    auto staged = [&](int g) -> int {
+        const int t = g / Lp, o = g - t * Lp;
+        const int pos = o / C, c = o - pos * C;
+        const int w = pos / H_f, r = pos - w * H_f;
+        return (t * p.s_h + r) * RL + w * C + c + lead;
+    };
+    const int64_t f0 = ((int64_t)n * p.H_o + ho0) * Lp;
+    const int64_t f1 = f0 + (int64_t)rows_out * Lp;
+    const int64_t head = min(f1, (f0 + V - 1) / V * V);  // first aligned element
+    const int64_t vend = max(head, f1 / V * V);           // end of the whole vectors
+    for (int64_t e = f0 + threadIdx.x; e < head; e += 256) win[e] = s_in[staged((int)(e - f0))];
+    for (int64_t e = vend + threadIdx.x; e < f1; e += 256) win[e] = s_in[staged((int)(e - f0))];
+    for (int64_t vv = head / V + threadIdx.x; vv < vend / V; vv += 256) {
+        const int g = (int)(vv * V - f0);
+        int t = g / Lp;
+        const int o = g - t * Lp;
+        const int pos = o / C;
+        int c = o - pos * C;
+        int w = pos / H_f, r = pos - w * H_f;
+        int src = (t * p.s_h + r) * RL + w * C + c + lead;
+        union {
+            uint4 u;
+            E e[V];
+        } out;
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            out.e[e] = s_in[src];
+            if (++c == C) {  // next row offset r of column w
+                c = 0;
+                src += RL - C + 1;
+                if (++r == H_f) {  // next column w, back to the first row
+                    r = 0;
+                    src += C - H_f * RL;
+                    if (++w == W_i) {  // next output row of the band
+                        w = 0;
+                        src += (p.s_h - 1) * RL;
+                        ++t;
+                    }
+                }
+            } else {
+                ++src;
+            }
+        }
+        *reinterpret_cast<uint4 *>(win + vv * V) = out.u;
+    }
+}
+
+constexpr int kNhwcStageBudget = 48 * 1024;  // staged input rows per CTA
+
 }  // namespace
 
 cudaError_t launch_transform_nhwc(const void *x, void *win, const Shape &s, int esz, cudaStream_t st) {
@@ -400,11 +499,37 @@ cudaError_t launch_transform_nhwc(const void *x, void *win, const Shape &s, int 
     p.H_o = (int)s.H_o;
     const bool vec = (s.C_i * esz) % 16 == 0;
     p.VPR = vec ? (int)(s.C_i * esz / 16) : 1;
+    p.x_elems = s.N * s.H_i * s.W_i * s.C_i;
+    // staged path: as many output rows per band as the budget holds, balanced
+    const int64_t RLb = s.W_i * s.C_i * esz;  // bytes of an input row
+    int64_t T = 0;
+    while (T < s.H_o && (T * s.s_h + s.H_f) * RLb + 16 <= kNhwcStageBudget) ++T;
+    const bool staged = !vec && T >= 1;
+    if (staged) {
+        const int64_t tiles = (s.H_o + T - 1) / T;
+        T = (s.H_o + tiles - 1) / tiles;
+        p.T = (int)T;
+        p.tiles = (int)tiles;
+    }
     p.div_vpr = make_fastdiv((uint32_t)p.VPR);
     p.div_wh = make_fastdiv((uint32_t)(s.W_i * s.H_f));
     p.div_hf = make_fastdiv((uint32_t)s.H_f);
     p.div_ho = make_fastdiv((uint32_t)s.H_o);
     if (p.vecs == 0) return cudaSuccess;
+    if (staged) {
+        const size_t smem = (size_t)(((T - 1) * s.s_h + s.H_f) * RLb + 16 + 15) / 16 * 16;
+        const unsigned blocks = (unsigned)(s.N * p.tiles);
+        if (esz == 2) {
+            cudaFuncSetAttribute(transform_nhwc_staged<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+            transform_nhwc_staged<uint16_t><<<blocks, 256, smem, st>>>(p);
+        } else {
+            cudaFuncSetAttribute(transform_nhwc_staged<uint32_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+            transform_nhwc_staged<uint32_t><<<blocks, 256, smem, st>>>(p);
+        }
+        return cudaGetLastError();
+    }
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t per_pass = vec ? 4 : 1;  // vectors per thread and grid pass

@@ -46,6 +46,8 @@ def _check_full(out, x_cl, w, stride, what):
 T_CASES = [  # N, C_i, H_i, W_i, H_f, s_h
     (2, 3, 32, 32, 3, 1), (3, 5, 37, 45, 11, 4), (2, 8, 20, 21, 3, 2), (1, 64, 17, 19, 7, 2),
     (2, 12, 9, 13, 9, 1), (1, 1, 40, 5, 1, 1), (2, 4, 50, 17, 3, 5), (1, 96, 24, 24, 5, 1),
+    # input rows too long to stage a band in shared memory: element-wise path
+    (1, 3, 12, 12000, 3, 2),
 ]
 
 
@@ -64,7 +66,7 @@ def test_transform_nhwc_small_bit_exact(case, dt):
 
 
 def test_transform_nhwc_does_not_write_past_the_window():
-    x = torch.randn(2, 31, 45, 3, dtype=torch.float16)  # 3 channels: element path, partial last vector
+    x = torch.randn(2, 31, 45, 3, dtype=torch.float16)  # 3 channels: staged bands, unaligned band ends
     H_f, s_h = 11, 4
     H_o = (31 - H_f) // s_h + 1
     n = 2 * H_o * 45 * H_f * 3
@@ -75,7 +77,7 @@ def test_transform_nhwc_does_not_write_past_the_window():
     assert _raw(buf[:n]).tobytes() == oracle.im2win_nhwc(_raw(x), H_f, s_h).tobytes()
 
 
-@pytest.mark.parametrize("layer,dt", [(wl.CV1, "f16"), (wl.CV5, "bf16"), (wl.SWEEP[1], "bf16")],
+@pytest.mark.parametrize("layer,dt", [(wl.CV1, "f16"), (wl.CV1, "f32"), (wl.CV5, "bf16"), (wl.SWEEP[1], "bf16")],
                          ids=lambda v: getattr(v, "name", v))
 def test_transform_nhwc_full_size_bit_exact(layer, dt):
     x, _ = wl.make_inputs(layer, dt)
