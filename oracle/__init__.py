@@ -19,6 +19,10 @@ Each wrapper names the passage of the method it follows:
   tensor layouts by title only, and this is the plainest reading of it.
 * ``conv_direct_nhwc`` / ``conv_points_nhwc`` -- the direct sums above on
   channels-last tensors: a transpose to NCHW, the NCHW routine, a transpose back.
+* ``conv_direct_pd`` / ``conv_points_pd`` / ``im2win_pd`` / ``conv_im2win_pd``
+  -- zero padding (p_h, p_w) and dilation (d_h, d_w), in either layout: the
+  usual definitions of the two options (the pages' layers use neither), with
+  the window row running over the W_i + 2 p_w padded columns.
 
 Inputs are numpy arrays; floating inputs are widened to float64 exactly before
 the call (the caller has already rounded them to the dtype under test).
@@ -72,9 +76,15 @@ def _load():
             lib.oracle_im2win.argtypes = [ctypes.c_void_p, ctypes.c_void_p] + [_I64] * 6
             lib.oracle_im2win_nhwc.argtypes = [ctypes.c_void_p, ctypes.c_void_p] + [_I64] * 6
             lib.oracle_conv_im2win_nhwc.argtypes = [_PD, _PD, _PD] + shp
+            ci = ctypes.c_int
+            lib.oracle_conv_direct_pd.argtypes = [_PD, _PD, _PD, _PD, ci] + shp + [_I64] * 4
+            lib.oracle_conv_points_pd.argtypes = [_PD, _PD, _PI, _I64, _PD, _PD, ci] + shp + [_I64] * 4
+            lib.oracle_im2win_pd.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _I64, ci] + [_I64] * 12
+            lib.oracle_conv_im2win_pd.argtypes = [_PD, _PD, _PD, ci] + shp + [_I64] * 4
             for f in (lib.oracle_conv_direct, lib.oracle_conv_points, lib.oracle_conv_im2win,
                       lib.oracle_conv_im2col, lib.oracle_im2win, lib.oracle_im2win_nhwc,
-                      lib.oracle_conv_im2win_nhwc):
+                      lib.oracle_conv_im2win_nhwc, lib.oracle_conv_direct_pd, lib.oracle_conv_points_pd,
+                      lib.oracle_im2win_pd, lib.oracle_conv_im2win_pd):
                 f.restype = ctypes.c_int
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -228,4 +238,87 @@ def conv_im2win_nhwc(x, w, stride=(1, 1)):
                                          stride[0], stride[1])
     if rc:
         raise ValueError("oracle_conv_im2win_nhwc: bad shape")
+    return out
+
+
+# ---- zero padding and dilation (either layout)
+
+def _dims(x_shape, layout):
+    if layout == "nhwc":
+        n, hi, wi, ci = x_shape
+    else:
+        n, ci, hi, wi = x_shape
+    return n, ci, hi, wi
+
+
+def out_shape_pd(x_shape, w_shape, stride, pad, dil, layout="nchw"):
+    n, ci, hi, wi = _dims(x_shape, layout)
+    co, ci2, hf, wf = w_shape
+    if ci != ci2:
+        raise ValueError("channel mismatch")
+    ho = (hi + 2 * pad[0] - dil[0] * (hf - 1) - 1) // stride[0] + 1
+    wo = (wi + 2 * pad[1] - dil[1] * (wf - 1) - 1) // stride[1] + 1
+    return (n, ho, wo, co) if layout == "nhwc" else (n, co, ho, wo)
+
+
+def _pd_args(x, w, stride, pad, dil, layout):
+    n, ci, hi, wi = _dims(x.shape, layout)
+    co, _, hf, wf = w.shape
+    return [n, ci, hi, wi, co, hf, wf, stride[0], stride[1], pad[0], pad[1], dil[0], dil[1]]
+
+
+def conv_direct_pd(x, w, stride=(1, 1), pad=(0, 0), dil=(1, 1), layout="nchw"):
+    """Padded, dilated direct convolution in fp64; returns (out, S) in the layout of x."""
+    x, w = _f64(x), _f64(w)
+    shp = out_shape_pd(x.shape, w.shape, stride, pad, dil, layout)
+    out = np.empty(shp, np.float64)
+    scale = np.empty(shp, np.float64)
+    rc = _load().oracle_conv_direct_pd(_dp(x), _dp(w), _dp(out), _dp(scale), int(layout == "nhwc"),
+                                       *_pd_args(x, w, stride, pad, dil, layout))
+    if rc:
+        raise ValueError("oracle_conv_direct_pd: bad shape")
+    return out, scale
+
+
+def conv_points_pd(x, w, idx, stride=(1, 1), pad=(0, 0), dil=(1, 1), layout="nchw"):
+    """The padded, dilated direct sum at idx[t] = (n, co, ho, wo) (NCHW output coordinates)."""
+    x, w = _f64(x), _f64(w)
+    idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64).reshape(-1, 4))
+    out = np.empty(len(idx), np.float64)
+    scale = np.empty(len(idx), np.float64)
+    rc = _load().oracle_conv_points_pd(_dp(x), _dp(w), idx.ctypes.data_as(_PI), len(idx), _dp(out),
+                                       _dp(scale), int(layout == "nhwc"),
+                                       *_pd_args(x, w, stride, pad, dil, layout))
+    if rc:
+        raise ValueError("oracle_conv_points_pd: bad shape or index")
+    return out, scale
+
+
+def im2win_pd(x, w_shape, stride=(1, 1), pad=(0, 0), dil=(1, 1), layout="nchw"):
+    """Window tensor of the padded input with row dilation, same dtype, byte copy:
+    NCHW win[n][ci][ho][w*H_f + r], NHWC win[n][ho][w*H_f + r][ci], w < W_i + 2 p_w."""
+    x = np.ascontiguousarray(x)
+    n, ci, hi, wi = _dims(x.shape, layout)
+    _, _, hf, wf = w_shape
+    ho = (hi + 2 * pad[0] - dil[0] * (hf - 1) - 1) // stride[0] + 1
+    wp = wi + 2 * pad[1]
+    shp = (n, ho, wp * hf, ci) if layout == "nhwc" else (n, ci, ho, wp * hf)
+    win = np.empty(shp, dtype=x.dtype)
+    rc = _load().oracle_im2win_pd(x.ctypes.data, win.ctypes.data, x.dtype.itemsize, int(layout == "nhwc"),
+                                  n, ci, hi, wi, hf, wf, stride[0], stride[1], pad[0], pad[1],
+                                  dil[0], dil[1])
+    if rc:
+        raise ValueError("oracle_im2win_pd: bad shape")
+    return win
+
+
+def conv_im2win_pd(x, w, stride=(1, 1), pad=(0, 0), dil=(1, 1), layout="nchw"):
+    """Convolution through the fp64 padded window tensor (column runs at dilation d_w)."""
+    x, w = _f64(x), _f64(w)
+    win = im2win_pd(x, w.shape, stride, pad, dil, layout)
+    out = np.empty(out_shape_pd(x.shape, w.shape, stride, pad, dil, layout), np.float64)
+    rc = _load().oracle_conv_im2win_pd(_dp(win), _dp(w), _dp(out), int(layout == "nhwc"),
+                                       *_pd_args(x, w, stride, pad, dil, layout))
+    if rc:
+        raise ValueError("oracle_conv_im2win_pd: bad shape")
     return out

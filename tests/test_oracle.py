@@ -265,3 +265,110 @@ def test_nhwc_one_hot_filter_is_strided_crop():
     crop = x[:, 2:2 + (ho - 1) * sh + 1:sh, 3:3 + (wo - 1) * sw + 1:sw, 4]
     np.testing.assert_array_equal(out[..., 3], crop)
     assert not out[..., [0, 1, 2, 4]].any()
+
+
+# ---- zero padding and dilation (the pages' layers use neither; these pin the
+# usual definitions against independent formulations)
+
+def _random_pd_case(rng):
+    hf, wf = (int(v) for v in rng.integers(1, 4, size=2))
+    sh, sw = (int(v) for v in rng.integers(1, 3, size=2))
+    ph, pw = (int(v) for v in rng.integers(0, 3, size=2))
+    dh, dw = (int(v) for v in rng.integers(1, 3, size=2))
+    hi = int(rng.integers(max(1, dh * (hf - 1) + 1 - 2 * ph), 9))
+    wi = int(rng.integers(max(1, dw * (wf - 1) + 1 - 2 * pw), 9))
+    ci = int(rng.choice([1, 2, 3, 5]))
+    co = int(rng.choice([1, 4]))
+    n = int(rng.choice([1, 2]))
+    return (n, ci, hi, wi, co, hf, wf), (sh, sw), (ph, pw), (dh, dw)
+
+
+def _dilate(w, dh, dw):
+    co, ci, hf, wf = w.shape
+    out = np.zeros((co, ci, dh * (hf - 1) + 1, dw * (wf - 1) + 1), dtype=w.dtype)
+    out[:, :, ::dh, ::dw] = w
+    return out
+
+
+def test_pd_matches_torch_conv2d_fp64():
+    rng = np.random.default_rng(40)
+    for _ in range(80):
+        (n, ci, hi, wi, co, hf, wf), st, pd, dl = _random_pd_case(rng)
+        x = rng.uniform(-1, 1, size=(n, ci, hi, wi))
+        w = rng.standard_normal((co, ci, hf, wf))
+        d, s = oracle.conv_direct_pd(x, w, st, pd, dl)
+        t = torch.nn.functional.conv2d(torch.from_numpy(x), torch.from_numpy(w), stride=st,
+                                       padding=pd, dilation=dl).numpy()
+        assert d.shape == t.shape
+        assert np.all(np.abs(d - t) <= 1e-12 * s + 1e-300)
+
+
+def test_pd_is_explicit_padding_and_dilated_filter_exactly():
+    """Padding = np.pad of x; dilation = the filter with zeros inserted; both through
+    the unpadded direct routine, bit for bit on integers."""
+    rng = np.random.default_rng(41)
+    for _ in range(150):
+        (n, ci, hi, wi, co, hf, wf), st, pd, dl = _random_pd_case(rng)
+        x = rng.integers(-3, 4, size=(n, ci, hi, wi)).astype(np.float64)
+        w = rng.integers(-3, 4, size=(co, ci, hf, wf)).astype(np.float64)
+        d, _ = oracle.conv_direct_pd(x, w, st, pd, dl)
+        xp = np.pad(x, ((0, 0), (0, 0), (pd[0], pd[0]), (pd[1], pd[1])))
+        want, _ = oracle.conv_direct(xp, _dilate(w, *dl), st)
+        np.testing.assert_array_equal(d, want)
+
+
+def test_pd_reduces_to_the_unpadded_routines():
+    rng = np.random.default_rng(42)
+    x = rng.integers(-9, 10, size=(2, 3, 11, 13)).astype(np.float64)
+    w = rng.integers(-3, 4, size=(4, 3, 3, 2)).astype(np.float64)
+    d, s = oracle.conv_direct_pd(x, w, (2, 1))
+    d0, s0 = oracle.conv_direct(x, w, (2, 1))
+    np.testing.assert_array_equal(d, d0)
+    np.testing.assert_array_equal(s, s0)
+    xi = x.astype(np.int16)
+    assert oracle.im2win_pd(xi, w.shape, (2, 1)).tobytes() == oracle.im2win(xi, 3, 2).tobytes()
+    xc = np.ascontiguousarray(np.transpose(xi, (0, 2, 3, 1)))
+    assert (oracle.im2win_pd(xc, w.shape, (2, 1), layout="nhwc").tobytes()
+            == oracle.im2win_nhwc(xc, 3, 2).tobytes())
+
+
+def test_pd_window_rows_of_a_hand_example():
+    """x[0][0] = 3h + w (3x3), H_f = 2, padding 1: the first window row covers the
+    zero row above x and x's row 0, column by column over 5 padded columns:
+    (0,0) (0,0) (0,1) (0,2) (0,0); the second covers rows 0 and 1 of x."""
+    x = (3 * np.arange(3)[:, None] + np.arange(3)[None, :]).astype(np.float64)[None, None]
+    win = oracle.im2win_pd(x, (1, 1, 2, 2), (1, 1), (1, 1))
+    assert win.shape == (1, 1, 4, 10)
+    np.testing.assert_array_equal(win[0, 0, 0], [0, 0, 0, 0, 0, 1, 0, 2, 0, 0])
+    np.testing.assert_array_equal(win[0, 0, 1], [0, 0, 0, 3, 1, 4, 2, 5, 0, 0])
+    # dilation 2 along H: rows r*2 under ho: ho = 0 pairs the zero row with x row 1
+    wind = oracle.im2win_pd(x, (1, 1, 2, 2), (1, 1), (1, 1), (2, 1))
+    assert wind.shape == (1, 1, 3, 10)
+    np.testing.assert_array_equal(wind[0, 0, 0], [0, 0, 0, 3, 0, 4, 0, 5, 0, 0])
+
+
+@pytest.mark.parametrize("layout", ["nchw", "nhwc"])
+def test_pd_window_formulation_agrees_exactly_on_integers(layout):
+    rng = np.random.default_rng(43)
+    for _ in range(150):
+        (n, ci, hi, wi, co, hf, wf), st, pd, dl = _random_pd_case(rng)
+        shape = (n, hi, wi, ci) if layout == "nhwc" else (n, ci, hi, wi)
+        x = rng.integers(-3, 4, size=shape).astype(np.float64)
+        w = rng.integers(-3, 4, size=(co, ci, hf, wf)).astype(np.float64)
+        d, _ = oracle.conv_direct_pd(x, w, st, pd, dl, layout)
+        np.testing.assert_array_equal(oracle.conv_im2win_pd(x, w, st, pd, dl, layout), d)
+        if layout == "nhwc":
+            ref, _ = oracle.conv_direct_pd(np.transpose(x, (0, 3, 1, 2)), w, st, pd, dl)
+            np.testing.assert_array_equal(d, np.transpose(ref, (0, 2, 3, 1)))
+        nchw = d if layout == "nchw" else np.transpose(d, (0, 3, 1, 2))
+        idx = np.stack([rng.integers(0, s, 6) for s in nchw.shape], axis=1)
+        v, _ = oracle.conv_points_pd(x, w, idx, st, pd, dl, layout)
+        np.testing.assert_array_equal(v, nchw[tuple(idx.T)])
+
+
+def test_pd_bad_shapes_are_rejected():
+    x = np.zeros((1, 2, 4, 4))
+    with pytest.raises(ValueError):   # dilated extent 7 > 4 + 2
+        oracle.conv_direct_pd(x, np.zeros((1, 2, 3, 3)), (1, 1), (1, 1), (3, 3))
+    with pytest.raises(ValueError):
+        oracle.conv_direct_pd(x, np.zeros((1, 2, 3, 3)), (1, 1), (-1, 0))
