@@ -148,14 +148,14 @@ def job_tflops(world: int, flops_per_rank_step: float, ms_per_step: float) -> fl
 
 
 def conv_flops(layer) -> float:
-    ho = (layer.H_i - layer.H_f) // layer.s_h + 1
-    wo = (layer.W_i - layer.W_f) // layer.s_w + 1
+    ho, wo = layer.out_hw
     return 2.0 * layer.N * layer.C_o * ho * wo * layer.C_i * layer.H_f * layer.W_f
 
 
 def workload_str(layer) -> str:
+    pd = "" if layer.plain else f", padding {layer.pad[0]}x{layer.pad[1]}, dilation {layer.dil[0]}x{layer.dil[1]}"
     return (f"{layer.name}: N={layer.N}, C_i={layer.C_i}, {layer.H_i}x{layer.W_i}, C_o={layer.C_o}, "
-            f"{layer.H_f}x{layer.W_f}, stride {layer.s_h}x{layer.s_w}; {' and '.join(layer.dtypes)}")
+            f"{layer.H_f}x{layer.W_f}, stride {layer.s_h}x{layer.s_w}{pd}; {' and '.join(layer.dtypes)}")
 
 
 class OracleSampler:
@@ -184,8 +184,13 @@ class OracleSampler:
             n = (self.i // len(self.inputs)) % x.shape[0]
             xd = np.ascontiguousarray(x[n:n + 1])
             t0 = time.perf_counter()
-            self.oracle.im2win(xd, L.H_f, L.s_h)
-            self.oracle.conv_direct(xd, w, (L.s_h, L.s_w))
+            if L.plain:
+                self.oracle.im2win(xd, L.H_f, L.s_h)
+                self.oracle.conv_direct(xd, w, (L.s_h, L.s_w))
+            else:
+                st = (L.s_h, L.s_w)
+                self.oracle.im2win_pd(xd, w.shape, st, L.pad, L.dil)
+                self.oracle.conv_direct_pd(xd, w, st, L.pad, L.dil)
             t_total += time.perf_counter() - t0
             done += 1
             self.i += 1
@@ -242,7 +247,7 @@ def main():
 
     from memory_efficient_cnn_gb300 import workloads as wl
 
-    layers = {l.name: l for l in wl.ALL}
+    layers = {l.name: l for l in wl.ALL + wl.PADDED}
     if args.layer not in layers:
         ap.error(f"--layer must be one of {sorted(layers)}")
     layer = layers[args.layer]
@@ -277,7 +282,9 @@ def main():
     stride = (layer.s_h, layer.s_w)
     shp = layer.shape_args
     N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w = shp
-    H_o, W_o = mec.out_hw(H_i, W_i, H_f, W_f, *stride)
+    H_o, W_o = layer.out_hw
+    W_p = W_i + 2 * layer.pad[1]  # window row: W_p*H_f elements
+    pdargs = (*shp, layer.pad[0], layer.pad[1], layer.dil[0], layer.dil[1])
 
     # one step: per dtype, the transform, the conv from the window tensor and
     # (fp16/bf16) the fused conv; fp32 runs on the CUDA cores
@@ -302,29 +309,46 @@ def main():
         dev_in += [x, w]
         nchw = (N, C_i, H_i, W_i)
         if cl:
-            win = torch.empty((N, H_o, W_i * H_f, C_i), dtype=tdt, device=dev)
+            win = torch.empty((N, H_o, W_p * H_f, C_i), dtype=tdt, device=dev)
             out_w = torch.empty((N, H_o, W_o, C_o), dtype=tdt, device=dev)
-            tr, cv, cvf = mec.im2win_transform_nhwc, mec.im2win_conv_nhwc, mec.im2win_conv_fused_nhwc
-            op_w, op_f = mec.OP_CONV_NHWC, mec.OP_CONV_FUSED_NHWC
         else:
-            win = torch.empty((N, C_i, H_o, W_i * H_f), dtype=tdt, device=dev)
+            win = torch.empty((N, C_i, H_o, W_p * H_f), dtype=tdt, device=dev)
             out_w = torch.empty((N, C_o, H_o, W_o), dtype=tdt, device=dev)
-            tr, cv, cvf = mec.im2win_transform, mec.im2win_conv, mec.im2win_conv_fused
-            op_w, op_f = mec.OP_CONV, mec.OP_CONV_FUSED
-        ws = mec.workspace(op_w, nchw, w.shape, stride, tdt, dev)
+        if not layer.plain:
+            # padding / dilation: the *_ex calls, layout as an argument
+            lo = mec.NHWC if cl else mec.NCHW
+            dc = mec._binding._DTYPE[tdt]
+            ws = torch.empty(mec.im2win_workspace_size_ex(mec.OP_CONV, *pdargs, lo, dc), dtype=torch.uint8,
+                             device=dev)
+            wsf = torch.empty(mec.im2win_workspace_size_ex(mec.OP_CONV_FUSED, *pdargs, lo, dc),
+                              dtype=torch.uint8, device=dev)
+            tr = lambda x, win: mec.im2win_transform_ex(x, win, *pdargs, lo)
+            cv = lambda win, w, o, ws: mec.im2win_conv_ex(win, w, o, ws, *pdargs, lo)
+            cvf = lambda x, w, o, ws: mec.im2win_conv_fused_ex(x, w, o, ws, *pdargs, lo)
+        else:
+            if cl:
+                tr0, cv0, cvf0 = mec.im2win_transform_nhwc, mec.im2win_conv_nhwc, mec.im2win_conv_fused_nhwc
+                op_w, op_f = mec.OP_CONV_NHWC, mec.OP_CONV_FUSED_NHWC
+            else:
+                tr0, cv0, cvf0 = mec.im2win_transform, mec.im2win_conv, mec.im2win_conv_fused
+                op_w, op_f = mec.OP_CONV, mec.OP_CONV_FUSED
+            ws = mec.workspace(op_w, nchw, w.shape, stride, tdt, dev)
+            wsf = mec.workspace(op_f, nchw, w.shape, stride, tdt, dev)
+            tr = lambda x, win, tr0=tr0: tr0(x, win, C_o, H_f, W_f, s_h, s_w)
+            cv = lambda win, w, o, ws, cv0=cv0: cv0(win, w, o, ws, *shp)
+            cvf = lambda x, w, o, ws, cvf0=cvf0: cvf0(x, w, o, ws, s_h, s_w)
         ops.append((f"transform_{d}{sfx}", d, "transform",
-                    lambda x=x, win=win: tr(x, win, C_o, H_f, W_f, s_h, s_w),
+                    lambda x=x, win=win, tr=tr: tr(x, win),
                     {"win_bytes": win.numel() * win.element_size()}))
         kind = "conv_f32" if d == "f32" else "conv_tc"
         ops.append((f"{kind}_window_{d}{sfx}", d, "window",
-                    lambda win=win, w=w, o=out_w, ws=ws: cv(win, w, o, ws, *shp),
+                    lambda win=win, w=w, o=out_w, ws=ws, cv=cv: cv(win, w, o, ws),
                     {"ws_bytes": ws.numel()}))
         outs.append(out_w)
         if d != "f32":
             out_f = torch.empty_like(out_w)
-            wsf = mec.workspace(op_f, nchw, w.shape, stride, tdt, dev)
             ops.append((f"conv_tc_fused_{d}{sfx}", d, "fused",
-                        lambda x=x, w=w, o=out_f, ws=wsf: cvf(x, w, o, ws, s_h, s_w),
+                        lambda x=x, w=w, o=out_f, ws=wsf, cvf=cvf: cvf(x, w, o, ws),
                         {"ws_bytes": wsf.numel()}))
             outs.append(out_f)
 
@@ -431,7 +455,7 @@ def main():
     fp32_peak = SMS * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12  # FFMA lanes x 2 flop x clock
     esz = {"f16": 2, "bf16": 2, "f32": 4}
     x_b = {d: N * C_i * H_i * W_i * esz[d] for d in esz}
-    win_b = {d: N * C_i * H_o * W_i * H_f * esz[d] for d in esz}
+    win_b = {d: N * C_i * H_o * W_p * H_f * esz[d] for d in esz}
     out_b = {d: N * C_o * H_o * W_o * esz[d] for d in esz}
     w_b = {d: C_o * C_i * H_f * W_f * esz[d] for d in esz}
     col_b = {d: N * C_i * H_f * W_f * H_o * W_o * esz[d] for d in esz}

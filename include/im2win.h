@@ -174,6 +174,56 @@ im2win_status im2win_conv_fused_nhwc(const void *x, const void *filt, void *out,
                                      int64_t W_i, int64_t C_o, int64_t H_f, int64_t W_f,
                                      int64_t s_h, int64_t s_w, int dtype, void *stream);
 
+/*
+ * Zero padding, dilation and the layout as arguments
+ * --------------------------------------------------
+ * The pages' layers are valid convolutions; these calls add the two usual CNN
+ * options (neither is on the pages, so this is the usual definition):
+ *   out[n][co][ho][wo] = sum_ci sum_r sum_j xpad[n][ci][ho*s_h + r*d_h][wo*s_w + j*d_w] * filt[co][ci][r][j],
+ * where xpad is x with p_h zero rows above and below and p_w zero columns on
+ * each side, and
+ *   H_o = (H_i + 2 p_h - d_h (H_f - 1) - 1) / s_h + 1,  W_o likewise (floor).
+ * Requirements: p_h, p_w >= 0; d_h, d_w >= 1; d_h (H_f - 1) + 1 <= H_i + 2 p_h and
+ * d_w (W_f - 1) + 1 <= W_i + 2 p_w (else IM2WIN_ERR_INVALID_ARG).
+ * The window tensor runs over the W_p = W_i + 2 p_w padded columns and holds the
+ * dilated rows:
+ *   NCHW: win[n][ci][ho][w*H_f + r] = xpad[n][ci][ho*s_h + r*d_h][w],
+ *   NHWC: win[n][ho][w*H_f + r][ci] = xpad[n][ci][ho*s_h + r*d_h][w],   w < W_p,
+ * N*C_i*H_o*W_p*H_f elements; the convolution from it sums, per filter column j,
+ * the run of H_f window elements starting at (wo*s_w + j*d_w)*H_f.
+ * `layout` is an im2win_layout and applies to x, win and out (the filter is
+ * always filt[C_o][C_i][H_f][W_f]). With p = 0 and d = 1 each call equals its
+ * counterpart above. Other arguments, dtypes and errors as above; a workspace
+ * comes from im2win_workspace_size_ex with the same padding, dilation and
+ * layout (op IM2WIN_OP_TRANSFORM, IM2WIN_OP_CONV or IM2WIN_OP_CONV_FUSED).
+ * F16/BF16 convolutions with padding or dilation run the channel-group tensor-core
+ * kernel only and return IM2WIN_ERR_UNSUPPORTED where it has no tiling.
+ */
+typedef enum {
+    IM2WIN_LAYOUT_NCHW = 0,
+    IM2WIN_LAYOUT_NHWC = 1
+} im2win_layout;
+
+im2win_status im2win_workspace_size_ex(int op, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i,
+                                       int64_t C_o, int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w,
+                                       int64_t p_h, int64_t p_w, int64_t d_h, int64_t d_w, int layout,
+                                       int dtype, size_t *bytes);
+
+im2win_status im2win_transform_ex(const void *x, void *win, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i,
+                                  int64_t C_o, int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w,
+                                  int64_t p_h, int64_t p_w, int64_t d_h, int64_t d_w, int layout, int dtype,
+                                  void *stream);
+
+im2win_status im2win_conv_ex(const void *win, const void *filt, void *out, void *ws, size_t ws_bytes,
+                             int64_t N, int64_t C_i, int64_t H_i, int64_t W_i, int64_t C_o, int64_t H_f,
+                             int64_t W_f, int64_t s_h, int64_t s_w, int64_t p_h, int64_t p_w, int64_t d_h,
+                             int64_t d_w, int layout, int dtype, void *stream);
+
+im2win_status im2win_conv_fused_ex(const void *x, const void *filt, void *out, void *ws, size_t ws_bytes,
+                                   int64_t N, int64_t C_i, int64_t H_i, int64_t W_i, int64_t C_o, int64_t H_f,
+                                   int64_t W_f, int64_t s_h, int64_t s_w, int64_t p_h, int64_t p_w, int64_t d_h,
+                                   int64_t d_w, int layout, int dtype, void *stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *im2win_status_string(int status);
 

@@ -14,4 +14,6 @@ from ._binding import (  # noqa: F401
     conv, conv_fused, conv_fused_nhwc, conv_nhwc, im2win_conv, im2win_conv_fused, im2win_conv_fused_nhwc,
     im2win_conv_fused_noalloc, im2win_conv_nhwc, im2win_device_status, im2win_status_string,
     im2win_transform, im2win_transform_nhwc,
-    im2win_workspace_size, lib, library_path, out_hw, status_string, transform, transform_nhwc, workspace)
+    im2win_workspace_size, lib, library_path, out_hw, status_string, transform, transform_nhwc, workspace,
+    NCHW, NHWC, conv_ex, conv_fused_ex, im2win_conv_ex, im2win_conv_fused_ex, im2win_transform_ex,
+    im2win_workspace_size_ex, out_hw_pd, transform_ex)

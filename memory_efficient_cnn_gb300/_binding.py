@@ -19,11 +19,13 @@ from . import build as _build
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 OP_TRANSFORM, OP_CONV, OP_CONV_FUSED, OP_CONV_NHWC, OP_CONV_FUSED_NHWC = 0, 1, 2, 3, 4
 F32, F16, BF16 = 0, 1, 2
+NCHW, NHWC = 0, 1
 _DTYPE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 
 EXPORTS = ("im2win_workspace_size", "im2win_transform", "im2win_conv", "im2win_conv_fused",
            "im2win_status_string", "im2win_device_status", "im2win_conv_fused_noalloc",
-           "im2win_transform_nhwc", "im2win_conv_nhwc", "im2win_conv_fused_nhwc")
+           "im2win_transform_nhwc", "im2win_conv_nhwc", "im2win_conv_fused_nhwc",
+           "im2win_workspace_size_ex", "im2win_transform_ex", "im2win_conv_ex", "im2win_conv_fused_ex")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lock = threading.Lock()
@@ -64,9 +66,16 @@ def lib() -> ctypes.CDLL:
             L.im2win_transform_nhwc.argtypes = [vp, vp] + shp + [ctypes.c_int, vp]
             L.im2win_conv_nhwc.argtypes = [vp, vp, vp, vp, sz] + shp + [ctypes.c_int, vp]
             L.im2win_conv_fused_nhwc.argtypes = [vp, vp, vp, vp, sz] + shp + [ctypes.c_int, vp]
+            pd = [i64] * 4 + [ctypes.c_int, ctypes.c_int]  # p_h, p_w, d_h, d_w, layout, dtype
+            L.im2win_workspace_size_ex.argtypes = [ctypes.c_int] + shp + pd + [ctypes.POINTER(sz)]
+            L.im2win_transform_ex.argtypes = [vp, vp] + shp + pd + [vp]
+            L.im2win_conv_ex.argtypes = [vp, vp, vp, vp, sz] + shp + pd + [vp]
+            L.im2win_conv_fused_ex.argtypes = [vp, vp, vp, vp, sz] + shp + pd + [vp]
             for f in ("im2win_workspace_size", "im2win_transform", "im2win_conv",
                       "im2win_conv_fused", "im2win_device_status", "im2win_conv_fused_noalloc",
-                      "im2win_transform_nhwc", "im2win_conv_nhwc", "im2win_conv_fused_nhwc"):
+                      "im2win_transform_nhwc", "im2win_conv_nhwc", "im2win_conv_fused_nhwc",
+                      "im2win_workspace_size_ex", "im2win_transform_ex", "im2win_conv_ex",
+                      "im2win_conv_fused_ex"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -209,6 +218,51 @@ def im2win_conv_fused_nhwc(x: torch.Tensor, filt: torch.Tensor, out: torch.Tenso
                                         W_f, s_h, s_w, _dtype_code(x), _stream(x)))
 
 
+def im2win_workspace_size_ex(op: int, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, p_h, p_w, d_h, d_w,
+                             layout: int, dtype: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("im2win_workspace_size_ex",
+           lib().im2win_workspace_size_ex(op, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, p_h, p_w, d_h, d_w,
+                                          layout, dtype, ctypes.byref(out)))
+    return out.value
+
+
+def im2win_transform_ex(x: torch.Tensor, win: torch.Tensor, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
+                        p_h, p_w, d_h, d_w, layout: int) -> None:
+    _cuda(x, win)
+    if win.dtype != x.dtype:
+        raise TypeError("win must have the dtype of x")
+    need = im2win_workspace_size_ex(OP_TRANSFORM, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, p_h, p_w,
+                                    d_h, d_w, layout, _dtype_code(x))
+    if win.numel() * win.element_size() < need:
+        raise ValueError("win is smaller than the window tensor")
+    _check("im2win_transform_ex",
+           lib().im2win_transform_ex(x.data_ptr(), win.data_ptr(), N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
+                                     p_h, p_w, d_h, d_w, layout, _dtype_code(x), _stream(x)))
+
+
+def im2win_conv_ex(win: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                   N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, p_h, p_w, d_h, d_w, layout: int) -> None:
+    _cuda(win, filt, out, ws)
+    if not (win.dtype == filt.dtype == out.dtype):
+        raise TypeError("win, filt and out must share a dtype")
+    _check("im2win_conv_ex",
+           lib().im2win_conv_ex(win.data_ptr(), filt.data_ptr(), out.data_ptr(), ws.data_ptr(),
+                                ws.numel() * ws.element_size(), N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
+                                p_h, p_w, d_h, d_w, layout, _dtype_code(win), _stream(win)))
+
+
+def im2win_conv_fused_ex(x: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                         N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, p_h, p_w, d_h, d_w, layout: int) -> None:
+    _cuda(x, filt, out, ws)
+    if not (x.dtype == filt.dtype == out.dtype):
+        raise TypeError("x, filt and out must share a dtype")
+    _check("im2win_conv_fused_ex",
+           lib().im2win_conv_fused_ex(x.data_ptr(), filt.data_ptr(), out.data_ptr(), ws.data_ptr(),
+                                      ws.numel() * ws.element_size(), N, C_i, H_i, W_i, C_o, H_f, W_f, s_h,
+                                      s_w, p_h, p_w, d_h, d_w, layout, _dtype_code(x), _stream(x)))
+
+
 def im2win_device_status(ws: torch.Tensor) -> int:
     """Synchronise the current stream and return the status word of `ws`."""
     _cuda(ws)
@@ -301,4 +355,67 @@ def conv_fused_nhwc(x: torch.Tensor, filt: torch.Tensor, stride=(1, 1), ws: torc
     if out is None:
         out = torch.empty((N, H_o, W_o, C_o), dtype=x.dtype, device=x.device)
     im2win_conv_fused_nhwc(x, filt, out, ws, stride[0], stride[1])
+    return out
+
+
+# ---------------------------------------------------------------- padding / dilation
+def _pd_dims(x_shape, layout):
+    if layout == NHWC:
+        N, H_i, W_i, C_i = x_shape
+    else:
+        N, C_i, H_i, W_i = x_shape
+    return N, C_i, H_i, W_i
+
+
+def out_hw_pd(H_i, W_i, H_f, W_f, stride, pad, dil):
+    """Output extent with zero padding and dilation."""
+    return ((H_i + 2 * pad[0] - dil[0] * (H_f - 1) - 1) // stride[0] + 1,
+            (W_i + 2 * pad[1] - dil[1] * (W_f - 1) - 1) // stride[1] + 1)
+
+
+def transform_ex(x: torch.Tensor, H_f: int, W_f: int, stride=(1, 1), pad=(0, 0), dil=(1, 1),
+                 layout: int = NCHW) -> torch.Tensor:
+    """Window tensor of the padded input with row dilation (W_i + 2 p_w columns)."""
+    N, C_i, H_i, W_i = _pd_dims(x.shape, layout)
+    H_o, _ = out_hw_pd(H_i, W_i, H_f, W_f, stride, pad, dil)
+    L = (W_i + 2 * pad[1]) * H_f
+    shape = (N, H_o, L, C_i) if layout == NHWC else (N, C_i, H_o, L)
+    win = torch.empty(shape, dtype=x.dtype, device=x.device)
+    im2win_transform_ex(x, win, N, C_i, H_i, W_i, 1, H_f, W_f, stride[0], stride[1], pad[0], pad[1],
+                        dil[0], dil[1], layout)
+    return win
+
+
+def conv_ex(win: torch.Tensor, filt: torch.Tensor, x_shape, stride=(1, 1), pad=(0, 0), dil=(1, 1),
+            layout: int = NCHW, ws: torch.Tensor | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Convolution from a window tensor produced by transform_ex(); x_shape is the
+    input's shape in `layout`."""
+    N, C_i, H_i, W_i = _pd_dims(x_shape, layout)
+    C_o, _, H_f, W_f = filt.shape
+    H_o, W_o = out_hw_pd(H_i, W_i, H_f, W_f, stride, pad, dil)
+    args = (N, C_i, H_i, W_i, C_o, H_f, W_f, stride[0], stride[1], pad[0], pad[1], dil[0], dil[1])
+    if ws is None:
+        b = im2win_workspace_size_ex(OP_CONV, *args, layout, _DTYPE[win.dtype])
+        ws = torch.empty(max(b, 16), dtype=torch.uint8, device=win.device)
+    if out is None:
+        shape = (N, H_o, W_o, C_o) if layout == NHWC else (N, C_o, H_o, W_o)
+        out = torch.empty(shape, dtype=win.dtype, device=win.device)
+    im2win_conv_ex(win, filt, out, ws, *args, layout)
+    return out
+
+
+def conv_fused_ex(x: torch.Tensor, filt: torch.Tensor, stride=(1, 1), pad=(0, 0), dil=(1, 1),
+                  layout: int = NCHW, ws: torch.Tensor | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Fused convolution with zero padding and dilation, straight from x."""
+    N, C_i, H_i, W_i = _pd_dims(x.shape, layout)
+    C_o, _, H_f, W_f = filt.shape
+    H_o, W_o = out_hw_pd(H_i, W_i, H_f, W_f, stride, pad, dil)
+    args = (N, C_i, H_i, W_i, C_o, H_f, W_f, stride[0], stride[1], pad[0], pad[1], dil[0], dil[1])
+    if ws is None:
+        b = im2win_workspace_size_ex(OP_CONV_FUSED, *args, layout, _DTYPE[x.dtype])
+        ws = torch.empty(max(b, 16), dtype=torch.uint8, device=x.device)
+    if out is None:
+        shape = (N, H_o, W_o, C_o) if layout == NHWC else (N, C_o, H_o, W_o)
+        out = torch.empty(shape, dtype=x.dtype, device=x.device)
+    im2win_conv_fused_ex(x, filt, out, ws, *args, layout)
     return out

@@ -28,6 +28,12 @@
 //    column wo*s_w (channel stride W_i*C_i, pixel stride s_w*C_i).
 // In both the filter is re-laid in the matching order and the epilogue writes
 // out[n][ho][wo][co].
+//
+// Zero padding and dilation (GEN): the same kernel with the fused variant's
+// lane mapping and a general gather: element (ci, r, j) of pixel (ho, wo) is
+// x[ci][ho*s_h + r*d_h - p_h][wo*s_w + j*d_w - p_w] (zero outside x; either
+// layout), or, from the padded window tensor, window column
+// (wo*s_w + j*d_w)*H_f + r of window row (ci, ho).
 #include <algorithm>
 
 #include "im2win_internal.cuh"
@@ -51,6 +57,10 @@ struct F32Params {
     int S;               // s_w * H_f
     int64_t img_src;     // elements of src per image
     int cs;              // window path: element stride between channels (H_o*L for the NCHW window)
+    // general gather (padding / dilation)
+    int from_win;        // source is the padded window tensor (else the input)
+    int p_h, p_w, d_h, d_w, W_f;
+    int Lw;              // padded window row length W_p*H_f
     int C_o_pad;         // row length of the transposed filter (a multiple of the channel tile)
     FastDiv div_KK, div_Wo, div_Hf;
 };
@@ -101,7 +111,7 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // w % (KC/8) and walks every (NW/(KC/8))-th group of 4 pixels. From the NCHW
 // input consecutive pixels of a row are (unit stride), so lane l of warp w
 // gathers pixels l + 32i at the KPT values of k w*KPT ...
-template <int TM, int KC, int STAGES, int MINB, bool FROM_X, bool CL>
+template <int TM, int KC, int STAGES, int MINB, bool FROM_X, bool CL, bool GEN>
 __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
     constexpr int NT = TM * 2;                 // (TM/8) x 16 threads
     constexpr int NW = NT / 32;                           // warps
@@ -131,14 +141,20 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
     const int k0 = FROM_X ? (tid >> 5) * KPT : ((tid >> 5) % KG) * 8 + (tid & 7);
     int pos_off[PPT];     // offset of the pixel's window segment; pixels past P read offset 0, size 0
     uint32_t pos_ok = 0;  // bit i: pixel i exists
+    int gh[GEN ? PPT : 1], gw[GEN ? PPT : 1];  // GEN: the pixel's first input row / column
 #pragma unroll
     for (int i = 0; i < PPT; ++i) {
         const int pg = p0 + px0 + PXS * i;
         pos_off[i] = 0;
+        if (GEN) gh[i] = gw[i] = 0;
         if (pg < p.P) {
             const int ho = (int)fdiv((uint32_t)pg, p.div_Wo);
             const int wo = pg - ho * p.W_o;
             pos_off[i] = FROM_X ? (ho * p.s_h * p.W_i + wo * p.s_w) : (ho * p.L + wo * p.S);
+            if (GEN) {
+                gh[i] = p.from_win ? ho : ho * p.s_h - p.p_h;
+                gw[i] = p.from_win ? wo * p.s_w : wo * p.s_w - p.p_w;
+            }
             pos_ok |= 1u << i;
         }
     }
@@ -151,7 +167,34 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
         const int buf = c % STAGES;
         const uint32_t a_dst = a_dst0 + buf * A_BUF;
 #pragma unroll
-        for (int j = 0; j < KPT; ++j) {
+        for (int j = 0; j < (GEN ? KPT : 0); ++j) {
+            // general gather: k = ci*KK + jj*H_f + r
+            const int kg = c * KC + k0 + j;
+            int ci = 0, jj = 0, r = 0;
+            const bool kin = kg < p.K;
+            if (kin) {
+                ci = (int)fdiv((uint32_t)kg, p.div_KK);
+                const int kk = kg - ci * p.KK;
+                jj = (int)fdiv((uint32_t)kk, p.div_Hf);
+                r = kk - jj * p.H_f;
+            }
+#pragma unroll
+            for (int i = 0; i < PPT; ++i) {
+                bool ok = kin && ((pos_ok >> i) & 1u);
+                int off = 0;
+                if (p.from_win) {
+                    const int col = (gw[i] + jj * p.d_w) * p.H_f + r;
+                    off = CL ? (gh[i] * p.Lw + col) * p.C_i + ci : (ci * p.H_o + gh[i]) * p.Lw + col;
+                } else {
+                    const int h = gh[i] + r * p.d_h, w = gw[i] + jj * p.d_w;
+                    ok = ok && (unsigned)h < (unsigned)p.H_i && (unsigned)w < (unsigned)p.W_i;
+                    off = CL ? (h * p.W_i + w) * p.C_i + ci : (ci * p.H_i + h) * p.W_i + w;
+                }
+                cp_async4(a_dst + (j * (TP + 4) + PXS * i) * 4, ok ? src + off : src, ok ? 4u : 0u);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < (GEN ? 0 : KPT); ++j) {
             const int kg = c * KC + k0 + j;
             int coff = 0;
             uint32_t ok = 0;
@@ -238,17 +281,17 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
                     if (cb + i < p.C_o) d[i] = acc[i][j];
             }
         }
-        return;
-    }
+    } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int co = co0 + ty * 8 + i;
-        if (co >= p.C_o) continue;
-        float *orow = p.out + ((int64_t)n * p.C_o + co) * p.P;
+        for (int i = 0; i < 8; ++i) {
+            const int co = co0 + ty * 8 + i;
+            if (co >= p.C_o) continue;
+            float *orow = p.out + ((int64_t)n * p.C_o + co) * p.P;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int pg = p0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
-            if (pg < p.P) orow[pg] = acc[i][j];
+            for (int j = 0; j < 8; ++j) {
+                const int pg = p0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
+                if (pg < p.P) orow[pg] = acc[i][j];
+            }
         }
     }
 }
@@ -279,14 +322,14 @@ __global__ void relayout_filter_f32(const float *__restrict__ filt, float *__res
     }
 }
 
-template <int TM, int KC, int STAGES, int MINB, bool FROM_X, bool CL = false>
+template <int TM, int KC, int STAGES, int MINB, bool FROM_X, bool CL = false, bool GEN = false>
 cudaError_t launch_tm(const F32Params &p, int N, cudaStream_t st) {
     dim3 grid((unsigned)(p.pos_tiles * N), (unsigned)((p.C_o + TM - 1) / TM));
     constexpr size_t smem = f32_smem_bytes<TM, KC, STAGES>();
-    cudaError_t e = cudaFuncSetAttribute(conv_f32_kernel<TM, KC, STAGES, MINB, FROM_X, CL>,
+    cudaError_t e = cudaFuncSetAttribute(conv_f32_kernel<TM, KC, STAGES, MINB, FROM_X, CL, GEN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    conv_f32_kernel<TM, KC, STAGES, MINB, FROM_X, CL><<<grid, TM * 2, smem, st>>>(p);
+    conv_f32_kernel<TM, KC, STAGES, MINB, FROM_X, CL, GEN><<<grid, TM * 2, smem, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -320,7 +363,7 @@ size_t conv_f32_filter_bytes(const Shape &s, bool, int) {
 
 bool conv_f32_supported(const Shape &s, bool from_x, int) {
     // elements of one image of the source (the same count in either layout)
-    const int64_t img = from_x ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * s.W_i * s.H_f;
+    const int64_t img = from_x ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * padded_w(s) * s.H_f;
     const int64_t P = s.H_o * s.W_o;
     const int64_t tiles = (P + TP - 1) / TP;
     return img < (1ll << 31) && k_pad(s) < (1ll << 30) && tiles * s.N < (1ll << 31) &&
@@ -333,10 +376,12 @@ cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *
     float *fp = reinterpret_cast<float *>(static_cast<unsigned char *>(ws) + kStatusBytes);
     const int64_t Kp = k_pad(s), Cp = c_o_pad(s);
     const bool cl = layout == LAYOUT_NHWC;
+    const bool gen = !plain(s);  // padding or dilation: the general gather, filter in NCHW window order
     // virtual filter extents and view (see the head of this file)
-    const int64_t H_fv = cl ? 1 : s.H_f;
-    const int64_t W_fv = !cl ? s.W_f : from_x ? s.W_f * s.C_i : s.W_f * s.H_f * s.C_i;
-    const int view = !cl ? VIEW_IDENT : from_x ? VIEW_CL_ROWS : VIEW_CL_WIN;
+    const bool view_cl = cl && !gen;
+    const int64_t H_fv = view_cl ? 1 : s.H_f;
+    const int64_t W_fv = !view_cl ? s.W_f : from_x ? s.W_f * s.C_i : s.W_f * s.H_f * s.C_i;
+    const int view = !view_cl ? VIEW_IDENT : from_x ? VIEW_CL_ROWS : VIEW_CL_WIN;
     const dim3 rgrid((unsigned)std::min<int64_t>((Cp + 127) / 128, 8), (unsigned)std::min<int64_t>(Kp, 65535));
     relayout_filter_f32<<<rgrid, 128, 0, st>>>(static_cast<const float *>(filt), fp, status,
                                                (int)(s.C_i * s.H_f * s.W_f), (int)Kp, (int)s.C_o, (int)Cp,
@@ -365,13 +410,20 @@ cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *
     p.pos_tiles = (p.P + TP - 1) / TP;
     p.L = (int)(s.W_i * s.H_f);
     p.S = (int)(s.s_w * s.H_f);
-    p.img_src = from_x ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * s.W_i * s.H_f;
+    p.img_src = from_x ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * padded_w(s) * s.H_f;
     p.cs = (int)(s.H_o * s.W_i * s.H_f);
+    p.from_win = from_x ? 0 : 1;
+    p.p_h = (int)s.p_h;
+    p.p_w = (int)s.p_w;
+    p.d_h = (int)s.d_h;
+    p.d_w = (int)s.d_w;
+    p.W_f = (int)s.W_f;
+    p.Lw = (int)(padded_w(s) * s.H_f);
     p.C_o_pad = (int)Cp;
     p.div_KK = make_fastdiv((uint32_t)(s.H_f * s.W_f));
     p.div_Wo = make_fastdiv((uint32_t)s.W_o);
     p.div_Hf = make_fastdiv((uint32_t)s.H_f);
-    if (cl) {
+    if (view_cl) {
         // the window path over the virtual shape: KK = H_fv*W_fv taps per channel
         p.KK = (int)(H_fv * W_fv);
         p.div_KK = make_fastdiv((uint32_t)p.KK);
@@ -388,6 +440,18 @@ cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *
 
     const int best = choose_tm(s);
     const int N = (int)s.N;
+    if (gen) {  // padding or dilation: the general gather
+        if (cl) {
+            if (best == 128) return launch_tm<F32_CFG_128, true, true, true>(p, N, st);
+            if (best == 96) return launch_tm<F32_CFG_96, true, true, true>(p, N, st);
+            if (best == 64) return launch_tm<F32_CFG_64, true, true, true>(p, N, st);
+            return launch_tm<F32_CFG_32, true, true, true>(p, N, st);
+        }
+        if (best == 128) return launch_tm<F32_CFG_128, true, false, true>(p, N, st);
+        if (best == 96) return launch_tm<F32_CFG_96, true, false, true>(p, N, st);
+        if (best == 64) return launch_tm<F32_CFG_64, true, false, true>(p, N, st);
+        return launch_tm<F32_CFG_32, true, false, true>(p, N, st);
+    }
     if (cl) {  // the window path with the channels-last epilogue
         if (best == 128) return launch_tm<F32_CFG_128, false, true>(p, N, st);
         if (best == 96) return launch_tm<F32_CFG_96, false, true>(p, N, st);

@@ -364,7 +364,16 @@ struct TapParams {
     int stack;             // CH, C_o <= 64: two taps per MMA, stacked along M (see below)
     int Gr;                // stacked: tap groups per filter row
     int nhwc;              // output out[n][ho][wo][co] (else out[n][co][ho][wo])
-    FastDiv div_wi;        // CL: positions of an input row
+    FastDiv div_wi;        // CL: positions of a slab row (W_i, or Wp when padded)
+    // zero padding and dilation (CH / CL). Filter tap (r, j) reads slab row
+    // r*dil_h and column (j / g_w)*dil_w*g_w + j % g_w relative to the output's
+    // origin; the slab covers the Wp = W_i + 2 p_w padded columns, and with
+    // padding its entry (row lr, column col) is input (ho0*s_h + lr - p_h, col - p_w),
+    // zero outside the input.
+    int p_h, p_w, dil_h, dil_w, g_w;
+    int Hfe;               // slab rows a filter spans: (H_f - 1)*dil_h + 1
+    int Wp;                // slab columns
+    int padded;            // p_h or p_w > 0: the producers zero-fill outside the input
 };
 
 // A tile: output rows [ho0, ho0 + Q) of image n, output channels [mt*128, mt*128 + 128).
@@ -398,12 +407,17 @@ __device__ __forceinline__ int tile_n0(const TapParams &p, int NTp) {
     return min(NTp, split_n0((p.Qmax * p.pitch + p.stack + 15) / 16 * 16));
 }
 
+// Slab row and column offsets of filter tap (r, j) (dilation; see TapParams).
+__host__ __device__ inline int tap_dr(int r, int dil_h) { return r * dil_h; }
+__host__ __device__ inline int tap_dc(int j, int dil_w, int g_w) { return (j / g_w) * dil_w * g_w + j % g_w; }
+
 template <int MODE>
 __device__ __forceinline__ uint32_t tap_offset(const TapParams &p, int t) {
     if (MODE == TAP_CH || MODE == TAP_CL) {
         const int r = t / p.W_f, j = t - r * p.W_f;
-        return (uint32_t)((((r % p.s_h) * p.s_w + (j % p.s_w)) * p.PB) +
-                          (((r / p.s_h) * p.pitch + (j / p.s_w)) * 16));
+        const int dr = tap_dr(r, p.dil_h), dc = tap_dc(j, p.dil_w, p.g_w);
+        return (uint32_t)((((dr % p.s_h) * p.s_w + (dc % p.s_w)) * p.PB) +
+                          (((dr / p.s_h) * p.pitch + (dc / p.s_w)) * 16));
     } else {
         const int a = t / p.U, u = t - a * p.U;
         return (uint32_t)(2 * u) * p.lbo + (uint32_t)a * 16u;
@@ -649,7 +663,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         auto issue_raw = [&](const TapTile &t, int cc, int slot) {
             const uint32_t dst0 = smem_u32(sRaw + (size_t)slot * p.raw_slot);
             if (MODE == TAP_CH) {
-                const int rows = (t.Q - 1) * p.s_h + p.H_f;
+                const int rows = (t.Q - 1) * p.s_h + p.Hfe;
                 const int vpc = rows * p.W_i / 8;  // 16-byte vectors per channel
                 const int64_t plane = (int64_t)p.H_i * p.W_i;
                 const uint16_t *x0 = p.src + ((int64_t)t.n * p.C_i * p.H_i + (int64_t)t.ho0 * p.s_h) * p.W_i;
@@ -731,29 +745,70 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 // entry (8-channel half c8, tile row lr, column col) is x[n][R0 + lr][col][cc*16 + c8*8 ..
                 // + 8]: one 16-byte copy. Lane pairs take the two halves of a position (32
                 // contiguous bytes); halves past C_i (a multiple of 8) are zero-filled.
-                const int rows = (Q - 1) * p.s_h + p.H_f;
-                const int items = 2 * rows * p.W_i;
-                const uint16_t *xr = p.src + (((int64_t)n * p.H_i + (int64_t)ho0 * p.s_h) * p.W_i) * p.C_i + cc * 16;
+                // With padding the slab spans Wp columns and the entries outside the input
+                // are zero-filled copies. C_i not a multiple of 8 (vec == 0): each entry is
+                // built from element loads and stored, then the usual fence and arrival.
+                const int rows = (Q - 1) * p.s_h + p.Hfe;
+                const int items = 2 * rows * p.Wp;
+                const int R0 = ho0 * p.s_h - p.p_h;  // input row of slab row 0
+                const uint16_t *xn = p.src + (int64_t)n * p.H_i * p.W_i * p.C_i + cc * 16;
                 for (int it = pt; it < items; it += NPT) {
                     const int c8 = it & 1;
                     const int pos = it >> 1;
                     const int lr = (int)fdiv((uint32_t)pos, p.div_wi);
-                    const int col = pos - lr * p.W_i;
+                    const int col = pos - lr * p.Wp;
                     const int lq = (int)fdiv((uint32_t)lr, p.div_sh);
                     const int cq = (int)fdiv((uint32_t)col, p.div_sw);
-                    const uint32_t dst = smem_u32(slab + (size_t)c8 * p.lbo +
-                                                  (size_t)((lr - lq * p.s_h) * p.s_w + (col - cq * p.s_w)) * p.PB +
-                                                  (size_t)(lq * p.pitch + cq) * 16);
-                    const bool ok = cc * 16 + c8 * 8 < p.C_i;
-                    cp_async16z(dst, ok ? (const void *)(xr + (int64_t)pos * p.C_i + c8 * 8) : (const void *)p.src,
-                                ok ? 16u : 0u);
+                    uint8_t *dstp = slab + (size_t)c8 * p.lbo +
+                                    (size_t)((lr - lq * p.s_h) * p.s_w + (col - cq * p.s_w)) * p.PB +
+                                    (size_t)(lq * p.pitch + cq) * 16;
+                    const int h = R0 + lr, w = col - p.p_w;
+                    const bool inside = (unsigned)h < (unsigned)p.H_i && (unsigned)w < (unsigned)p.W_i;
+                    const int c0 = cc * 16 + c8 * 8;  // first channel of the entry
+                    const uint16_t *src = xn + ((int64_t)h * p.W_i + w) * p.C_i + c8 * 8;
+                    if (p.vec) {
+                        const bool ok = inside && c0 < p.C_i;
+                        cp_async16z(smem_u32(dstp), ok ? (const void *)src : (const void *)p.src, ok ? 16u : 0u);
+                    } else {
+                        uint32_t e16[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            e16[e] = (inside && c0 + e < p.C_i) ? (uint32_t)__ldg(src + e) : 0u;
+                        *reinterpret_cast<uint4 *>(dstp) =
+                            make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
+                                       e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
+                    }
                 }
             } else if (MODE == TAP_CH) {
-                const int rows = (Q - 1) * p.s_h + p.H_f;
+                const int rows = (Q - 1) * p.s_h + p.Hfe;
                 const int64_t plane = (int64_t)p.H_i * p.W_i;
                 const uint16_t *__restrict__ xn = p.src + (int64_t)n * p.C_i * plane;
                 const int R0 = ho0 * p.s_h;
-                if (p.vec) {
+                if (p.padded) {
+                    // one slab column of 8 channels per item over the Wp padded columns;
+                    // input (R0 + lr - p_h, col - p_w), zero outside the input
+                    const int items = 2 * rows * p.Wp;
+                    for (int it = pt; it < items; it += NPT) {
+                        const int t2 = it / p.Wp;
+                        const int col = it - t2 * p.Wp;
+                        const int c8 = t2 >= rows ? 1 : 0;
+                        const int lr = t2 - c8 * rows;
+                        const int ci0 = cc * 16 + c8 * 8;
+                        const int h = R0 + lr - p.p_h, w = col - p.p_w;
+                        const bool inside = (unsigned)h < (unsigned)p.H_i && (unsigned)w < (unsigned)p.W_i;
+                        const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)h * p.W_i + w;
+                        uint32_t e16[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            e16[e] = (inside && ci0 + e < p.C_i) ? (uint32_t)__ldg(src + e * plane) : 0u;
+                        uint8_t *dst = slab + (size_t)c8 * p.lbo +
+                                       (size_t)((lr % p.s_h) * p.s_w + col % p.s_w) * p.PB +
+                                       (size_t)((lr / p.s_h) * p.pitch + col / p.s_w) * 16;
+                        *reinterpret_cast<uint4 *>(dst) =
+                            make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
+                                       e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
+                    }
+                } else if (p.vec) {
                     // 8 channels x 8 columns per item: 8 16-byte loads (from the raw slot or
                     // global memory), 8x8 transpose, 8 16-byte stores
                     const int cgs = p.W_i / 8;
@@ -858,7 +913,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 }
             }
             if (pok) {
-                if (MODE == TAP_CL) {
+                if (MODE == TAP_CL && p.vec) {
                     cp_async_mbar_arrive_noinc(full_b(sb_g));  // once this thread's copies land
                 } else {
                     fence_async_smem();
@@ -1091,13 +1146,17 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
     const int64_t smem_max = 227 * 1024 - 1024;
     if (s.C_i * s.H_i * s.W_i >= (1ll << 31)) return pl;
     const bool chan = mode == TAP_CH || mode == TAP_CL;
-    if (mode == TAP_CL && s.C_i % 8 != 0) return pl;  // 16-byte entries of 8 channels
+    if (!chan && !plain(s)) return pl;  // padding / dilation: channel modes only
+    const int64_t Wp = padded_w(s);
+    const int64_t Hfe = (s.H_f - 1) * s.d_h + 1;  // slab rows a filter spans
+    if (Wp * s.C_i * (s.H_i + 2 * s.p_h) >= (1ll << 31)) return pl;
     int64_t pitch, T, U = 0, S = 0, A = 0, NCH;
-    // stacking (TAP_CH / TAP_CL, C_o <= 64, some tap has a partner): T counts tap groups
-    const int stack = (chan && s.C_o <= 64 && s.W_f > s.s_w) ? 1 : 0;
+    // stacking (TAP_CH / TAP_CL, C_o <= 64, some tap has a partner, no dilation): T
+    // counts tap groups
+    const int stack = (chan && s.C_o <= 64 && s.W_f > s.s_w && s.d_h == 1 && s.d_w == 1) ? 1 : 0;
     const int Gr = stack ? stacked_groups_per_row((int)s.W_f, (int)s.s_w) : 0;
     if (chan) {
-        pitch = (s.W_i + s.s_w - 1) / s.s_w;
+        pitch = (Wp + s.s_w - 1) / s.s_w;
         T = stack ? s.H_f * Gr : s.H_f * s.W_f;
         NCH = (s.C_i + 15) / 16;
     } else {
@@ -1129,7 +1188,7 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
             if (t < best * 0.99) { best = t; Q = q; }
         }
         const int64_t NTp = (Q * pitch + stack + 15) / 16 * 16;
-        const int64_t RR = (Q - 1) * s.s_h + s.H_f;  // input rows under a tile of Q rows
+        const int64_t RR = (Q - 1) * s.s_h + Hfe;  // slab rows under a tile of Q rows
         int64_t PB = 0, lbo, stage_b;
         if (chan) {
             const int64_t HH = (RR + s.s_h - 1) / s.s_h;
@@ -1137,9 +1196,11 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
             lbo = s.s_h * s.s_w * PB;
             int64_t max_tap = 0;
             for (int64_t r = 0; r < s.H_f; ++r)
-                for (int64_t j = 0; j < s.W_f; ++j)
-                    max_tap = std::max(max_tap, ((r % s.s_h) * s.s_w + j % s.s_w) * PB +
-                                                    ((r / s.s_h) * pitch + j / s.s_w) * 16);
+                for (int64_t j = 0; j < s.W_f; ++j) {
+                    const int64_t dr = tap_dr((int)r, (int)s.d_h), dc = tap_dc((int)j, (int)s.d_w, (int)s.g_w);
+                    max_tap = std::max(max_tap, ((dr % s.s_h) * s.s_w + dc % s.s_w) * PB +
+                                                    ((dr / s.s_h) * pitch + dc / s.s_w) * 16);
+                }
             // plane 1 is written up to 2*lbo and read up to lbo + max_tap + NTp*16
             stage_b = std::max(2 * lbo, lbo + max_tap + NTp * 16);
         } else {
@@ -1153,7 +1214,7 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
         // input rows, TAP_WW its window rows, each with room for the alignment lead;
         // TAP_CL copies straight into the slab
         const int64_t slot = mode == TAP_CL ? 0
-                             : mode == TAP_CH ? (s.W_i % 8 == 0 ? 16 * RR * s.W_i : 0)
+                             : mode == TAP_CH ? (s.W_i % 8 == 0 && s.p_h == 0 && s.p_w == 0 ? 16 * RR * s.W_i : 0)
                              : mode == TAP_WX ? RR * s.W_i + 16
                                               : Q * s.W_i * s.H_f + 16;
         const int64_t slot_e = (slot + 63) / 64 * 64;
@@ -1186,6 +1247,11 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
                     p.T = (int)T;
                     p.stack = stack;
                     p.Gr = Gr;
+                    p.p_h = (int)s.p_h; p.p_w = (int)s.p_w;
+                    p.dil_h = (int)s.d_h; p.dil_w = (int)s.d_w; p.g_w = (int)s.g_w;
+                    p.Hfe = (int)Hfe;
+                    p.Wp = (int)Wp;
+                    p.padded = (s.p_h > 0 || s.p_w > 0) ? 1 : 0;
                     p.TG = tg;
                     p.ntg = (int)((T + tg - 1) / tg);
                     p.Qmax = (int)Q;
@@ -1243,15 +1309,22 @@ ExpandGeom expand_geom(const Shape &s) {
 // the re-laid filter as one row of W_f*H_f taps, and output pixel wo starts at
 // window offset wo*s_w*H_f (the dot product of the im2win convolution). So the
 // window tensor is an input of H_o x W_i*H_f, filtered by 1 x W_f*H_f at stride
-// (1, s_w*H_f); the output extents are unchanged.
+// (1, s_w*H_f); the output extents are unchanged. A padded window tensor has
+// rows of W_p*H_f elements and needs no padding of its own; with column
+// dilation d_w, filter column j (run j / H_f) starts (j / H_f)*d_w*H_f + j % H_f
+// into the pixel's window (g_w = H_f).
 static Shape window_as_input(const Shape &s) {
     Shape v = s;
     v.H_i = s.H_o;
-    v.W_i = s.W_i * s.H_f;
+    v.W_i = padded_w(s) * s.H_f;
     v.H_f = 1;
     v.W_f = s.W_f * s.H_f;
     v.s_h = 1;
     v.s_w = s.s_w * s.H_f;
+    v.p_h = v.p_w = 0;
+    v.d_h = 1;
+    v.d_w = s.d_w;
+    v.g_w = s.d_w > 1 ? s.H_f : 1;
     return v;
 }
 
@@ -1278,7 +1351,10 @@ static Shape channels_as_columns(const Shape &s) {
 //   NHWC window:  TAP_CL over the window tensor seen as an input; TAP_WW over it
 //                 seen as one channel.
 // NCHW falls back to the expand kernel when the choice's K padding costs more
-// than half again the expand kernel's K; NHWC has no fallback.
+// than half again the expand kernel's K; NHWC has no fallback. Padding and
+// dilation run the channel modes only (TAP_CH / TAP_CL), without fallback.
+static bool has_expand(const Shape &s, int layout) { return layout == LAYOUT_NCHW && plain(s); }
+
 static TapPlan choose_tap(const Shape &s, bool fused, int layout, int64_t sms = 148) {
     struct Cand {
         int mode;
@@ -1305,21 +1381,21 @@ static TapPlan choose_tap(const Shape &s, bool fused, int layout, int64_t sms = 
         if (pl.ok && (!best.ok || pl.kslots < best.kslots)) best = pl;
     }
     const int64_t expand_k = s.C_i * ((s.H_f * s.W_f + 7) / 8 * 8);
-    if (layout == LAYOUT_NCHW && best.ok && best.kslots * 2 > expand_k * 3) best.ok = false;
+    if (has_expand(s, layout) && best.ok && best.kslots * 2 > expand_k * 3) best.ok = false;
     return best;
 }
 
 size_t conv_tc_filter_bytes(const Shape &s, bool fused, int layout) {
     const TapPlan pl = choose_tap(s, fused, layout);
     if (pl.ok) return round_up((size_t)pl.mtiles * pl.p.NCH * pl.p.T * TAP_A_BYTES, 256);
-    if (layout != LAYOUT_NCHW) return 0;
+    if (!has_expand(s, layout)) return 0;
     const ExpandGeom g = expand_geom(s);
     return round_up((size_t)g.mtiles * BM * (size_t)g.K_pad * 2, 256);
 }
 
 bool conv_tc_supported(const Shape &s, bool fused, int layout) {
     if (choose_tap(s, fused, layout).ok) return true;
-    if (layout != LAYOUT_NCHW) return false;
+    if (!has_expand(s, layout)) return false;
     const int64_t img = fused ? s.C_i * s.H_i * s.W_i : s.C_i * s.H_o * s.W_i * s.H_f;
     const int64_t KKP = (s.H_f * s.W_f + 7) / 8 * 8;
     const int64_t P = s.H_o * s.W_o;
@@ -1351,13 +1427,15 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
     p.out = static_cast<uint16_t *>(out);
     p.status = status;
     p.vec = (p.W_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
+    if (pl.mode == TAP_CL)  // 16-byte entries: 8 channels of one position
+        p.vec = (p.C_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
     if (pl.mode == TAP_CH && !p.vec) p.ring = 0;  // 16-byte copies need 16-byte rows
     p.div_pitch = make_fastdiv((uint32_t)p.pitch);
     p.div_cgs = make_fastdiv((uint32_t)std::max(1, p.W_i / 8));
     p.div_sh = make_fastdiv((uint32_t)p.s_h);
     p.div_sw = make_fastdiv((uint32_t)p.s_w);
-    p.div_vpc = make_fastdiv((uint32_t)std::max(1, ((p.Qmax - 1) * p.s_h + p.H_f) * p.W_i / 8));
-    p.div_wi = make_fastdiv((uint32_t)p.W_i);
+    p.div_vpc = make_fastdiv((uint32_t)std::max(1, ((p.Qmax - 1) * p.s_h + p.Hfe) * p.W_i / 8));
+    p.div_wi = make_fastdiv((uint32_t)p.Wp);
     p.nhwc = layout == LAYOUT_NHWC ? 1 : 0;
     p.bf16 = bf16 ? 1 : 0;
     const unsigned grid = (unsigned)std::min<int64_t>(sm_count(), p.tiles_total);
@@ -1388,7 +1466,7 @@ cudaError_t launch_conv_tc(const void *src, const void *filt, void *out, void *w
                            bool fused, int layout, bool bf16, cudaStream_t st) {
     const TapPlan pl = choose_tap(s, fused, layout, sm_count());
     if (pl.ok) return launch_tap(pl, src, filt, out, ws, s, layout, bf16, st);
-    if (layout != LAYOUT_NCHW) return cudaErrorNotSupported;
+    if (!has_expand(s, layout)) return cudaErrorNotSupported;
     const ExpandGeom g = expand_geom(s);
     uint32_t *status = static_cast<uint32_t *>(ws);
     uint16_t *fa = reinterpret_cast<uint16_t *>(static_cast<unsigned char *>(ws) + kStatusBytes);

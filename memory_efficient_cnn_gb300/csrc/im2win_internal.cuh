@@ -9,11 +9,23 @@
 
 namespace im2win {
 
-// Problem shape with the valid-convolution output extents derived
-// (Table I of the GPU im2win paper: no padding, floor division).
+// Problem shape with the output extents derived. Table I of the GPU im2win
+// paper has valid convolutions (no padding, floor division); the optional zero
+// padding p_h, p_w and dilation d_h, d_w follow the usual CNN definitions:
+//   H_o = (H_i + 2 p_h - d_h (H_f - 1) - 1) / s_h + 1   (likewise W_o),
+// input element (ho*s_h + r*d_h - p_h, wo*s_w + j*d_w - p_w), zero outside.
+// g_w > 1 only in the virtual shape of a window tensor read as an input with
+// column dilation: filter column j there sits at input column
+// (j / g_w)*d_w*g_w + j % g_w (runs of g_w = H_f window elements).
 struct Shape {
     int64_t N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, H_o, W_o;
+    int64_t p_h = 0, p_w = 0, d_h = 1, d_w = 1, g_w = 1;
 };
+
+// No padding, no dilation: the pages' valid convolution.
+inline bool plain(const Shape &s) { return s.p_h == 0 && s.p_w == 0 && s.d_h == 1 && s.d_w == 1 && s.g_w == 1; }
+// Padded input width.
+inline int64_t padded_w(const Shape &s) { return s.W_i + 2 * s.p_w; }
 
 // Status block at the start of every convolution workspace (256 bytes).
 // word 0: im2win_status of the last call; word 1: wait site that gave up;
@@ -89,11 +101,15 @@ enum Layout { LAYOUT_NCHW = 0, LAYOUT_NHWC = 1 };
 // ---- launchers (each returns cudaSuccess or the launch error) ----
 
 // Window transform of esz-byte elements (NCHW), and its channels-last form
-// win[n][ho][w*H_f + r][c] = x[n][ho*s_h + r][w][c].
+// win[n][ho][w*H_f + r][c] = x[n][ho*s_h + r][w][c]; the padded/dilated form
+// (either layout) runs over the W_i + 2 p_w padded columns and rows
+// ho*s_h + r*d_h - p_h, zero outside x.
 cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, cudaStream_t st);
 bool transform_supported(const Shape &s, int esz);
 cudaError_t launch_transform_nhwc(const void *x, void *win, const Shape &s, int esz, cudaStream_t st);
 bool transform_nhwc_supported(const Shape &s, int esz);
+cudaError_t launch_transform_pd(const void *x, void *win, const Shape &s, int esz, int layout, cudaStream_t st);
+bool transform_pd_supported(const Shape &s, int esz);
 
 // fp32 CUDA-core convolution; from_x selects the fused variant that gathers
 // from the input instead of the window tensor; layout is NCHW or NHWC for the

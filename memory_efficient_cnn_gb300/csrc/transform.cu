@@ -551,6 +551,170 @@ bool transform_nhwc_supported(const Shape &s, int esz) {
     return bytes / 16 < (1ll << 30) && runs < (1ll << 31) && s.W_i * s.H_f * s.C_i < (1ll << 40);
 }
 
+// ---- padded / dilated window transform (either layout)
+// A plane is one (image, channel) of NCHW (C = 1 element per position) or one
+// image of NHWC (C = C_i channels per position, innermost). Its window row ho
+// holds, for the W_p = W_i + 2 p_w padded columns w and the H_f rows r,
+//   win[plane][ho][(w*H_f + r)*C + c] = x[plane][ho*s_h + r*d_h - p_h][w - p_w][c]
+// (zero outside x). A CTA owns a band of output rows of one plane; the input
+// rows under it that exist are one contiguous range of x, staged in shared
+// memory when they fit (else read from global memory); each thread builds
+// 16-byte output vectors by stepping (c, r, w, row), the band's unaligned ends
+// element by element.
+namespace {
+
+struct TPParams {
+    const void *x;
+    void *win;
+    int64_t x_elems;
+    int H_i, W_i, C, H_f, s_h, p_h, p_w, d_h, H_o, Wp;
+    int Lp;              // window row length W_p*H_f*C
+    int T, tiles;        // output rows per band, bands per plane
+    int staged;          // 1: input rows staged in shared memory
+};
+
+template <typename E>
+__global__ void __launch_bounds__(256) transform_pd_kernel(TPParams p) {
+    extern __shared__ __align__(16) unsigned char smem_pd[];
+    constexpr int V = 16 / sizeof(E);
+    E *s_in = reinterpret_cast<E *>(smem_pd);
+    const E *__restrict__ x = static_cast<const E *>(p.x);
+    E *__restrict__ win = static_cast<E *>(p.win);
+    const int64_t plane = blockIdx.x / p.tiles;
+    const int tile = (int)(blockIdx.x - plane * p.tiles);
+    const int ho0 = tile * p.T;
+    const int rows_out = min(p.T, p.H_o - ho0);
+    const int RL = p.W_i * p.C;
+    // input rows [hs, he) of the plane under the band (clipped to x)
+    const int hs = max(0, ho0 * p.s_h - p.p_h);
+    const int he = min(p.H_i, (ho0 + rows_out - 1) * p.s_h + (p.H_f - 1) * p.d_h - p.p_h + 1);
+    const int64_t in0 = (plane * p.H_i + hs) * (int64_t)RL;
+    const E *src = x + in0;  // element (h, w, c) of the plane at src[(h - hs)*RL + w*C + c]
+    if (p.staged) {
+        const int cnt = max(0, he - hs) * RL;
+        const int64_t base = in0 - (in0 % V);
+        const int lead = (int)(in0 - base);
+        const int nvec = (lead + cnt + V - 1) / V;
+        const int64_t inside = (p.x_elems - base) / V;
+        const int nfull = inside < (int64_t)nvec ? (int)inside : nvec;
+        const uint4 *gx = reinterpret_cast<const uint4 *>(x + base);
+        uint4 *sx = reinterpret_cast<uint4 *>(s_in);
+        int v = threadIdx.x;
+        for (; v + 3 * 256 < nfull; v += 4 * 256) {
+            const uint4 r0 = __ldg(gx + v), r1 = __ldg(gx + v + 256);
+            const uint4 r2 = __ldg(gx + v + 512), r3 = __ldg(gx + v + 768);
+            sx[v] = r0;
+            sx[v + 256] = r1;
+            sx[v + 512] = r2;
+            sx[v + 768] = r3;
+        }
+        for (; v < nfull; v += 256) sx[v] = __ldg(gx + v);
+        for (int e = nfull * V + (int)threadIdx.x; e < nvec * V; e += 256)
+            if (base + e < p.x_elems) s_in[e] = x[base + e];
+        __syncthreads();
+        src = s_in + lead;
+    }
+    const int C = p.C, H_f = p.H_f, Lp = p.Lp;
+    // element g of the band: t = g / Lp, (w*H_f + r)*C + c = g % Lp
+    auto value = [&](int t, int w, int r, int c) -> E {
+        const int h = (ho0 + t) * p.s_h + r * p.d_h - p.p_h;
+        const int wx = w - p.p_w;
+        return ((unsigned)h < (unsigned)p.H_i && (unsigned)wx < (unsigned)p.W_i) ? src[(h - hs) * RL + wx * C + c]
+                                                                                   : E(0);
+    };
+    auto value_at = [&](int g) -> E {
+        const int t = g / Lp, o = g - t * Lp;
+        const int pos = o / C, c = o - pos * C;
+        const int w = pos / H_f, r = pos - w * H_f;
+        return value(t, w, r, c);
+    };
+    const int64_t f0 = (plane * p.H_o + ho0) * (int64_t)Lp;
+    const int64_t f1 = f0 + (int64_t)rows_out * Lp;
+    const int64_t head = min(f1, (f0 + V - 1) / V * V);
+    const int64_t vend = max(head, f1 / V * V);
+    for (int64_t e = f0 + threadIdx.x; e < head; e += 256) win[e] = value_at((int)(e - f0));
+    for (int64_t e = vend + threadIdx.x; e < f1; e += 256) win[e] = value_at((int)(e - f0));
+    for (int64_t vv = head / V + threadIdx.x; vv < vend / V; vv += 256) {
+        const int g = (int)(vv * V - f0);
+        int t = g / Lp;
+        const int o = g - t * Lp;
+        const int pos = o / C;
+        int c = o - pos * C;
+        int w = pos / H_f, r = pos - w * H_f;
+        union {
+            uint4 u;
+            E e[V];
+        } out;
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            out.e[e] = value(t, w, r, c);
+            if (++c == C) {
+                c = 0;
+                if (++r == H_f) {
+                    r = 0;
+                    if (++w == p.Wp) { w = 0; ++t; }
+                }
+            }
+        }
+        *reinterpret_cast<uint4 *>(win + vv * V) = out.u;
+    }
+}
+
+constexpr int kPdStageBudget = 48 * 1024;
+
+}  // namespace
+
+cudaError_t launch_transform_pd(const void *x, void *win, const Shape &s, int esz, int layout,
+                                cudaStream_t st) {
+    const bool cl = layout == LAYOUT_NHWC;
+    TPParams p;
+    p.x = x;
+    p.win = win;
+    p.x_elems = s.N * s.C_i * s.H_i * s.W_i;
+    p.H_i = (int)s.H_i;
+    p.W_i = (int)s.W_i;
+    p.C = cl ? (int)s.C_i : 1;
+    p.H_f = (int)s.H_f;
+    p.s_h = (int)s.s_h;
+    p.p_h = (int)s.p_h;
+    p.p_w = (int)s.p_w;
+    p.d_h = (int)s.d_h;
+    p.H_o = (int)s.H_o;
+    p.Wp = (int)padded_w(s);
+    p.Lp = (int)(padded_w(s) * s.H_f * p.C);
+    const int64_t planes = cl ? s.N : s.N * s.C_i;
+    const int64_t RLb = s.W_i * p.C * esz;
+    // output rows per band: as many as the staging budget holds (at least one band
+    // row per CTA; rows too long to stage are read from global memory)
+    int64_t T = 0;
+    while (T < s.H_o && (T * s.s_h + (s.H_f - 1) * s.d_h + 1) * RLb + 16 <= kPdStageBudget) ++T;
+    p.staged = T >= 1 ? 1 : 0;
+    if (T < 1) T = std::min<int64_t>(s.H_o, 4);
+    const int64_t tiles = (s.H_o + T - 1) / T;
+    T = (s.H_o + tiles - 1) / tiles;
+    p.T = (int)T;
+    p.tiles = (int)tiles;
+    if (planes == 0 || s.H_o == 0) return cudaSuccess;
+    const size_t smem =
+        p.staged ? (size_t)((((T - 1) * s.s_h + (s.H_f - 1) * s.d_h + 1) * RLb + 16 + 15) / 16 * 16) : 0;
+    const unsigned blocks = (unsigned)(planes * tiles);
+    if (esz == 2) {
+        if (smem) cudaFuncSetAttribute(transform_pd_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        transform_pd_kernel<uint16_t><<<blocks, 256, smem, st>>>(p);
+    } else {
+        if (smem) cudaFuncSetAttribute(transform_pd_kernel<uint32_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        transform_pd_kernel<uint32_t><<<blocks, 256, smem, st>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+// 32-bit indexing within a band and a plane; one CTA per (plane, band).
+bool transform_pd_supported(const Shape &s, int esz) {
+    const int64_t Lp = padded_w(s) * s.H_f * s.C_i;  // the longest window row (NHWC)
+    return s.H_o * Lp < (1ll << 31) && s.H_i * s.W_i * s.C_i < (1ll << 31) &&
+           s.N * s.C_i * ((s.H_o + 3) / 4 + 1) < (1ll << 31) && esz > 0;
+}
+
 // The transform indexes a band with 32-bit arithmetic and launches one CTA per
 // (plane, band, column tile).
 bool transform_supported(const Shape &s, int esz) {

@@ -39,15 +39,26 @@ class Layer:
     s_w: int
     seed: int
     dtypes: tuple = field(default=("f32",))
+    pad: tuple = (0, 0)   # zero padding (p_h, p_w)
+    dil: tuple = (1, 1)   # dilation (d_h, d_w)
 
     @property
     def shape_args(self):
         return (self.N, self.C_i, self.H_i, self.W_i, self.C_o, self.H_f, self.W_f,
                 self.s_h, self.s_w)
 
+    @property
+    def plain(self) -> bool:
+        return tuple(self.pad) == (0, 0) and tuple(self.dil) == (1, 1)
+
+    @property
+    def out_hw(self):
+        return ((self.H_i + 2 * self.pad[0] - self.dil[0] * (self.H_f - 1) - 1) // self.s_h + 1,
+                (self.W_i + 2 * self.pad[1] - self.dil[1] * (self.W_f - 1) - 1) // self.s_w + 1)
+
     def with_batch(self, n: int) -> "Layer":
         return Layer(self.name, n, self.C_i, self.H_i, self.W_i, self.C_o, self.H_f,
-                     self.W_f, self.s_h, self.s_w, self.seed, self.dtypes)
+                     self.W_f, self.s_h, self.s_w, self.seed, self.dtypes, self.pad, self.dil)
 
 
 TINY = Layer("tiny_3x32x32_8x3x3", 1, 3, 32, 32, 8, 3, 3, 1, 1, seed=0, dtypes=("f32",))
@@ -63,6 +74,14 @@ CV2 = Layer("cv2", 128, 3, 231, 231, 96, 11, 11, 4, 4, seed=5, dtypes=("f16", "f
 CV3 = Layer("cv3", 128, 3, 227, 227, 64, 7, 7, 2, 2, seed=6, dtypes=("f16", "f32"))
 
 ALL = (TINY, CV1, CV4, CV5) + SWEEP + (CV2, CV3)
+
+# Zero padding and dilation (not on the pages; the usual CNN options): the 3x3
+# sweep layer as a "same" convolution, and with dilation 2.
+SAME_3x3 = Layer("sweep_3x3_pad1", 64, 128, 56, 56, 128, 3, 3, 1, 1, seed=500, dtypes=("f32", "bf16"),
+                 pad=(1, 1))
+DIL_3x3 = Layer("sweep_3x3_pad2_dil2", 64, 128, 56, 56, 128, 3, 3, 1, 1, seed=501, dtypes=("f32", "bf16"),
+                pad=(2, 2), dil=(2, 2))
+PADDED = (SAME_3x3, DIL_3x3)
 
 
 def make_inputs(layer: Layer, dtype: str, seed: int | None = None, n_images: int | None = None):

@@ -89,3 +89,35 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(1, 3, 8, 8)
     with pytest.raises(ValueError, match="CUDA"):
         mec.transform(x, 3, 1)
+
+
+def test_ex_workspace_sizes_and_argument_errors(lib):
+    sz = ctypes.c_size_t()
+    L = lib
+    base = [2, 16, 20, 21, 32, 3, 3, 1, 1]
+    # padding widens the window rows: N*C_i*H_o*(W_i + 2 p_w)*H_f elements
+    b = mec.im2win_workspace_size_ex(mec.OP_TRANSFORM, *base, 1, 2, 1, 1, mec.NCHW, mec.F16)
+    assert b == 2 * 16 * 20 * (21 + 4) * 3 * 2
+    b = mec.im2win_workspace_size_ex(mec.OP_TRANSFORM, *base, 0, 0, 2, 1, mec.NHWC, mec.F32)
+    assert b == 2 * 16 * 16 * 21 * 3 * 4  # dilation 2: H_o = 20 - 4
+    # with p = 0 and d = 1 the sizes equal the valid calls'
+    for op, op_plain in ((mec.OP_CONV, mec.OP_CONV), (mec.OP_CONV_FUSED, mec.OP_CONV_FUSED)):
+        for dt in (mec.F32, mec.F16):
+            assert (mec.im2win_workspace_size_ex(op, *base, 0, 0, 1, 1, mec.NCHW, dt)
+                    == mec.im2win_workspace_size(op_plain, *base, dt))
+    for op in (mec.OP_CONV, mec.OP_CONV_FUSED):
+        for lo in (mec.NCHW, mec.NHWC):
+            for dt in (mec.F32, mec.F16, mec.BF16):
+                b = mec.im2win_workspace_size_ex(op, *base, 1, 1, 2, 2, lo, dt)
+                assert b % 256 == 0 and b >= 256 + 32 * 16 * 9 * (4 if dt == mec.F32 else 2)
+    bad = mec._binding.ERR_INVALID_ARG
+    pd = [ctypes.c_int64(v) for v in (1, 1, 1, 1)]
+    assert L.im2win_workspace_size_ex(0, *base, *pd, 7, 0, ctypes.byref(sz)) == bad   # layout
+    assert L.im2win_workspace_size_ex(0, *base, -1, 0, 1, 1, 0, 0, ctypes.byref(sz)) == bad
+    assert L.im2win_workspace_size_ex(0, *base, 0, 0, 0, 1, 0, 0, ctypes.byref(sz)) == bad
+    # the dilated filter (7 rows) does not fit 20 + 2*0 rows? it does; 11 rows of d=10 do not
+    assert L.im2win_workspace_size_ex(0, *base[:5], 3, 3, 1, 1, 0, 0, 10, 1, 0, 0,
+                                      ctypes.byref(sz)) == bad
+    assert L.im2win_transform_ex(None, 256, *base, 0, 0, 1, 1, 0, 0, None) == bad
+    assert L.im2win_conv_fused_ex(1024 + 4, 2048, 4096, 8192, 1 << 20, *base, 0, 0, 1, 1, 0, 1,
+                                  None) == mec._binding.ERR_MISALIGNED
