@@ -663,18 +663,24 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         auto issue_raw = [&](const TapTile &t, int cc, int slot) {
             const uint32_t dst0 = smem_u32(sRaw + (size_t)slot * p.raw_slot);
             if (MODE == TAP_CH) {
+                // raw row lr is input row ho0*s_h - p_h + lr (zero-filled outside the input)
                 const int rows = (t.Q - 1) * p.s_h + p.Hfe;
-                const int vpc = rows * p.W_i / 8;  // 16-byte vectors per channel
+                const int cgs = p.W_i / 8;
+                const int vpc = rows * cgs;  // 16-byte vectors per channel
                 const int64_t plane = (int64_t)p.H_i * p.W_i;
-                const uint16_t *x0 = p.src + ((int64_t)t.n * p.C_i * p.H_i + (int64_t)t.ho0 * p.s_h) * p.W_i;
+                const uint16_t *xb = p.src + (int64_t)t.n * p.C_i * plane;
+                const int hb = t.ho0 * p.s_h - p.p_h;
                 const bool full = t.Q == p.Qmax;
                 for (int v = pt; v < 16 * vpc; v += NPT) {
                     const int k = full ? (int)fdiv((uint32_t)v, p.div_vpc) : v / vpc;
                     const int i = v - k * vpc;
+                    const int lr = (int)fdiv((uint32_t)i, p.div_cgs);
+                    const int h = hb + lr;
                     const int ci = cc * 16 + k;
-                    const bool ok = ci < p.C_i;
+                    const bool ok = ci < p.C_i && (unsigned)h < (unsigned)p.H_i;
                     cp_async16z(dst0 + (uint32_t)(k * p.raw_ch + i * 8) * 2,
-                                ok ? (const void *)(x0 + (int64_t)ci * plane + (int64_t)i * 8) : (const void *)p.src,
+                                ok ? (const void *)(xb + (int64_t)ci * plane + (int64_t)h * p.W_i + (i - lr * cgs) * 8)
+                                   : (const void *)p.src,
                                 ok ? 16u : 0u);
                 }
             } else {
@@ -706,6 +712,17 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 if (id < p.tiles_total) tile_at(p, id, t);
             }
         };
+        if (MODE == TAP_CH && p.vec && p.p_w > 0) {
+            // the 16-byte fills write only the slab columns of input columns: clear every
+            // stage once, so that the padding columns read as zero; all producers fence
+            // their clears and meet before any chunk is filled
+            const int ptid = threadIdx.x - 64;
+            const int n16 = (int)(p.BST * p.stage_b / 16);
+            for (int i = ptid; i < n16; i += TAP_PROD_WARPS * 32)
+                reinterpret_cast<uint4 *>(sB)[i] = make_uint4(0, 0, 0, 0);
+            fence_async_smem();
+            asm volatile("bar.sync %0, %1;" ::"r"(3), "r"(TAP_PROD_WARPS * 32) : "memory");
+        }
         int64_t id = blockIdx.x;
         int cc = 0;
         TapTile tl;
@@ -784,7 +801,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 const int64_t plane = (int64_t)p.H_i * p.W_i;
                 const uint16_t *__restrict__ xn = p.src + (int64_t)n * p.C_i * plane;
                 const int R0 = ho0 * p.s_h;
-                if (p.padded) {
+                if (p.padded && !p.vec) {
                     // one slab column of 8 channels per item over the Wp padded columns;
                     // input (R0 + lr - p_h, col - p_w), zero outside the input
                     const int items = 2 * rows * p.Wp;
@@ -825,18 +842,23 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
 #pragma unroll
                             for (int e = 0; e < 8; ++e) v[e] = *reinterpret_cast<const uint4 *>(src + (size_t)e * p.raw_ch);
                         } else {
-                            const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)(R0 + lr) * p.W_i + cg * 8;
+                            // input row R0 - p_h + lr (zero outside the input)
+                            const int h = R0 - p.p_h + lr;
+                            const bool rok = (unsigned)h < (unsigned)p.H_i;
+                            const uint16_t *src = xn + (int64_t)ci0 * plane + (int64_t)h * p.W_i + cg * 8;
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
-                                v[e] = (ci0 + e < p.C_i) ? __ldg(reinterpret_cast<const uint4 *>(src + e * plane))
-                                                         : make_uint4(0, 0, 0, 0);
+                                v[e] = (rok && ci0 + e < p.C_i)
+                                           ? __ldg(reinterpret_cast<const uint4 *>(src + e * plane))
+                                           : make_uint4(0, 0, 0, 0);
                         }
                         const int lq = (int)fdiv((uint32_t)lr, p.div_sh);
                         uint8_t *rowp = slab + (size_t)c8 * p.lbo + (size_t)((lr - lq * p.s_h) * p.s_w) * p.PB +
                                         (size_t)(lq * p.pitch) * 16;
-                        // column cg*8 + kk lives in phase block (col % s_w) at entry col / s_w
-                        int cq = (int)fdiv((uint32_t)(cg * 8), p.div_sw);
-                        int cph = cg * 8 - cq * p.s_w;
+                        // input column cg*8 + kk is slab column col = p_w + cg*8 + kk, in phase
+                        // block (col % s_w) at entry col / s_w
+                        int cq = (int)fdiv((uint32_t)(cg * 8 + p.p_w), p.div_sw);
+                        int cph = cg * 8 + p.p_w - cq * p.s_w;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint32_t sel = (kk & 1) ? 0x7632u : 0x5410u;
@@ -1214,7 +1236,7 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
         // input rows, TAP_WW its window rows, each with room for the alignment lead;
         // TAP_CL copies straight into the slab
         const int64_t slot = mode == TAP_CL ? 0
-                             : mode == TAP_CH ? (s.W_i % 8 == 0 && s.p_h == 0 && s.p_w == 0 ? 16 * RR * s.W_i : 0)
+                             : mode == TAP_CH ? (s.W_i % 8 == 0 ? 16 * RR * s.W_i : 0)
                              : mode == TAP_WX ? RR * s.W_i + 16
                                               : Q * s.W_i * s.H_f + 16;
         const int64_t slot_e = (slot + 63) / 64 * 64;

@@ -52,6 +52,10 @@ CASES = [
     (1, 12, 9, 10, 20, 2, 3, (1, 1), (1, 2), (2, 1)),       # channels not a multiple of 8
     (2, 5, 11, 13, 7, 3, 2, (2, 1), (0, 1), (1, 2)),        # mixed strides, one-sided options
     (1, 8, 6, 7, 16, 3, 3, (1, 1), (4, 4), (1, 1)),         # padding wider than the filter: all-zero rows
+    # rows of whole 16-byte vectors: the staged (ring) slab fill with shifted columns
+    (1, 40, 14, 32, 64, 5, 5, (1, 1), (2, 2), (1, 1)),      # stacked taps
+    (2, 16, 13, 24, 136, 3, 5, (2, 1), (1, 2), (1, 1)),     # two channel tiles, row stride 2
+    (1, 24, 12, 16, 96, 3, 3, (1, 2), (3, 1), (2, 3)),      # padding and dilation together
 ]
 
 
