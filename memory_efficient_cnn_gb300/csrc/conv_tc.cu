@@ -712,10 +712,13 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 if (id < p.tiles_total) tile_at(p, id, t);
             }
         };
-        if (MODE == TAP_CH && p.vec && p.p_w > 0) {
-            // the 16-byte fills write only the slab columns of input columns: clear every
-            // stage once, so that the padding columns read as zero; all producers fence
-            // their clears and meet before any chunk is filled
+        if (CHAN && (p.stack || (MODE == TAP_CH && p.vec && p.p_w > 0))) {
+            // Entries that no fill writes must read as zero: with padding, the 16-byte
+            // fills skip the padding columns; with tap stacking, a group whose second tap
+            // is missing multiplies zero filter rows by the entries one column past the
+            // input's last (for the column after the last output), and whatever bytes an
+            // earlier kernel left there may decode as Inf or NaN. Every stage is cleared
+            // once; all producers fence their clears and meet before any chunk is filled.
             const int ptid = threadIdx.x - 64;
             const int n16 = (int)(p.BST * p.stage_b / 16);
             for (int i = ptid; i < n16; i += TAP_PROD_WARPS * 32)

@@ -175,3 +175,34 @@ def test_conv_nhwc_full_size_sampled(layer, dt):
                       what=f"{layer.name} {dt} nhwc fused={fused}")
         del out
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("layout", ["nchw", "nhwc"])
+@pytest.mark.parametrize("fused", [False, True], ids=["window", "fused"])
+def test_stacked_taps_ignore_what_earlier_kernels_left_in_shared_memory(layout, fused):
+    """With tap stacking (C_o <= 64) a group without a second tap multiplies zero
+    filter rows by slab entries past the input's last column, which no fill
+    writes. Convolutions of all-NaN inputs of wider shapes first leave NaN bit
+    patterns in the SMs' shared memory; the exact integer result must follow."""
+    cl = layout == "nhwc"
+    for wi in (40, 48, 64, 96):
+        xn = torch.full((2, 24, 30, wi), float("nan"), dtype=torch.float16)
+        wn = torch.ones((40, 24, 5, 3), dtype=torch.float16)
+        xn = _cl(xn) if cl else xn
+        if cl:
+            _run(xn, wn, (1, 2), fused)
+        else:
+            xd = xn.cuda()
+            mec.conv_fused(xd, wn.cuda(), (1, 2)) if fused else mec.conv(mec.transform(xd, 5, 1), wn.cuda(), (1, 2))
+    layer = wl.Layer("stale", 2, 24, 30, 33, 40, 5, 3, 1, 2, seed=5)
+    x, w = wl.make_int_inputs(layer, "f16", seed=31, x_range=1, w_range=1, density=0.5)
+    if cl:
+        x = _cl(x)
+        out = _run(x, w, (1, 2), fused)
+        want, _ = oracle.conv_direct_nhwc(to_f64(x), to_f64(w), (1, 2))
+    else:
+        xd = x.cuda()
+        out = (mec.conv_fused(xd, w.cuda(), (1, 2)) if fused
+               else mec.conv(mec.transform(xd, 5, 1), w.cuda(), (1, 2)))
+        want, _ = oracle.conv_direct(to_f64(x), to_f64(w), (1, 2))
+    np.testing.assert_array_equal(to_f64(out), want)
