@@ -328,7 +328,13 @@ constexpr int TAP_ISSUER1_WARP = 2 + TAP_PROD_WARPS + TAP_EPI_WARPS;  // the sec
 constexpr int TAP_THREADS = (3 + TAP_PROD_WARPS + TAP_EPI_WARPS) * 32;
 constexpr uint32_t TAP_A_BYTES = BM * 16 * 2;  // one K=16 tap of 128 channels: 4 KB
 constexpr int TAP_MAX_NT = 512;
-constexpr uint32_t TAP_EPI_BYTES = TAP_EPI_WARPS * 32 * 33 * 4;
+// Epilogue staging per warp: 64-column blocks of 32 x 33 words. Without tap
+// stacking a warp stages its whole share of an accumulator (two blocks) before
+// releasing it; the stacked drain goes one block at a time.
+constexpr int TAP_EPI_BLOCK_WORDS = 32 * 33;
+__host__ __device__ constexpr uint32_t tap_epi_bytes(int blocks) {
+    return (uint32_t)(TAP_EPI_WARPS * blocks * TAP_EPI_BLOCK_WORDS * 4);
+}
 
 struct TapParams {
     const uint16_t *src;   // NCHW input (CH, WX), window tensor (WW), NHWC input (CL)
@@ -374,6 +380,7 @@ struct TapParams {
     int Hfe;               // slab rows a filter spans: (H_f - 1)*dil_h + 1
     int Wp;                // slab columns
     int padded;            // p_h or p_w > 0: the producers zero-fill outside the input
+    int epi_blocks;        // staging blocks per epilogue warp (2, or 1 when stacked)
 };
 
 // A tile: output rows [ho0, ho0 + Q) of image n, output channels [mt*128, mt*128 + 128).
@@ -451,7 +458,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     uint16_t *sRaw = reinterpret_cast<uint16_t *>(sB + (size_t)p.BST * p.stage_b);
     uint32_t *sE = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(sRaw) +
                                                 ((size_t)p.raw_elems * 2 + 127) / 128 * 128);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sE) + TAP_EPI_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sE) + tap_epi_bytes(p.epi_blocks));
     // [A stages][slab stages][raw rows (W modes)][epilogue staging] then
     // bars: full_a[AST] | empty_a[AST] | full_b[BST] | empty_b[BST] | tmem_full[2] | tmem_empty[2]
     //       | drain | stacked hand-over: full[4] | empty[4]
@@ -958,7 +965,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         const int ew = warp - 2 - TAP_PROD_WARPS;  // 0..7
         const int q4 = warp & 3;                  // TMEM lane quarter this warp may read
         const int hh = ew >> 2;                   // which half of the columns
-        uint32_t *stage = sE + ew * (32 * 33);
+        const int warp_words = p.epi_blocks * TAP_EPI_BLOCK_WORDS;
+        uint32_t *stage = sE + ew * warp_words;
         const int64_t plane = (int64_t)p.H_o * p.W_o;
         int k = 0;
         uint32_t xk = 0;  // stacked hand-overs so far (the same count in both warps of a pair)
@@ -1000,15 +1008,35 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     // a block may reach past the range (into the other accumulator, which
                     // may still be accumulating): only columns of the range are stored
                     auto off_in = [&](int pp) -> int { return pp < ce ? off_of(pp) : -1; };
-                    if (p.nhwc)
-                        drain_columns<true>(taddr, cb, ce, stage, min(32, p.C_o - co0), ostride, p.bf16, out_c,
-                                            off_in);
-                    else
-                        drain_columns<false>(taddr, cb, ce, stage, min(32, p.C_o - co0), ostride, p.bf16, out_c,
-                                             off_in);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tmem_empty(a));
+                    const int rows = min(32, p.C_o - co0);
+                    if (p.epi_blocks == 2) {
+                        // the warp's share (at most two 64-column blocks) goes to its staging
+                        // area, the accumulator is released, then the stores run while the
+                        // next tile's MMAs use it
+                        if (p.nhwc)
+                            stage_columns<true>(taddr, cb, ce, stage, TAP_EPI_BLOCK_WORDS, p.bf16);
+                        else
+                            stage_columns<false>(taddr, cb, ce, stage, TAP_EPI_BLOCK_WORDS, p.bf16);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tmem_empty(a));
+                        for (int c0 = cb, bi = 0; c0 < ce; c0 += 64, ++bi) {
+                            const uint32_t *blk = stage + bi * TAP_EPI_BLOCK_WORDS;
+                            if (p.nhwc)
+                                store_block_cl(blk, c0, rows, ostride, out_c, off_in);
+                            else
+                                store_block(blk, c0, rows, ostride, out_c, off_in);
+                        }
+                        __syncwarp();
+                    } else {
+                        if (p.nhwc)
+                            drain_columns<true>(taddr, cb, ce, stage, rows, ostride, p.bf16, out_c, off_in);
+                        else
+                            drain_columns<false>(taddr, cb, ce, stage, rows, ostride, p.bf16, out_c, off_in);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tmem_empty(a));
+                    }
                 }
             } else {
                 // the shifted add reads one column across the accumulators' boundary:
@@ -1029,7 +1057,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     } else {
                         const int co0 = q4 * 32;
                         uint16_t *out_c = out_at(co0);
-                        const float *xbuf = reinterpret_cast<const float *>(sE + (ew - 2) * (32 * 33));
+                        const float *xbuf = reinterpret_cast<const float *>(sE + (ew - 2) * warp_words);
                         const int rows = max(0, min(32, p.C_o - co0));
                         if (p.nhwc)
                             ok = drain_stacked_upper<true>(taddr, cb, ce, stage, xbuf, xfull(pair), xempty(pair),
@@ -1164,7 +1192,7 @@ static double tile_cost(int64_t NT) {
 // SMs, or !ok: the tiling with the least modelled time among those whose slab
 // stages fit shared memory. Whether a plan exists, and its filter layout, do
 // not depend on `sms`.
-TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
+TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks) {
     TapPlan pl{};
     pl.ok = false;
     pl.mode = mode;
@@ -1259,7 +1287,7 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
             for (int BST : {3, 2}) {
               for (int AST : {3, 2, 4}) {
                     int64_t total = (int64_t)AST * tg * TAP_A_BYTES + BST * stage_b + raw_e * 2 +
-                                    TAP_EPI_BYTES + 512 + 4 * T + 16 + 128 * U;
+                                    tap_epi_bytes(epi_blocks) + 512 + 4 * T + 16 + 128 * U;
                     if (total > smem_max) continue;
                     // the 512-column TMEM accumulator needs the SM to itself
                     total = std::max<int64_t>(total, 120 * 1024);
@@ -1277,6 +1305,7 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
                     p.Hfe = (int)Hfe;
                     p.Wp = (int)Wp;
                     p.padded = (s.p_h > 0 || s.p_w > 0) ? 1 : 0;
+                    p.epi_blocks = epi_blocks;
                     p.TG = tg;
                     p.ntg = (int)((T + tg - 1) / tg);
                     p.Qmax = (int)Q;
@@ -1309,6 +1338,19 @@ TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
         }
     }
     return pl;
+}
+
+// Epilogue staging of two blocks per warp (release the accumulator before the
+// stores) when it costs the tiling nothing: the same rows per tile and filter
+// stages of at least min(T, 8) taps as with one block; one block otherwise, and
+// always with tap stacking (its drain goes block by block).
+TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
+    const TapPlan one = plan_tap_epi(s, mode, sms, 1);
+    if (!one.ok || one.p.stack) return one;
+    const TapPlan two = plan_tap_epi(s, mode, sms, 2);
+    const int need_tg = std::min(one.p.TG, 8);
+    if (two.ok && two.p.Qmax == one.p.Qmax && two.p.TG >= need_tg) return two;
+    return one;
 }
 
 struct ExpandGeom {

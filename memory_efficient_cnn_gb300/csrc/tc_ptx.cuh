@@ -327,6 +327,75 @@ __device__ __forceinline__ void store_block_cl(const uint32_t *stage, int c0, in
     }
 }
 
+// Stages TMEM columns [c_begin, c_end) of the warp's 32 accumulator lanes (at
+// most two 64-column blocks) into consecutive staging blocks of block_words
+// words each, rounded to fp16/bf16, in the layout store_block (NCHW) or
+// store_block_cl (CL) reads. The caller releases the accumulator afterwards and
+// stores the blocks from shared memory.
+template <bool CL>
+__device__ __forceinline__ void stage_columns(uint32_t taddr, int c_begin, int c_end, uint32_t *stage,
+                                              int block_words, int bf16) {
+    const int lane = threadIdx.x & 31;
+    if (c_begin >= c_end) return;
+    uint32_t r[32];
+    tmem_ld32(taddr + (uint32_t)c_begin, r);
+    for (int c0 = c_begin, bi = 0; c0 < c_end; c0 += 64, ++bi) {
+        uint32_t *blk = stage + bi * block_words;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tmem_wait_ld();
+            if (CL) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                stage_half_cl(blk, half, v, bf16);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    blk[lane * 33 + half * 16 + i] =
+                        pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), bf16);
+            }
+            const int nxt = half == 0 ? c0 + 32 : c0 + 64;
+            if (nxt < c_end) tmem_ld32(taddr + (uint32_t)nxt, r);
+        }
+    }
+    __syncwarp();
+}
+
+// Channels-last store of 32 columns straight from registers: lane l holds
+// channel l of columns c0 + i in v[i] (fp32 bit patterns). Lane pairs swap values with one shuffle
+// per two columns, so that the even lane of a pair holds channels (l, l+1) of
+// column c0 + 2i and the odd lane the same channels of column c0 + 2i + 1; each
+// store instruction then writes the warp's 32 channels of two columns as two
+// runs of 64 contiguous bytes. off_of(col) < 0: not an output; rows: channels
+// of the warp that exist; cstride: elements between positions (C_o). 4-byte
+// stores when cstride is even, else 2-byte.
+template <typename OffFn>
+__device__ __forceinline__ void store_half_cl(const uint32_t (&v)[32], int c0, int rows, int64_t cstride,
+                                              uint16_t *out_c, OffFn off_of, int bf16) {
+    const int lane = threadIdx.x & 31;
+    const bool odd = (lane & 1) != 0;
+    const int ch = lane & ~1;  // first channel of the lane's pair
+    const int o_mine = off_of(c0 + lane);
+    const bool pairs = (cstride & 1) == 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float a = __uint_as_float(v[2 * i]), b = __uint_as_float(v[2 * i + 1]);
+        const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+        const float lo = odd ? recv : a, hi = odd ? b : recv;
+        const int o = __shfl_sync(0xffffffffu, o_mine, 2 * i + (odd ? 1 : 0));
+        if (o < 0 || ch >= rows) continue;
+        uint16_t *d = out_c + (int64_t)o * cstride + ch;
+        const uint32_t w = pack2(lo, hi, bf16);
+        if (pairs && ch + 1 < rows) {
+            *reinterpret_cast<uint32_t *>(d) = w;
+        } else {
+            d[0] = (uint16_t)(w & 0xFFFFu);
+            if (ch + 1 < rows) d[1] = (uint16_t)(w >> 16);
+        }
+    }
+}
+
 // Faster drain for the tap kernels. The warp owns TMEM columns [c_begin,
 // c_end) of its 32 accumulator lanes (taddr = lane quarter base). Per block of
 // 64 columns: two 32-column TMEM loads (the next block's first load is in
@@ -401,7 +470,9 @@ __device__ __forceinline__ bool drain_stacked_lower(uint32_t taddr, int c_begin,
 }
 
 // Stacked drain, upper half: accumulator rows 0..63 plus the partner's shifted
-// values give the outputs; rounding, transpose and store as in drain_columns.
+// values give the outputs; rounding, transpose and store as in drain_columns,
+// except that channels-last outputs are stored from registers (store_half_cl),
+// which measured faster here than staging them.
 template <bool CL, typename OffFn>
 __device__ __forceinline__ bool drain_stacked_upper(uint32_t taddr, int c_begin, int c_end, uint32_t *stage,
                                                     const float *xbuf, uint32_t bar_full, uint32_t bar_empty,
@@ -416,10 +487,11 @@ __device__ __forceinline__ bool drain_stacked_upper(uint32_t taddr, int c_begin,
             tmem_wait_ld();
             if (!warp_bar_wait(bar_full, *k & 1, ctl, site)) return false;
             if (CL) {
-                float v[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + xbuf[lane * 33 + i];
-                stage_half_cl(stage, half, v, bf16);
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + xbuf[lane * 33 + i]);
+                mbar_arrive(bar_empty);  // the partner's buffer is read
+                store_half_cl(r, c0 + 32 * half, rows, row_stride, out_c, off_of, bf16);
+                continue;
             } else {
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
@@ -429,12 +501,11 @@ __device__ __forceinline__ bool drain_stacked_upper(uint32_t taddr, int c_begin,
             }
             mbar_arrive(bar_empty);
         }
-        __syncwarp();
-        if (CL)
-            store_block_cl(stage, c0, rows, row_stride, out_c, off_of);
-        else
+        if (!CL) {
+            __syncwarp();
             store_block(stage, c0, rows, row_stride, out_c, off_of);
-        __syncwarp();
+            __syncwarp();
+        }
     }
     return true;
 }
