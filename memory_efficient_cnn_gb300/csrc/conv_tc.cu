@@ -443,6 +443,11 @@ __device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.w
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
+// word i of v for a run-time i, by selects (no indexed registers)
+__device__ __forceinline__ uint32_t word_sel(const uint4 &v, int i) {
+    const uint32_t lo = (i & 1) ? v.y : v.x, hi = (i & 1) ? v.w : v.z;
+    return (i & 2) ? hi : lo;
+}
 
 // Persistent: one CTA per SM, each owning an equal share of the output rows.
 // Warp 0 issues the MMAs, warp 1 streams filter tiles, warps 2..9 fill the
@@ -866,20 +871,26 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                         uint8_t *rowp = slab + (size_t)c8 * p.lbo + (size_t)((lr - lq * p.s_h) * p.s_w) * p.PB +
                                         (size_t)(lq * p.pitch) * 16;
                         // input column cg*8 + kk is slab column col = p_w + cg*8 + kk, in phase
-                        // block (col % s_w) at entry col / s_w
-                        int cq = (int)fdiv((uint32_t)(cg * 8 + p.p_w), p.div_sw);
-                        int cph = cg * 8 + p.p_w - cq * p.s_w;
+                        // block (col % s_w) at entry col / s_w. The lanes of a warp hold
+                        // column groups 8 entries (128 bytes) apart, so lane l writes its
+                        // entries starting at kk = l % 8: the 8 lanes of a group then store to
+                        // 8 different bank groups instead of one.
+                        const int rot = threadIdx.x & 7;
+                        const int col0 = cg * 8 + p.p_w;
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
+                        for (int st = 0; st < 8; ++st) {
+                            const int kk = (st + rot) & 7;
                             const uint32_t sel = (kk & 1) ? 0x7632u : 0x5410u;
                             const int wd = kk >> 1;
-                            const uint32_t w0 = __byte_perm(word_of(v[0], wd), word_of(v[1], wd), sel);
-                            const uint32_t w1 = __byte_perm(word_of(v[2], wd), word_of(v[3], wd), sel);
-                            const uint32_t w2 = __byte_perm(word_of(v[4], wd), word_of(v[5], wd), sel);
-                            const uint32_t w3 = __byte_perm(word_of(v[6], wd), word_of(v[7], wd), sel);
+                            const uint32_t w0 = __byte_perm(word_sel(v[0], wd), word_sel(v[1], wd), sel);
+                            const uint32_t w1 = __byte_perm(word_sel(v[2], wd), word_sel(v[3], wd), sel);
+                            const uint32_t w2 = __byte_perm(word_sel(v[4], wd), word_sel(v[5], wd), sel);
+                            const uint32_t w3 = __byte_perm(word_sel(v[6], wd), word_sel(v[7], wd), sel);
+                            const int col = col0 + kk;
+                            const int cq = (int)fdiv((uint32_t)col, p.div_sw);
+                            const int cph = col - cq * p.s_w;
                             uint8_t *dst = rowp + (size_t)cph * p.PB + (size_t)cq * 16;
                             *reinterpret_cast<uint4 *>(dst) = make_uint4(w0, w1, w2, w3);
-                            if (++cph == p.s_w) { cph = 0; ++cq; }
                         }
                     }
                 } else {
