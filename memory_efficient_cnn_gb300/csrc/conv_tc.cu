@@ -538,8 +538,11 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
     const Ctl ctl{reinterpret_cast<volatile int *>(abort_word), p.status};
-    // the filter tiles and the cleared status word come from the re-layout kernel
-    grid_dependency_wait();
+    // Only the filter loader reads what the re-layout kernel writes (the filter
+    // tiles); it alone waits for that kernel, so the prologue and the first slab
+    // fills overlap it. (The re-layout kernel also clears the status word, in
+    // microseconds; a wait gives up only after seconds.) Everything earlier in
+    // the stream is complete: the re-layout kernel started after it.
 
     if (warp == 0 || warp == TAP_ISSUER1_WARP) {
         // ---------------- MMA issuers
@@ -616,6 +619,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     } else if (warp == 1) {
         // ---------------- filter loader
         if (lane == 0) {
+            grid_dependency_wait();
             int issued = 0;
             bool ok = true;
             TapTile tl;
