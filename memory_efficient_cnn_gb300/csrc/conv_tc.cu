@@ -466,8 +466,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sE) + tap_epi_bytes(p.epi_blocks));
     // [A stages][slab stages][raw rows (W modes)][epilogue staging] then
     // bars: full_a[AST] | empty_a[AST] | full_b[BST] | empty_b[BST] | tmem_full[2] | tmem_empty[2]
-    //       | drain | stacked hand-over: full[4] | empty[4]
-    const int nb = 2 * p.AST + 2 * p.BST + 5 + 8;
+    //       | drain | stacked hand-over: full[4] | empty[4] | raw slot full[2]
+    const int nb = 2 * p.AST + 2 * p.BST + 5 + 8 + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + nb);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
     uint32_t *toff = reinterpret_cast<uint32_t *>(bars + nb + 1);  // [T] tap offsets (16-byte units)
@@ -505,6 +505,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     const uint32_t drain = smem_u32(bars + 2 * p.AST + 2 * p.BST + 4);
     auto xfull = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 5 + i); };
     auto xempty = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 9 + i); };
+    // TAP_CH with a raw ring: the bulk copies of a slot complete here
+    auto raw_full = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 13 + i); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.AST; ++s) {
@@ -526,6 +528,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             mbar_init(xfull(i), 32);
             mbar_init(xempty(i), 32);
         }
+        for (int i = 0; i < 2; ++i) mbar_init(raw_full(i), 1);
         *abort_word = 0;
         fence_mbar_init();
     }
@@ -679,25 +682,43 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         auto issue_raw = [&](const TapTile &t, int cc, int slot) {
             const uint32_t dst0 = smem_u32(sRaw + (size_t)slot * p.raw_slot);
             if (MODE == TAP_CH) {
-                // raw row lr is input row ho0*s_h - p_h + lr (zero-filled outside the input)
+                // Raw row lr of channel k is input row ho0*s_h - p_h + lr of channel
+                // cc*16 + k. The rows that exist are one contiguous, 16-byte aligned range
+                // of each channel plane: one bulk copy per channel, completing on the
+                // slot's barrier. Rows outside the input and channels past C_i are
+                // zeroed by the group's threads (the group's barrier orders them).
                 const int rows = (t.Q - 1) * p.s_h + p.Hfe;
-                const int cgs = p.W_i / 8;
-                const int vpc = rows * cgs;  // 16-byte vectors per channel
                 const int64_t plane = (int64_t)p.H_i * p.W_i;
-                const uint16_t *xb = p.src + (int64_t)t.n * p.C_i * plane;
                 const int hb = t.ho0 * p.s_h - p.p_h;
-                const bool full = t.Q == p.Qmax;
-                for (int v = pt; v < 16 * vpc; v += NPT) {
-                    const int k = full ? (int)fdiv((uint32_t)v, p.div_vpc) : v / vpc;
-                    const int i = v - k * vpc;
-                    const int lr = (int)fdiv((uint32_t)i, p.div_cgs);
-                    const int h = hb + lr;
-                    const int ci = cc * 16 + k;
-                    const bool ok = ci < p.C_i && (unsigned)h < (unsigned)p.H_i;
-                    cp_async16z(dst0 + (uint32_t)(k * p.raw_ch + i * 8) * 2,
-                                ok ? (const void *)(xb + (int64_t)ci * plane + (int64_t)h * p.W_i + (i - lr * cgs) * 8)
-                                   : (const void *)p.src,
-                                ok ? 16u : 0u);
+                const int r0 = max(0, -hb), r1 = min(rows, p.H_i - hb);
+                const int nch = min(16, p.C_i - cc * 16);
+                const uint32_t row_bytes = (uint32_t)p.W_i * 2;
+                const uint32_t ch_bytes = r1 > r0 ? (uint32_t)(r1 - r0) * row_bytes : 0u;
+                if (pt == 0) {
+                    const uint32_t bar = raw_full(slot);
+                    if (ch_bytes > 0 && nch > 0) {
+                        mbar_arrive_expect_tx(bar, ch_bytes * (uint32_t)nch);
+                        const uint16_t *x0 = p.src + ((int64_t)t.n * p.C_i + cc * 16) * plane +
+                                             (int64_t)(hb + r0) * p.W_i;
+                        for (int k = 0; k < nch; ++k)
+                            bulk_g2s(dst0 + (uint32_t)(k * p.raw_ch + r0 * p.W_i) * 2, x0 + (int64_t)k * plane,
+                                     ch_bytes, bar);
+                    } else {
+                        mbar_arrive(bar);
+                    }
+                }
+                if (r0 > 0 || r1 < rows || nch < 16) {
+                    // zero rows [0, r0) and [r1, rows) of the channels that exist, every row of
+                    // the channels that do not (16-byte stores)
+                    const int vpr = p.W_i / 8;  // vectors per row
+                    const int nv = 16 * rows * vpr;
+                    uint4 *raw16 = reinterpret_cast<uint4 *>(sRaw + (size_t)slot * p.raw_slot);
+                    for (int v = pt; v < nv; v += NPT) {
+                        const int k = v / (rows * vpr);
+                        const int lr = (v - k * rows * vpr) / vpr;
+                        if (k >= nch || lr < r0 || lr >= r1)
+                            raw16[(k * p.raw_ch + lr * p.W_i) / 8 + (v % vpr)] = make_uint4(0, 0, 0, 0);
+                    }
                 }
             } else {
                 int64_t g0, cnt, total;
@@ -745,8 +766,15 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         int64_t id = blockIdx.x;
         int cc = 0;
         TapTile tl;
+        // TAP_CH raw ring: parity of each slot's next completion, and whether a copy
+        // into it is outstanding
+        uint32_t raw_ph[2] = {0u, 0u};
+        bool raw_issued[2] = {false, false};
         if (id < p.tiles_total) tile_at(p, id, tl);
-        if (prefetch && id < p.tiles_total) issue_raw(tl, cc, 0);
+        if (prefetch && id < p.tiles_total) {
+            issue_raw(tl, cc, 0);
+            raw_issued[0] = true;
+        }
         cp_async_commit_group();
         for (int g = 0; id < p.tiles_total; ++g, next_chunk(id, cc, tl)) {
             // slab stage of chunk g, advanced for every chunk
@@ -761,14 +789,40 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 int cc2 = cc;
                 TapTile t2 = tl;
                 next_chunk(id2, cc2, t2);
-                if (pok && id2 < p.tiles_total) issue_raw(t2, cc2, slot ^ 1);
+                if (pok && id2 < p.tiles_total) {
+                    issue_raw(t2, cc2, slot ^ 1);
+                    raw_issued[slot ^ 1] = true;
+                }
                 cp_async_commit_group();
-                cp_async_wait_group<1>();
+                if (MODE == TAP_CH) {
+                    if (raw_issued[slot] && pok) {
+                        pok = warp_bar_wait(raw_full(slot), raw_ph[slot], ctl, SITE_RAW);
+                        if (pok) {
+                            raw_ph[slot] ^= 1u;
+                            raw_issued[slot] = false;
+                        }
+                    }
+                } else {
+                    cp_async_wait_group<1>();
+                }
                 asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(NPT) : "memory");
             } else if (staged) {
-                if (pok) issue_raw(tl, cc, slot);
+                if (pok) {
+                    issue_raw(tl, cc, slot);
+                    raw_issued[slot] = true;
+                }
                 cp_async_commit_group();
-                cp_async_wait_group<0>();
+                if (MODE == TAP_CH) {
+                    if (pok) {
+                        pok = warp_bar_wait(raw_full(slot), raw_ph[slot], ctl, SITE_RAW);
+                        if (pok) {
+                            raw_ph[slot] ^= 1u;
+                            raw_issued[slot] = false;
+                        }
+                    }
+                } else {
+                    cp_async_wait_group<0>();
+                }
                 asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(NPT) : "memory");
             }
             const int n = tl.n, ho0 = tl.ho0, Q = tl.Q;
@@ -975,6 +1029,11 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         }
         cp_async_commit_group();
         cp_async_wait_group<0>();
+        // bulk copies still in flight (an aborted wait) land before the CTA exits
+        if (MODE == TAP_CH) {
+            for (int s2 = 0; s2 < 2; ++s2)
+                if (raw_issued[s2]) bar_wait(raw_full(s2), raw_ph[s2], ctl, SITE_DRAIN, false);
+        }
     } else {
         // ---------------- epilogue: TMEM -> registers -> smem transpose -> coalesced stores
         const int ew = warp - 2 - TAP_PROD_WARPS;  // 0..7

@@ -145,7 +145,7 @@ __host__ __device__ inline uint32_t make_idesc(bool bf16, int M, int N) {
 }
 
 enum WaitSite : uint32_t { SITE_FULL_A = 1, SITE_FULL_B, SITE_EMPTY_MMA, SITE_EMPTY_LOAD,
-                           SITE_EMPTY_PROD, SITE_DONE, SITE_DRAIN, SITE_STACK };
+                           SITE_EMPTY_PROD, SITE_DONE, SITE_DRAIN, SITE_STACK, SITE_RAW };
 
 struct Ctl {
     volatile int *abort_flag;
