@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     const uint32_t drain = smem_u32(bars + 2 * p.AST + 2 * p.BST + 4);
     auto xfull = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 5 + i); };
     auto xempty = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 9 + i); };
-    // TAP_CH with a raw ring: the bulk copies of a slot complete here
+    // raw staging slots (TAP_CH ring, TAP_WX, TAP_WW): their bulk copies complete here
     auto raw_full = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 13 + i); };
 
     if (threadIdx.x == 0) {
@@ -731,14 +731,29 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     cnt = (int64_t)t.Q * p.L;
                     total = p.win_elems;
                 }
+                // the rows are one contiguous range of the source: one bulk copy of the
+                // 16-byte vectors that lie wholly inside it, completing on the slot's
+                // barrier; a partial last vector (the source's end) is copied by hand
                 const int lead = (int)(g0 & 7);
                 const int64_t base = g0 - lead;
                 const int nvec = (int)((lead + cnt + 7) / 8);
-                for (int v = pt; v < nvec; v += NPT) {
-                    const int64_t gg = base + (int64_t)v * 8;
-                    const int64_t left = total - gg;
-                    const uint32_t bytes = left >= 8 ? 16u : left > 0 ? (uint32_t)left * 2u : 0u;
-                    cp_async16z(dst0 + (uint32_t)v * 16, bytes ? (const void *)(p.src + gg) : (const void *)p.src, bytes);
+                const int64_t inside = (total - base) / 8;
+                const int nfull = inside < (int64_t)nvec ? (int)inside : nvec;
+                if (pt == 0) {
+                    const uint32_t bar = raw_full(slot);
+                    if (nfull > 0) {
+                        mbar_arrive_expect_tx(bar, (uint32_t)nfull * 16u);
+                        bulk_g2s(dst0, p.src + base, (uint32_t)nfull * 16u, bar);
+                    } else {
+                        mbar_arrive(bar);
+                    }
+                }
+                if (nfull < nvec && pt == NPT - 1) {
+                    uint16_t *d = sRaw + (size_t)slot * p.raw_slot + (size_t)nfull * 8;
+                    for (int e = 0; e < 8; ++e) {
+                        const int64_t gg = base + (int64_t)nfull * 8 + e;
+                        d[e] = gg < total ? p.src[gg] : (uint16_t)0;
+                    }
                 }
             }
         };
@@ -766,8 +781,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         int64_t id = blockIdx.x;
         int cc = 0;
         TapTile tl;
-        // TAP_CH raw ring: parity of each slot's next completion, and whether a copy
-        // into it is outstanding
+        // raw staging (TAP_CH ring, TAP_WX, TAP_WW): parity of each slot's next
+        // completion, and whether a bulk copy into it is outstanding
         uint32_t raw_ph[2] = {0u, 0u};
         bool raw_issued[2] = {false, false};
         if (id < p.tiles_total) tile_at(p, id, tl);
@@ -794,7 +809,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     raw_issued[slot ^ 1] = true;
                 }
                 cp_async_commit_group();
-                if (MODE == TAP_CH) {
+                if (MODE != TAP_CL) {
                     if (raw_issued[slot] && pok) {
                         pok = warp_bar_wait(raw_full(slot), raw_ph[slot], ctl, SITE_RAW);
                         if (pok) {
@@ -812,7 +827,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     raw_issued[slot] = true;
                 }
                 cp_async_commit_group();
-                if (MODE == TAP_CH) {
+                if (MODE != TAP_CL) {
                     if (pok) {
                         pok = warp_bar_wait(raw_full(slot), raw_ph[slot], ctl, SITE_RAW);
                         if (pok) {
@@ -1030,7 +1045,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         cp_async_commit_group();
         cp_async_wait_group<0>();
         // bulk copies still in flight (an aborted wait) land before the CTA exits
-        if (MODE == TAP_CH) {
+        if (MODE != TAP_CL) {
             for (int s2 = 0; s2 < 2; ++s2)
                 if (raw_issued[s2]) bar_wait(raw_full(s2), raw_ph[s2], ctl, SITE_DRAIN, false);
         }
