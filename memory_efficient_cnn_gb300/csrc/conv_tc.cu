@@ -9,8 +9,11 @@
 // A = filt' (M = 128 output channels per tile), B[p][(ci, k)] = the pixel's
 // contiguous window segment of channel ci (N = 256 pixels per tile).
 //
-// This file holds the "expand" kernel: every pipeline stage covers 64 values
-// of K; producer warps gather, for each of the tile's 256 pixels, its 64
+// This file holds two kernel families. The tap kernels (second half of the
+// file) run every shape a tiling exists for, in both layouts and with padding
+// and dilation. The "expand" kernel is the NCHW fallback for the rest: every
+// pipeline stage covers 64 values of K; producer warps gather, for each of the
+// tile's 256 pixels, its 64
 // window values of the stage (im2win order) into the canonical K-major
 // operand layout in shared memory, reading either the window tensor (the
 // two-step path) or the NCHW input directly (the fused path, which then never
@@ -300,6 +303,10 @@ __global__ void relayout_filter_expand(const uint16_t *__restrict__ filt, uint16
 // K = 16) is issued per tap and half tile; positions whose column is >= W_o are
 // computed and discarded. Filter tiles arrive per (chunk, group of taps) by
 // bulk copy, pre-laid by a re-layout kernel as [tap][co group][K half][8 co][8 K].
+// Raw source rows, where a staging ring exists, arrive by bulk copies too.
+// The channel modes also take zero padding (the slab spans the padded width;
+// producers zero-fill outside the input) and dilation (tap (r, j) reads slab
+// row r*d_h, column j*d_w); TAP_CL is the channel mode on channels-last input.
 // =========================================================================
 // TAP_CL (channels-last input, C_i a multiple of 8): the slab of TAP_CH, whose
 // 16-byte entries (8 channels of one input position) are 16 contiguous bytes of
@@ -357,7 +364,7 @@ struct TapParams {
     int64_t win_elems;     // WW: elements of the window tensor
     int N_img;             // images (bound of the staged reads)
     int raw_elems;         // elements of the raw staging area (all slots)
-    int ring;              // 1: raw chunks staged by cp.async two deep (next chunk in flight)
+    int ring;              // 1: raw chunks staged two deep (next chunk's bulk copy in flight)
     int raw_slot;          // elements of one raw slot (a multiple of 64)
     int raw_ch;            // CH with ring: elements per channel in a slot (rows x W_i)
     uint32_t stage_b;      // bytes of one slab stage
@@ -653,14 +660,16 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         // ---------------- slab producers
         // Chunks are walked in order (tile by tile, NCH per tile). Their source rows
         // are contiguous in global memory; where a raw staging area exists they are
-        // copied there by cp.async and the slab is built from shared memory. Without
-        // one (TAP_CH whose rows are not 16-byte aligned, or whose staging does not
-        // fit) the slab is gathered straight from global memory. For TAP_CH with a raw
-        // ring or with tap stacking a chunk's fill is mostly latency (copy, barriers,
-        // shared-memory round trips), so the producers form two groups of four warps
-        // that fill alternate chunks at the same time, each with its own raw slot and
-        // named barrier. Otherwise all eight warps fill every chunk, and with two raw
-        // slots the next chunk's copy is in flight while this one is re-laid.
+        // copied there by bulk copies (completing on the slot's barrier) and the slab
+        // is built from shared memory. Without one (TAP_CH whose rows are not 16-byte
+        // aligned, or whose staging does not fit) the slab is gathered straight from
+        // global memory; TAP_CL copies its entries with cp.async. For TAP_CH with a
+        // raw ring or with tap stacking a chunk's fill is mostly latency (copy,
+        // barriers, shared-memory round trips), so the producers form two groups of
+        // four warps that fill alternate chunks at the same time, each with its own
+        // raw slot and named barrier. Otherwise all eight warps fill every chunk, and
+        // with two raw slots the next chunk's copy is in flight while this one is
+        // re-laid.
         const bool staged = !CHAN || (MODE == TAP_CH && p.ring);
         const int ngroups = (MODE == TAP_CH && (p.ring || p.stack)) ? 2 : 1;
         const bool prefetch = ngroups == 1 && staged && p.ring;
@@ -790,7 +799,6 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             issue_raw(tl, cc, 0);
             raw_issued[0] = true;
         }
-        cp_async_commit_group();
         for (int g = 0; id < p.tiles_total; ++g, next_chunk(id, cc, tl)) {
             // slab stage of chunk g, advanced for every chunk
             const int sb_g = sb;
@@ -808,17 +816,12 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     issue_raw(t2, cc2, slot ^ 1);
                     raw_issued[slot ^ 1] = true;
                 }
-                cp_async_commit_group();
-                if (MODE != TAP_CL) {
-                    if (raw_issued[slot] && pok) {
-                        pok = warp_bar_wait(raw_full(slot), raw_ph[slot], ctl, SITE_RAW);
-                        if (pok) {
-                            raw_ph[slot] ^= 1u;
-                            raw_issued[slot] = false;
-                        }
+                if (raw_issued[slot] && pok) {
+                    pok = warp_bar_wait(raw_full(slot), raw_ph[slot], ctl, SITE_RAW);
+                    if (pok) {
+                        raw_ph[slot] ^= 1u;
+                        raw_issued[slot] = false;
                     }
-                } else {
-                    cp_async_wait_group<1>();
                 }
                 asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(NPT) : "memory");
             } else if (staged) {
@@ -826,17 +829,12 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     issue_raw(tl, cc, slot);
                     raw_issued[slot] = true;
                 }
-                cp_async_commit_group();
-                if (MODE != TAP_CL) {
+                if (pok) {
+                    pok = warp_bar_wait(raw_full(slot), raw_ph[slot], ctl, SITE_RAW);
                     if (pok) {
-                        pok = warp_bar_wait(raw_full(slot), raw_ph[slot], ctl, SITE_RAW);
-                        if (pok) {
-                            raw_ph[slot] ^= 1u;
-                            raw_issued[slot] = false;
-                        }
+                        raw_ph[slot] ^= 1u;
+                        raw_issued[slot] = false;
                     }
-                } else {
-                    cp_async_wait_group<0>();
                 }
                 asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(NPT) : "memory");
             }
