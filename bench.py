@@ -241,6 +241,9 @@ def main():
                     help="seconds of oracle time for the cpu_baseline (0 disables it)")
     ap.add_argument("--layout", choices=["nchw", "nhwc"], default="nchw",
                     help="tensor layout of input, window tensor and output")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="images per step (default: the layer's batch); smaller batches keep "
+                         "profiler captures small")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -251,6 +254,11 @@ def main():
     if args.layer not in layers:
         ap.error(f"--layer must be one of {sorted(layers)}")
     layer = layers[args.layer]
+    if args.batch < 0:
+        ap.error("--batch must be positive")
+    batch_changed = args.batch > 0 and args.batch != layer.N
+    if batch_changed:
+        layer = layer.with_batch(args.batch)
     rank, world, local = _dist()
     if args.impl == "reference":
         run_reference(args, layer, rank, world)
@@ -489,7 +497,8 @@ def main():
         workspace[f"im2col_{d}"] = col_b[d]
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     dk = kernels[dom]
-    traffic = DRAM_TRAFFIC.get((layer.name, dom))
+    # the captured traffic is that of the layer's own batch
+    traffic = None if batch_changed else DRAM_TRAFFIC.get((layer.name, dom))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

@@ -532,8 +532,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         }
         mbar_init(drain, 2);
         for (int i = 0; i < 4; ++i) {
-            mbar_init(xfull(i), 32);
-            mbar_init(xempty(i), 32);
+            mbar_init(xfull(i), 1);  // lane 0 of the writing / reading warp
+            mbar_init(xempty(i), 1);
         }
         for (int i = 0; i < 2; ++i) mbar_init(raw_full(i), 1);
         *abort_word = 0;

@@ -444,10 +444,11 @@ __device__ __forceinline__ void drain_columns(uint32_t taddr, int c_begin, int c
 // (the second tap of each stacked group) and hands, per 32-column half block
 // starting at column c, the fp32 values of columns c+1 .. c+32 to its partner
 // through xbuf (32 rows x 33 words). Hand-over number k (counted over the whole
-// kernel in *k, identically by both warps) completes phase k of bar_full (32
-// arrivals: every lane releases its own writes); xbuf is reused once phase k-1
-// of bar_empty (the partner's 32 arrivals) has completed. Waits are bounded;
-// false means the CTA aborted.
+// kernel in *k, identically by both warps) completes phase k of bar_full; xbuf
+// is reused once phase k-1 of bar_empty has completed. Each side signals with
+// one arrival by lane 0 after a warp barrier, which orders every lane's shared
+// memory accesses before it (one arrival measured faster than 32). Waits are
+// bounded; false means the CTA aborted.
 __device__ __forceinline__ bool drain_stacked_lower(uint32_t taddr, int c_begin, int c_end, float *xbuf,
                                                     uint32_t bar_full, uint32_t bar_empty, uint32_t *k,
                                                     const Ctl &ctl, uint32_t site) {
@@ -463,7 +464,8 @@ __device__ __forceinline__ bool drain_stacked_lower(uint32_t taddr, int c_begin,
 #pragma unroll
             for (int i = 0; i < 31; ++i) xbuf[lane * 33 + i] = __uint_as_float(r[i + 1]);
             xbuf[lane * 33 + 31] = __uint_as_float(extra);
-            mbar_arrive(bar_full);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_full);
         }
     }
     return true;
@@ -486,20 +488,18 @@ __device__ __forceinline__ bool drain_stacked_upper(uint32_t taddr, int c_begin,
             tmem_ld32(taddr + (uint32_t)(c0 + 32 * half), r);
             tmem_wait_ld();
             if (!warp_bar_wait(bar_full, *k & 1, ctl, site)) return false;
-            if (CL) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + xbuf[lane * 33 + i]);
-                mbar_arrive(bar_empty);  // the partner's buffer is read
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + xbuf[lane * 33 + i]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty);  // the partner's buffer is read
+            if (CL) {
                 store_half_cl(r, c0 + 32 * half, rows, row_stride, out_c, off_of, bf16);
-                continue;
             } else {
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     stage[lane * 33 + half * 16 + i] =
-                        pack2(__uint_as_float(r[2 * i]) + xbuf[lane * 33 + 2 * i],
-                              __uint_as_float(r[2 * i + 1]) + xbuf[lane * 33 + 2 * i + 1], bf16);
+                        pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), bf16);
             }
-            mbar_arrive(bar_empty);
         }
         if (!CL) {
             __syncwarp();
