@@ -33,6 +33,10 @@ CASES = [  # N, C_i, H_i, W_i, H_f, s_h
     (1, 2, 6, 12000, 3, 2),  # one output row of input exceeds the default band budget
     # many small planes: several whole planes per CTA, the last group ragged
     (64, 64, 11, 13, 3, 2), (27, 113, 7, 9, 2, 1),
+    # rows of whole 16-byte vectors (16-bit: staged as vertical pairs): bands of a tall
+    # plane, H_f >= 8, H_f = 1, many planes per CTA, stride = H_f, one output row
+    (1, 3, 200, 64, 7, 1), (2, 4, 30, 16, 11, 3), (3, 5, 10, 8, 1, 1), (64, 32, 12, 8, 2, 2),
+    (1, 2, 50, 96, 4, 4), (2, 3, 9, 40, 9, 1),
 ]
 
 
@@ -51,11 +55,12 @@ def test_transform_empty_batch_is_a_noop():
     assert win.shape == (0, 3, 6, 24)
 
 
-def test_transform_does_not_write_past_the_window():
-    x = torch.randn(2, 3, 31, 227, dtype=torch.float16)
+@pytest.mark.parametrize("W_i", [227, 64])
+def test_transform_does_not_write_past_the_window(W_i):
+    x = torch.randn(2, 3, 31, W_i, dtype=torch.float16)
     H_f, s_h = 11, 4
     H_o = (31 - H_f) // s_h + 1
-    n = 2 * 3 * H_o * 227 * H_f
+    n = 2 * 3 * H_o * W_i * H_f
     buf = torch.full((n + 64,), 7, dtype=torch.float16, device="cuda")
     mec.im2win_transform(x.cuda(), buf, 1, H_f, 1, s_h, 1)
     torch.cuda.synchronize()
