@@ -172,6 +172,17 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
             }
 #pragma unroll
             for (int i = 0; i < V; ++i) e[i] = (uint32_t)sl[top + o[i]];
+        } else if (!TABLE && H_f >= V && w * H_f + r + V <= Lw) {
+            // H_f >= V and one window row: the vector is the rest of column w and at
+            // most the start of column w + 1, so its elements' staged indices are
+            // independent of one another
+            const int top = idx - r * Wc;
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int t = r + i;
+                const int c = t >= H_f ? 1 : 0;
+                e[i] = (uint32_t)sl[top + (t - c * H_f) * Wc + c];
+            }
         } else {
 #pragma unroll
             for (int i = 0; i < V; ++i) {
