@@ -176,13 +176,13 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
             // H_f >= V and one window row: the vector is the rest of column w and at
             // most the start of column w + 1, so its elements' staged indices are
             // independent of one another
-            const int top = idx - r * Wc;
+            // element i: idx + i*Wc in column w, or that minus (H_f*Wc - 1) once
+            // r + i reaches the next column
+            const int wrap = H_f * Wc - 1;
+            const int th = H_f - r;
+            const E *s0 = sl + idx;
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
-                const int t = r + i;
-                const int c = t >= H_f ? 1 : 0;
-                e[i] = (uint32_t)sl[top + (t - c * H_f) * Wc + c];
-            }
+            for (int i = 0; i < V; ++i) e[i] = (uint32_t)s0[i * Wc - (i >= th ? wrap : 0)];
         } else {
 #pragma unroll
             for (int i = 0; i < V; ++i) {
@@ -202,8 +202,8 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
         }
         uint4 out;
         if (V == 8) {
-            out = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16),
-                             e[6] | (e[7] << 16));
+            out = make_uint4(__byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410),
+                             __byte_perm(e[4], e[5], 0x5410), __byte_perm(e[6], e[7], 0x5410));
         } else {
             out = make_uint4(e[0], e[1], e[2], e[3]);
         }
