@@ -241,24 +241,45 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
         if (c < nchunks) issue_chunk(c);
         cp_async_commit();
     }
+    // k values of the last chunk (the rest of it is the filter's zero padding);
+    // the 128-channel tile, whose registers are capped at 128, always runs whole
+    // chunks (a separate short loop makes it spill)
+    const int k_last = TM == 128 ? KC : p.K - (nchunks - 1) * KC;
     for (int c = 0; c < nchunks; ++c) {
         cp_async_wait<STAGES - 2>();  // chunk c has landed (this thread's copies)
         __syncthreads();              // ... and every thread's; chunk c-1's buffer is free
         if (c + STAGES - 1 < nchunks) issue_chunk(c + STAGES - 1);
         cp_async_commit();
         const int buf = c % STAGES;
+        if (TM == 128 || c + 1 < nchunks || k_last == KC) {
 #pragma unroll
-        for (int k = 0; k < KC; ++k) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][k][tx * 4]);
-            const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][k][64 + tx * 4]);
-            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8]);
-            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8 + 4]);
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            for (int k = 0; k < KC; ++k) {
+                const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][k][tx * 4]);
+                const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][k][64 + tx * 4]);
+                const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8]);
+                const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8 + 4]);
+                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(bv[i], av[j], acc[i][j]);
+                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(bv[i], av[j], acc[i][j]);
+            }
+        } else {
+            // the same k steps, only the k_last that are not padding
+#pragma unroll 1
+            for (int k = 0; k < k_last; ++k) {
+                const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][k][tx * 4]);
+                const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][k][64 + tx * 4]);
+                const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8]);
+                const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8 + 4]);
+                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(bv[i], av[j], acc[i][j]);
+            }
         }
     }
     cp_async_wait<0>();
