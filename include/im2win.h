@@ -224,6 +224,46 @@ im2win_status im2win_conv_fused_ex(const void *x, const void *filt, void *out, v
                                    int64_t W_f, int64_t s_h, int64_t s_w, int64_t p_h, int64_t p_w, int64_t d_h,
                                    int64_t d_w, int layout, int dtype, void *stream);
 
+/*
+ * Plan query (host only: no GPU work, usable without a device). Reports which
+ * kernel a convolution call with these arguments would launch and, for the
+ * tensor-core tap kernel, its tiling. op is IM2WIN_OP_CONV (from the window
+ * tensor) or IM2WIN_OP_CONV_FUSED; the shape, padding, dilation, layout and
+ * dtype are those of im2win_conv_ex / im2win_conv_fused_ex; sms is the SM count
+ * the persistent grid is planned for, or <= 0 for the current device's (148
+ * when no device is visible). Returns INVALID_ARG or UNSUPPORTED where the call
+ * would, else fills *info (every field zero where it does not apply).
+ */
+typedef enum {
+    IM2WIN_KERNEL_F32 = 0,      /* fp32 CUDA-core convolution */
+    IM2WIN_KERNEL_TAP = 1,      /* tensor-core tap kernel (tcgen05, persistent) */
+    IM2WIN_KERNEL_EXPAND = 2    /* tensor-core expand kernel (fallback, NCHW without padding) */
+} im2win_kernel;
+
+typedef struct {
+    int32_t kernel;             /* im2win_kernel */
+    int32_t tap_mode;           /* tap kernel: 0 channel slab (NCHW input, or window tensor read as an
+                                   input), 1 window rows of one channel from the input, 2 window rows
+                                   from the window tensor, 3 channel slab of a channels-last tensor;
+                                   -1 for the other kernels */
+    int32_t stacked;            /* 1: two filter taps per MMA along M (C_o <= 64) */
+    int32_t rows_per_tile;      /* output rows per tile */
+    int32_t pitch;              /* accumulator columns per output row */
+    int32_t tmem_columns;       /* accumulator columns of the widest tile (<= 512) */
+    int32_t tmem_read_end;      /* one past the highest accumulator column the epilogue reads */
+    int32_t smem_bytes;         /* dynamic shared memory per CTA */
+    int32_t filter_stage_taps;  /* filter taps per shared-memory stage */
+    int32_t filter_stages;      /* filter stages */
+    int32_t slab_stages;        /* input slab stages */
+    int32_t reserved;
+    int64_t tiles;              /* tiles of the launch: N * ceil(C_o / 128) * ceil(H_o / rows_per_tile) */
+    int64_t grid;               /* CTAs launched: min(sms, tiles) */
+} im2win_plan_info;
+
+im2win_status im2win_plan(int op, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i, int64_t C_o,
+                          int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w, int64_t p_h, int64_t p_w,
+                          int64_t d_h, int64_t d_w, int layout, int dtype, int sms, im2win_plan_info *info);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *im2win_status_string(int status);
 

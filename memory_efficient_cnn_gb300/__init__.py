@@ -16,4 +16,5 @@ from ._binding import (  # noqa: F401
     im2win_transform, im2win_transform_nhwc,
     im2win_workspace_size, lib, library_path, out_hw, status_string, transform, transform_nhwc, workspace,
     NCHW, NHWC, conv_ex, conv_fused_ex, im2win_conv_ex, im2win_conv_fused_ex, im2win_transform_ex,
-    im2win_workspace_size_ex, out_hw_pd, transform_ex)
+    im2win_workspace_size_ex, out_hw_pd, transform_ex,
+    KERNEL_EXPAND, KERNEL_F32, KERNEL_TAP, PlanInfo, im2win_plan)

@@ -25,8 +25,18 @@ _DTYPE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 EXPORTS = ("im2win_workspace_size", "im2win_transform", "im2win_conv", "im2win_conv_fused",
            "im2win_status_string", "im2win_device_status", "im2win_conv_fused_noalloc",
            "im2win_transform_nhwc", "im2win_conv_nhwc", "im2win_conv_fused_nhwc",
-           "im2win_workspace_size_ex", "im2win_transform_ex", "im2win_conv_ex", "im2win_conv_fused_ex")
+           "im2win_workspace_size_ex", "im2win_transform_ex", "im2win_conv_ex", "im2win_conv_fused_ex",
+           "im2win_plan")
 NOALLOC_SCRATCH_BYTES = 16 << 20
+KERNEL_F32, KERNEL_TAP, KERNEL_EXPAND = 0, 1, 2
+
+
+class PlanInfo(ctypes.Structure):
+    """im2win_plan_info: the kernel and tiling a convolution call launches."""
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "kernel", "tap_mode", "stacked", "rows_per_tile", "pitch", "tmem_columns", "tmem_read_end",
+        "smem_bytes", "filter_stage_taps", "filter_stages", "slab_stages", "reserved")] + [
+        ("tiles", ctypes.c_int64), ("grid", ctypes.c_int64)]
 
 _lock = threading.Lock()
 _lib = None
@@ -71,11 +81,12 @@ def lib() -> ctypes.CDLL:
             L.im2win_transform_ex.argtypes = [vp, vp] + shp + pd + [vp]
             L.im2win_conv_ex.argtypes = [vp, vp, vp, vp, sz] + shp + pd + [vp]
             L.im2win_conv_fused_ex.argtypes = [vp, vp, vp, vp, sz] + shp + pd + [vp]
+            L.im2win_plan.argtypes = [ctypes.c_int] + shp + pd + [ctypes.c_int, ctypes.POINTER(PlanInfo)]
             for f in ("im2win_workspace_size", "im2win_transform", "im2win_conv",
                       "im2win_conv_fused", "im2win_device_status", "im2win_conv_fused_noalloc",
                       "im2win_transform_nhwc", "im2win_conv_nhwc", "im2win_conv_fused_nhwc",
                       "im2win_workspace_size_ex", "im2win_transform_ex", "im2win_conv_ex",
-                      "im2win_conv_fused_ex"):
+                      "im2win_conv_fused_ex", "im2win_plan"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -261,6 +272,17 @@ def im2win_conv_fused_ex(x: torch.Tensor, filt: torch.Tensor, out: torch.Tensor,
            lib().im2win_conv_fused_ex(x.data_ptr(), filt.data_ptr(), out.data_ptr(), ws.data_ptr(),
                                       ws.numel() * ws.element_size(), N, C_i, H_i, W_i, C_o, H_f, W_f, s_h,
                                       s_w, p_h, p_w, d_h, d_w, layout, _dtype_code(x), _stream(x)))
+
+
+def im2win_plan(op: int, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, p_h=0, p_w=0, d_h=1, d_w=1,
+                layout: int = NCHW, dtype: int = F16, sms: int = 0) -> dict:
+    """Kernel and tiling of a convolution call (host only, no device needed);
+    op OP_CONV (from the window tensor) or OP_CONV_FUSED. Raises Im2winError
+    where the call would fail."""
+    info = PlanInfo()
+    _check("im2win_plan", lib().im2win_plan(op, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, p_h, p_w, d_h, d_w,
+                                            layout, dtype, sms, ctypes.byref(info)))
+    return {name: getattr(info, name) for name, _ in PlanInfo._fields_ if name != "reserved"}
 
 
 def im2win_device_status(ws: torch.Tensor) -> int:

@@ -243,6 +243,41 @@ im2win_status im2win_conv_fused_ex(const void *x, const void *filt, void *out, v
     return conv_shape(s, x, filt, out, ws, ws_bytes, dtype, stream, true, layout);
 }
 
+im2win_status im2win_plan(int op, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i, int64_t C_o,
+                          int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w, int64_t p_h, int64_t p_w,
+                          int64_t d_h, int64_t d_w, int layout, int dtype, int sms, im2win_plan_info *info) {
+    if (!info || (layout != IM2WIN_LAYOUT_NCHW && layout != IM2WIN_LAYOUT_NHWC) ||
+        (op != IM2WIN_OP_CONV && op != IM2WIN_OP_CONV_FUSED) || elem_size(dtype) == 0)
+        return IM2WIN_ERR_INVALID_ARG;
+    Shape s;
+    im2win_status st = make_shape_pd(s, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, p_h, p_w, d_h, d_w);
+    if (st != IM2WIN_OK) return st;
+    const bool fused = op == IM2WIN_OP_CONV_FUSED;
+    std::memset(info, 0, sizeof(*info));
+    info->tap_mode = -1;
+    if (dtype == IM2WIN_F32) {
+        if (!conv_f32_supported(s, fused, layout)) return IM2WIN_ERR_UNSUPPORTED;
+        info->kernel = IM2WIN_KERNEL_F32;
+        return IM2WIN_OK;
+    }
+    TcPlanInfo t;
+    if (!conv_tc_plan_info(s, fused, layout, sms, t)) return IM2WIN_ERR_UNSUPPORTED;
+    info->kernel = t.kernel == 1 ? IM2WIN_KERNEL_TAP : IM2WIN_KERNEL_EXPAND;
+    info->tap_mode = t.tap_mode;
+    info->stacked = t.stacked;
+    info->rows_per_tile = t.rows_per_tile;
+    info->pitch = t.pitch;
+    info->tmem_columns = t.tmem_columns;
+    info->tmem_read_end = t.tmem_read_end;
+    info->smem_bytes = t.smem_bytes;
+    info->filter_stage_taps = t.filter_stage_taps;
+    info->filter_stages = t.filter_stages;
+    info->slab_stages = t.slab_stages;
+    info->tiles = t.tiles;
+    info->grid = t.grid;
+    return IM2WIN_OK;
+}
+
 const char *im2win_status_string(int status) {
     switch (status) {
         case IM2WIN_OK: return "ok";

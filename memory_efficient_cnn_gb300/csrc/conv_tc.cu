@@ -414,7 +414,7 @@ __device__ __forceinline__ void tile_at(const TapParams &p, int64_t id, TapTile 
 // an accumulator is released as soon as it is drained, so the next tile's MMAs
 // into it must not reach columns of the other, possibly still draining, one.
 // A narrower tile may leave the second accumulator empty.
-__device__ __forceinline__ int split_n0(int NTp) {
+__host__ __device__ __forceinline__ int split_n0(int NTp) {
     return NTp >= 32 ? min(NTp, (NTp / 2 + 31) / 32 * 32) : NTp;
 }
 __device__ __forceinline__ int tile_n0(const TapParams &p, int NTp) {
@@ -1553,6 +1553,56 @@ bool conv_tc_supported(const Shape &s, bool fused, int layout) {
     const int64_t pos_tiles = (P + NT - 1) / NT;
     return img < (1ll << 31) && s.C_i * KKP < (1ll << 30) && P < (1ll << 31) &&
            pos_tiles * s.N < (1ll << 31) && (s.C_o + BM - 1) / BM < 65536;
+}
+
+bool conv_tc_plan_info(const Shape &s, bool fused, int layout, int64_t sms, TcPlanInfo &info) {
+    if (!conv_tc_supported(s, fused, layout)) return false;
+    if (sms <= 0) sms = sm_count();
+    info = TcPlanInfo{};
+    const TapPlan pl = choose_tap(s, fused, layout, sms);
+    if (!pl.ok) {
+        info.kernel = 2;
+        info.tap_mode = -1;
+        return true;
+    }
+    const TapParams &p = pl.p;
+    info.kernel = 1;
+    info.tap_mode = pl.mode;
+    info.stacked = p.stack;
+    info.rows_per_tile = p.Qmax;
+    info.pitch = p.pitch;
+    const int NT = p.Qmax * p.pitch;  // the widest tile's positions
+    const int NTp = (NT + p.stack + 15) / 16 * 16;
+    info.tmem_columns = NTp;
+    // The epilogue's column walk: the two warps of a lane quarter split a range in
+    // 64-column blocks; without stacking a warp reads 32-column loads while they
+    // start inside its share, with stacking every block whole plus (lower half)
+    // the column after it.
+    int end = 0;
+    auto walk = [&](int a0, int a1) {
+        const int nb = (a1 - a0 + 63) / 64;
+        const int mid = a0 + ((nb + 1) / 2) * 64;
+        for (int hh = 0; hh < 2; ++hh) {
+            const int cb = hh == 0 ? a0 : mid, ce = hh == 0 ? std::min(a1, mid) : a1;
+            if (cb >= ce) continue;
+            end = std::max(end, p.stack ? cb + (ce - cb + 63) / 64 * 64 + 1 : cb + (ce - cb + 31) / 32 * 32);
+        }
+    };
+    if (p.stack) {
+        walk(0, (NT + 15) / 16 * 16);
+    } else {
+        const int N0 = split_n0(NTp);
+        walk(0, N0);
+        walk(N0, NTp);
+    }
+    info.tmem_read_end = end;
+    info.smem_bytes = (int)pl.smem;
+    info.filter_stage_taps = p.TG;
+    info.filter_stages = p.AST;
+    info.slab_stages = p.BST;
+    info.tiles = p.tiles_total;
+    info.grid = std::min<int64_t>(sms, p.tiles_total);
+    return true;
 }
 
 static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *filt, void *out,

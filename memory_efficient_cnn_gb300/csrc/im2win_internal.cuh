@@ -124,6 +124,18 @@ cudaError_t launch_conv_f32(const void *src, const void *filt, void *out, void *
 // from the input, in either layout.
 size_t conv_tc_filter_bytes(const Shape &s, bool fused, int layout);
 bool conv_tc_supported(const Shape &s, bool fused, int layout);
+
+// What a tensor-core convolution launches (host only; the plan query).
+// kernel 1: tap kernel, 2: expand kernel; the other fields describe the tap
+// kernel (zero for the expand kernel). tmem_read_end is one past the highest
+// accumulator column the epilogue reads, as its drain walks the columns.
+struct TcPlanInfo {
+    int kernel, tap_mode, stacked, rows_per_tile, pitch, tmem_columns, tmem_read_end, smem_bytes;
+    int filter_stage_taps, filter_stages, slab_stages;
+    int64_t tiles, grid;
+};
+// false: no tensor-core kernel covers the shape. sms <= 0: the current device's.
+bool conv_tc_plan_info(const Shape &s, bool fused, int layout, int64_t sms, TcPlanInfo &info);
 cudaError_t launch_conv_tc(const void *src, const void *filt, void *out, void *ws,
                            const Shape &s, bool fused, int layout, bool bf16, cudaStream_t st);
 
