@@ -13,6 +13,10 @@
  *    H_o = (H_i - H_f)/s_h + 1 and W_o = (W_i - W_f)/s_w + 1 (floor), which every
  *    layer of [GPU] Table I satisfies. All sizes are int64_t and must be >= 1
  *    (N may be 0: the call then does nothing), with H_f <= H_i and W_f <= W_i.
+ *    Each tensor a call touches (input, window tensor, output, filter) must hold
+ *    at most 2^50 elements; larger shapes return IM2WIN_ERR_UNSUPPORTED from
+ *    every call, the workspace queries included, so a size these return never
+ *    wraps around.
  *  - Layouts are dense and row-major: x[N][C_i][H_i][W_i] (NCHW),
  *    filt[C_o][C_i][H_f][W_f], out[N][C_o][H_o][W_o], and the window tensor
  *    win[N][C_i][H_o][W_i*H_f].
@@ -76,7 +80,8 @@ typedef enum {
  * W_i*H_f unique elements per channel and output row). For the two convolutions it
  * is a 256-byte status block plus the filter re-laid for the kernel that runs, each
  * part rounded up to 256 bytes; the fused convolution needs no window tensor.
- * Errors: INVALID_ARG for a bad shape, dtype or op, or bytes == NULL.
+ * Errors: INVALID_ARG for a bad shape, dtype or op, or bytes == NULL;
+ * UNSUPPORTED for a shape beyond the 2^50-element limit above.
  */
 im2win_status im2win_workspace_size(int op, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i,
                                     int64_t C_o, int64_t H_f, int64_t W_f, int64_t s_h,
@@ -291,6 +296,9 @@ im2win_status im2win_device_status(const void *ws, size_t ws_bytes, void *stream
  * that size is rejected with IM2WIN_ERR_WORKSPACE before any work is queued.
  * The first call on a device, with that device current, looks up the array's
  * device address (cudaGetSymbolAddress); make it before any stream capture.
+ * The address is kept for the life of the process: after cudaDeviceReset on
+ * that device the array may move and this call must not be used again in the
+ * process.
  * All calls share the array and it keeps the last call's contents (each call
  * re-lays the filter and clears the status word itself): calls whose work can
  * overlap on the GPU race and may return wrong results. Calls no cudaMalloc,

@@ -119,6 +119,43 @@ def _cuda(*ts):
             raise ValueError("im2win tensors must be contiguous")
 
 
+def _same_device(fn, *ts):
+    dev = ts[0].device
+    for t in ts[1:]:
+        if t.device != dev:
+            raise ValueError(f"{fn}: every tensor must be on one device ({dev} and {t.device} given)")
+
+
+def _check_conv(fn, src, filt, out, ws, dims, C_o, H_f, W_f, stride, pad=(0, 0), dil=(1, 1),
+                layout=NCHW, window=False):
+    """Shape and device checks of a convolution call, made before anything is
+    launched: the filter must be C_o x C_i x H_f x W_f, `out` must have the
+    output's exact shape in `layout`, the source must hold at least the input
+    (fused) or window tensor (window=True) of `dims` = (N, C_i, H_i, W_i), and
+    every tensor must be on one device. A mismatch raises ValueError; the
+    library itself checks the workspace size. An empty batch (N = 0) reads and
+    writes nothing, so its buffers are not checked."""
+    N, C_i, H_i, W_i = (int(v) for v in dims)
+    if filt.dim() != 4 or tuple(filt.shape) != (C_o, C_i, H_f, W_f):
+        raise ValueError(f"{fn}: filt has shape {tuple(filt.shape)}, expected {(C_o, C_i, H_f, W_f)}")
+    H_o, W_o = out_hw_pd(H_i, W_i, H_f, W_f, stride, pad, dil)
+    if N > 0 and H_o >= 1 and W_o >= 1:
+        want = (N, H_o, W_o, C_o) if layout == NHWC else (N, C_o, H_o, W_o)
+        if tuple(out.shape) != want:
+            raise ValueError(f"{fn}: out has shape {tuple(out.shape)}, expected {want}")
+        elems = N * C_i * H_o * (W_i + 2 * pad[1]) * H_f if window else N * C_i * H_i * W_i
+        if src.numel() < elems:
+            what = "window tensor" if window else "input"
+            raise ValueError(f"{fn}: the {what} has {src.numel()} elements, expected {elems}")
+    _same_device(fn, src, filt, out, *([ws] if ws is not None else []))
+
+
+def _check_transform(fn, x, win, dims):
+    if x.numel() < int(dims[0]) * int(dims[1]) * int(dims[2]) * int(dims[3]):
+        raise ValueError(f"{fn}: x has {x.numel()} elements, expected N*C_i*H_i*W_i of {tuple(dims)}")
+    _same_device(fn, x, win)
+
+
 def _stream(t: torch.Tensor):
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
@@ -137,8 +174,9 @@ def im2win_workspace_size(op: int, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, dt
 
 
 def im2win_transform(x: torch.Tensor, win: torch.Tensor, C_o, H_f, W_f, s_h, s_w) -> None:
-    _cuda(x, win)
     N, C_i, H_i, W_i = x.shape
+    _check_transform("im2win_transform", x, win, x.shape)
+    _cuda(x, win)
     if win.dtype != x.dtype:
         raise TypeError("win must have the dtype of x")
     need = im2win_workspace_size(OP_TRANSFORM, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
@@ -152,6 +190,8 @@ def im2win_transform(x: torch.Tensor, win: torch.Tensor, C_o, H_f, W_f, s_h, s_w
 
 def im2win_conv(win: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
                 N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w) -> None:
+    _check_conv("im2win_conv", win, filt, out, ws, (N, C_i, H_i, W_i), C_o, H_f, W_f, (s_h, s_w),
+                window=True)
     _cuda(win, filt, out, ws)
     if not (win.dtype == filt.dtype == out.dtype):
         raise TypeError("win, filt and out must share a dtype")
@@ -163,11 +203,12 @@ def im2win_conv(win: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: to
 
 def im2win_conv_fused(x: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
                       s_h, s_w) -> None:
+    N, C_i, H_i, W_i = x.shape
+    C_o, _, H_f, W_f = filt.shape
+    _check_conv("im2win_conv_fused", x, filt, out, ws, x.shape, C_o, H_f, W_f, (s_h, s_w))
     _cuda(x, filt, out, ws)
     if not (x.dtype == filt.dtype == out.dtype):
         raise TypeError("x, filt and out must share a dtype")
-    N, C_i, H_i, W_i = x.shape
-    C_o, _, H_f, W_f = filt.shape
     _check("im2win_conv_fused",
            lib().im2win_conv_fused(x.data_ptr(), filt.data_ptr(), out.data_ptr(), ws.data_ptr(),
                                    ws.numel() * ws.element_size(), N, C_i, H_i, W_i, C_o, H_f,
@@ -177,11 +218,12 @@ def im2win_conv_fused(x: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws
 def im2win_conv_fused_noalloc(x: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, s_h, s_w) -> None:
     """Fused convolution for callers that cannot allocate a workspace: the
     scratch is the library's built-in array (see include/im2win.h)."""
+    N, C_i, H_i, W_i = x.shape
+    C_o, _, H_f, W_f = filt.shape
+    _check_conv("im2win_conv_fused_noalloc", x, filt, out, None, x.shape, C_o, H_f, W_f, (s_h, s_w))
     _cuda(x, filt, out)
     if not (x.dtype == filt.dtype == out.dtype):
         raise TypeError("x, filt and out must share a dtype")
-    N, C_i, H_i, W_i = x.shape
-    C_o, _, H_f, W_f = filt.shape
     _check("im2win_conv_fused_noalloc",
            lib().im2win_conv_fused_noalloc(x.data_ptr(), filt.data_ptr(), out.data_ptr(), N, C_i,
                                            H_i, W_i, C_o, H_f, W_f, s_h, s_w, _dtype_code(x),
@@ -190,8 +232,9 @@ def im2win_conv_fused_noalloc(x: torch.Tensor, filt: torch.Tensor, out: torch.Te
 
 def im2win_transform_nhwc(x: torch.Tensor, win: torch.Tensor, C_o, H_f, W_f, s_h, s_w) -> None:
     """Channels-last window transform: x[N][H_i][W_i][C_i] -> win[N][H_o][W_i*H_f][C_i]."""
-    _cuda(x, win)
     N, H_i, W_i, C_i = x.shape
+    _check_transform("im2win_transform_nhwc", x, win, x.shape)
+    _cuda(x, win)
     if win.dtype != x.dtype:
         raise TypeError("win must have the dtype of x")
     need = im2win_workspace_size(OP_TRANSFORM, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
@@ -206,6 +249,8 @@ def im2win_transform_nhwc(x: torch.Tensor, win: torch.Tensor, C_o, H_f, W_f, s_h
 def im2win_conv_nhwc(win: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
                      N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w) -> None:
     """Convolution from the channels-last window tensor into out[N][H_o][W_o][C_o]."""
+    _check_conv("im2win_conv_nhwc", win, filt, out, ws, (N, C_i, H_i, W_i), C_o, H_f, W_f, (s_h, s_w),
+                layout=NHWC, window=True)
     _cuda(win, filt, out, ws)
     if not (win.dtype == filt.dtype == out.dtype):
         raise TypeError("win, filt and out must share a dtype")
@@ -218,11 +263,13 @@ def im2win_conv_nhwc(win: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, w
 def im2win_conv_fused_nhwc(x: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
                            s_h, s_w) -> None:
     """Fused convolution of x[N][H_i][W_i][C_i] into out[N][H_o][W_o][C_o]."""
+    N, H_i, W_i, C_i = x.shape
+    C_o, _, H_f, W_f = filt.shape
+    _check_conv("im2win_conv_fused_nhwc", x, filt, out, ws, (N, C_i, H_i, W_i), C_o, H_f, W_f, (s_h, s_w),
+                layout=NHWC)
     _cuda(x, filt, out, ws)
     if not (x.dtype == filt.dtype == out.dtype):
         raise TypeError("x, filt and out must share a dtype")
-    N, H_i, W_i, C_i = x.shape
-    C_o, _, H_f, W_f = filt.shape
     _check("im2win_conv_fused_nhwc",
            lib().im2win_conv_fused_nhwc(x.data_ptr(), filt.data_ptr(), out.data_ptr(), ws.data_ptr(),
                                         ws.numel() * ws.element_size(), N, C_i, H_i, W_i, C_o, H_f,
@@ -240,6 +287,7 @@ def im2win_workspace_size_ex(op: int, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
 
 def im2win_transform_ex(x: torch.Tensor, win: torch.Tensor, N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w,
                         p_h, p_w, d_h, d_w, layout: int) -> None:
+    _check_transform("im2win_transform_ex", x, win, (N, C_i, H_i, W_i))
     _cuda(x, win)
     if win.dtype != x.dtype:
         raise TypeError("win must have the dtype of x")
@@ -254,6 +302,8 @@ def im2win_transform_ex(x: torch.Tensor, win: torch.Tensor, N, C_i, H_i, W_i, C_
 
 def im2win_conv_ex(win: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
                    N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, p_h, p_w, d_h, d_w, layout: int) -> None:
+    _check_conv("im2win_conv_ex", win, filt, out, ws, (N, C_i, H_i, W_i), C_o, H_f, W_f, (s_h, s_w),
+                (p_h, p_w), (d_h, d_w), layout, window=True)
     _cuda(win, filt, out, ws)
     if not (win.dtype == filt.dtype == out.dtype):
         raise TypeError("win, filt and out must share a dtype")
@@ -265,6 +315,8 @@ def im2win_conv_ex(win: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws:
 
 def im2win_conv_fused_ex(x: torch.Tensor, filt: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
                          N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w, p_h, p_w, d_h, d_w, layout: int) -> None:
+    _check_conv("im2win_conv_fused_ex", x, filt, out, ws, (N, C_i, H_i, W_i), C_o, H_f, W_f, (s_h, s_w),
+                (p_h, p_w), (d_h, d_w), layout)
     _cuda(x, filt, out, ws)
     if not (x.dtype == filt.dtype == out.dtype):
         raise TypeError("x, filt and out must share a dtype")

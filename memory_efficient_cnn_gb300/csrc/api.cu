@@ -3,12 +3,39 @@
 // im2win_device_status), no CPU fallback: every result is computed on the GPU.
 #include <cstdint>
 #include <cstring>
+#include <initializer_list>
 
 #include "im2win_internal.cuh"
 
 using namespace im2win;
 
 namespace {
+
+// Every element count a call can touch (input, window tensor, output, filter)
+// stays at or below 2^50, so that byte counts and the kernels' 64-bit offsets
+// derived from them cannot overflow. Products are formed in 128 bits.
+constexpr int64_t kMaxElems = int64_t(1) << 50;
+
+bool product_within(std::initializer_list<int64_t> factors, int64_t lim) {
+    __int128 p = 1;
+    for (const int64_t f : factors) {
+        p *= (__int128)f;
+        if (p > (__int128)lim) return false;
+    }
+    return true;
+}
+
+// The shape's tensors: x (padded extent), the window tensor, the output and the
+// filter, each within kMaxElems elements.
+im2win_status bound_tensors(const Shape &s) {
+    const int64_t Hp = s.H_i + 2 * s.p_h, Wp = s.W_i + 2 * s.p_w;
+    if (!product_within({s.N, s.C_i, Hp, Wp}, kMaxElems) ||
+        !product_within({s.N, s.C_i, s.H_o, Wp, s.H_f}, kMaxElems) ||
+        !product_within({s.N, s.C_o, s.H_o, s.W_o}, kMaxElems) ||
+        !product_within({s.C_o, s.C_i, s.H_f, s.W_f}, kMaxElems))
+        return IM2WIN_ERR_UNSUPPORTED;
+    return IM2WIN_OK;
+}
 
 im2win_status make_shape(Shape &s, int64_t N, int64_t C_i, int64_t H_i, int64_t W_i, int64_t C_o,
                          int64_t H_f, int64_t W_f, int64_t s_h, int64_t s_w) {
@@ -24,7 +51,7 @@ im2win_status make_shape(Shape &s, int64_t N, int64_t C_i, int64_t H_i, int64_t 
     s.H_f = H_f; s.W_f = W_f; s.s_h = s_h; s.s_w = s_w;
     s.H_o = (H_i - H_f) / s_h + 1;
     s.W_o = (W_i - W_f) / s_w + 1;
-    return IM2WIN_OK;
+    return bound_tensors(s);
 }
 
 // make_shape with zero padding p_h, p_w >= 0 and dilation d_h, d_w >= 1; the
@@ -47,7 +74,7 @@ im2win_status make_shape_pd(Shape &s, int64_t N, int64_t C_i, int64_t H_i, int64
     s.p_h = p_h; s.p_w = p_w; s.d_h = d_h; s.d_w = d_w; s.g_w = 1;
     s.H_o = (H_i + 2 * p_h - d_h * (H_f - 1) - 1) / s_h + 1;
     s.W_o = (W_i + 2 * p_w - d_w * (W_f - 1) - 1) / s_w + 1;
-    return IM2WIN_OK;
+    return bound_tensors(s);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -15,7 +15,11 @@
 //    work is queued;
 //  * the device address of the array is looked up once per device, on the
 //    first call made while that device is current (cudaGetSymbolAddress);
-//    make that first call before capturing the stream into a graph;
+//    make that first call before capturing the stream into a graph. The
+//    address is kept until the process exits: cudaDeviceReset unloads the
+//    library's module on that device, the array may come back elsewhere, and
+//    the kept address would then be stale, so this entry point must not be
+//    called on a device after it has been reset;
 //  * all calls share the array, which keeps whatever the last call left in
 //    it: every call re-lays the filter and clears the status word itself, and
 //    two calls whose kernels overlap on the GPU (different streams, no

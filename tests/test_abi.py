@@ -121,3 +121,51 @@ def test_ex_workspace_sizes_and_argument_errors(lib):
     assert L.im2win_transform_ex(None, 256, *base, 0, 0, 1, 1, 0, 0, None) == bad
     assert L.im2win_conv_fused_ex(1024 + 4, 2048, 4096, 8192, 1 << 20, *base, 0, 0, 1, 1, 0, 1,
                                   None) == mec._binding.ERR_MISALIGNED
+
+
+def test_binding_refuses_mismatched_shapes_before_launching(lib):
+    """A filter, output or source of the wrong size is refused on the host, before
+    the C ABI (and so any kernel) is reached: these are CPU tensors, which the
+    binding would otherwise refuse for not being on the GPU."""
+    import torch
+    x = torch.zeros(2, 3, 9, 9)
+    w = torch.zeros(4, 3, 3, 3)
+    out = torch.zeros(2, 4, 7, 7)
+    ws = torch.zeros(1 << 12, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="out has shape"):
+        mec.im2win_conv_fused(x, w, torch.zeros(2, 4, 7, 6), ws, 1, 1)
+    with pytest.raises(ValueError, match="out has shape"):
+        mec.im2win_conv_fused_noalloc(x, w, torch.zeros(2, 4, 6, 7), 1, 1)
+    with pytest.raises(ValueError, match="filt has shape"):
+        mec.im2win_conv_fused(x, torch.zeros(4, 2, 3, 3), out, ws, 1, 1)
+    with pytest.raises(ValueError, match="window tensor has"):
+        mec.im2win_conv(torch.zeros(2 * 3 * 7 * 27 - 1), w, out, ws, 2, 3, 9, 9, 4, 3, 3, 1, 1)
+    with pytest.raises(ValueError, match="filt has shape"):
+        mec.im2win_conv(torch.zeros(2 * 3 * 7 * 27), w, out, ws, 2, 3, 9, 9, 5, 3, 3, 1, 1)
+    with pytest.raises(ValueError, match="out has shape"):
+        mec.im2win_conv_fused_nhwc(x.permute(0, 2, 3, 1).contiguous(), w, out, ws, 1, 1)
+    with pytest.raises(ValueError, match="out has shape"):
+        mec.im2win_conv_fused_ex(x, w, out, ws, 2, 3, 9, 9, 4, 3, 3, 1, 1, 1, 1, 1, 1, mec.NCHW)
+    with pytest.raises(ValueError, match="x has"):
+        mec.im2win_transform_ex(x[:1], torch.zeros(10 ** 4), 2, 3, 9, 9, 4, 3, 3, 1, 1, 0, 0, 1, 1, mec.NCHW)
+    # the right shapes pass the shape checks and stop at the device check
+    with pytest.raises(ValueError, match="CUDA"):
+        mec.im2win_conv_fused(x, w, out, ws, 1, 1)
+    with pytest.raises(ValueError, match="CUDA"):
+        mec.im2win_conv_fused_ex(x, w, torch.zeros(2, 4, 9, 9), ws, 2, 3, 9, 9, 4, 3, 3, 1, 1, 1, 1, 1, 1,
+                                 mec.NCHW)
+
+
+def test_workspace_query_refuses_shapes_whose_sizes_would_wrap(lib):
+    """Each factor below passes the per-dimension limits, but the window tensor
+    (N*C_i*H_o*W_i*H_f elements) would exceed 2^64 bytes: UNSUPPORTED, not a
+    wrapped-around size."""
+    sz = ctypes.c_size_t()
+    big = [1 << 20, 1 << 20, 1 << 19, 1 << 19, 1, 1 << 10, 1, 1, 1]
+    assert lib.im2win_workspace_size(0, *big, 0, ctypes.byref(sz)) == mec._binding.ERR_UNSUPPORTED
+    assert lib.im2win_workspace_size_ex(0, *big, 0, 0, 1, 1, 0, 0, ctypes.byref(sz)) == \
+        mec._binding.ERR_UNSUPPORTED
+    # just under the limit the size is exact
+    ok = [1, 1 << 10, 1 << 10, 1 << 10, 1, 1, 1, 1, 1]
+    assert lib.im2win_workspace_size(0, *ok, 1, ctypes.byref(sz)) == 0
+    assert sz.value == (1 << 30) * 2

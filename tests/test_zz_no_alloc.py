@@ -57,6 +57,32 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
             assert np.all(err <= TOL[x.dtype] * scale), (dt, layer.name, err.max())
 
 
+def test_noalloc_call_allocates_no_device_memory():
+    """What the entry point exists for: once its kernels are loaded (the first
+    call), a call takes no device memory -- neither from torch's allocator nor
+    from the driver (free bytes of the device unchanged)."""
+    dt, layer = CASES[0]
+    x, w = wl.make_inputs(layer, dt)
+    x, w = x.cuda(), w.cuda()
+    stride = (layer.s_h, layer.s_w)
+    _noalloc(x, w, stride)  # loads the kernels, looks up the scratch address
+    torch.cuda.synchronize()
+    H_o, W_o = mec.out_hw(layer.H_i, layer.W_i, layer.H_f, layer.W_f, *stride)
+    out = torch.empty((layer.N, layer.C_o, H_o, W_o), dtype=x.dtype, device=x.device)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    torch_before = torch.cuda.memory_allocated()
+    free_before, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        st = mec.lib().im2win_conv_fused_noalloc(
+            x.data_ptr(), w.data_ptr(), out.data_ptr(), layer.N, layer.C_i, layer.H_i, layer.W_i, layer.C_o,
+            layer.H_f, layer.W_f, stride[0], stride[1], mec._binding._dtype_code(x), stream)
+        assert st == 0, mec.status_string(st)
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == torch_before
+    assert free_after == free_before
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     # 512 x 512 channels of 11 x 11 taps: the re-laid fp32 filter alone is 121 MiB
     big = (1, 512, 16, 16, 512, 11, 11, 1, 1)
