@@ -1086,6 +1086,12 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 uint16_t *out_c = out_at(co0);
                 for (int a = 0; a < 2 && ok; ++a) {
                     if (!(ok = warp_bar_wait(tmem_full(a), k & 1, ctl, SITE_DONE))) break;
+                    if (co0 >= p.C_o) {
+                        // the warp's 32 channels lie past C_o (zero filter rows): nothing
+                        // to store, the accumulator is released at once
+                        if (lane == 0) mbar_arrive(tmem_empty(a));
+                        continue;
+                    }
                     tc_fence_after();
                     int cb, ce;
                     half_range(a == 0 ? 0 : N0, a == 0 ? N0 : NTp, cb, ce);
