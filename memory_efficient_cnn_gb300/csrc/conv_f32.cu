@@ -37,6 +37,7 @@
 #include <algorithm>
 
 #include "im2win_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace im2win {
 namespace {
@@ -235,22 +236,63 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
+    // Pacing of the pipeline. Channel tiles below 128 (24- and 16-k chunks): stage
+    // s has mbarriers; full[s] completes when every thread's copies of its chunk
+    // have landed (one cp.async.mbarrier.arrive.noinc per thread), empty[s] when
+    // every warp has computed it. Chunk c - 1's stage is refilled (with chunk
+    // c - 1 + STAGES) after this warp has computed chunk c, so a warp waits for
+    // the others only when it is a whole chunk ahead of the slowest (cv1: 574
+    // instead of 581 us). Waits are bounded: one that gives up records
+    // IM2WIN_ERR_TIMEOUT in the status word. The 128-channel tile's chunks are
+    // short (16 k); there a barrier per chunk, with two chunks in flight, measured
+    // faster (990 instead of 1002 us on the 3x3 sweep layer).
+    constexpr bool MBAR = TM < 128;
+    __shared__ uint64_t bar_full[STAGES], bar_empty[STAGES];
+    if (MBAR && tid == 0) {
+        for (int st = 0; st < STAGES; ++st) {
+            tc::mbar_init(tc::smem_u32(&bar_full[st]), NT);
+            tc::mbar_init(tc::smem_u32(&bar_empty[st]), NW);
+        }
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    auto wait_bar = [&](uint64_t *bar, uint32_t parity) -> bool {
+        const uint32_t a = tc::smem_u32(bar);
+        if (tc::mbar_try_wait(a, parity)) return true;
+        const uint64_t t0 = tc::globaltimer();
+        for (uint32_t spin = 1;; ++spin) {
+            if (tc::mbar_try_wait(a, parity)) return true;
+            if ((spin & 255u) == 0 && tc::globaltimer() - t0 > tc::kTimeoutNs) {
+                atomicCAS(p.status, 0u, (uint32_t)IM2WIN_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    };
+
     const int nchunks = (p.K + KC - 1) / KC;
 #pragma unroll
-    for (int c = 0; c < STAGES - 1; ++c) {
+    for (int c = 0; c < (MBAR ? STAGES : STAGES - 1); ++c) {
         if (c < nchunks) issue_chunk(c);
-        cp_async_commit();
+        if (MBAR) {
+            if (c < nchunks) tc::cp_async_mbar_arrive_noinc(tc::smem_u32(&bar_full[c]));
+        } else {
+            cp_async_commit();
+        }
     }
     // k values of the last chunk (the rest of it is the filter's zero padding);
     // the 128-channel tile, whose registers are capped at 128, always runs whole
     // chunks (a separate short loop makes it spill)
     const int k_last = TM == 128 ? KC : p.K - (nchunks - 1) * KC;
     for (int c = 0; c < nchunks; ++c) {
-        cp_async_wait<STAGES - 2>();  // chunk c has landed (this thread's copies)
-        __syncthreads();              // ... and every thread's; chunk c-1's buffer is free
-        if (c + STAGES - 1 < nchunks) issue_chunk(c + STAGES - 1);
-        cp_async_commit();
         const int buf = c % STAGES;
+        if (MBAR) {
+            if (!wait_bar(&bar_full[buf], (uint32_t)(c / STAGES) & 1u)) break;
+        } else {
+            cp_async_wait<STAGES - 2>();  // chunk c has landed (this thread's copies)
+            __syncthreads();              // ... and every thread's; chunk c-1's buffer is free
+            if (c + STAGES - 1 < nchunks) issue_chunk(c + STAGES - 1);
+            cp_async_commit();
+        }
         if (TM == 128 || c + 1 < nchunks || k_last == KC) {
 #pragma unroll
             for (int k = 0; k < KC; ++k) {
@@ -281,7 +323,19 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
                     for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(bv[i], av[j], acc[i][j]);
             }
         }
+        if (!MBAR) continue;
+        __syncwarp();
+        if ((tid & 31) == 0) tc::mbar_arrive(tc::smem_u32(&bar_empty[buf]));
+        // refill chunk c - 1's stage once every warp has computed it
+        const int cr = c - 1 + STAGES;
+        if (c >= 1 && cr < nchunks) {
+            const int sr = (c - 1) % STAGES;
+            if (!wait_bar(&bar_empty[sr], (uint32_t)((c - 1) / STAGES) & 1u)) break;
+            issue_chunk(cr);
+            tc::cp_async_mbar_arrive_noinc(tc::smem_u32(&bar_full[sr]));
+        }
     }
+    cp_async_commit();
     cp_async_wait<0>();
 
     // ---- epilogue: out[n][co][p], or (CL) out[n][p][co] (8 consecutive channels per pixel)
