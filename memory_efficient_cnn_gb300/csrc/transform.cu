@@ -24,6 +24,9 @@
 // The element type is the raw bit pattern (uint16_t / uint32_t), so the copy
 // is bit-exact for every dtype.
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "im2win_internal.cuh"
 
@@ -46,6 +49,8 @@ struct TParams {
     int Wt, ctiles;       // columns per tile and column tiles per band (1 unless a row is too wide)
     uint32_t L;           // W_i * H_f
     int in_cap;           // elements reserved for the staged input (the offset table follows)
+    int flip_bit;         // 16-bit gathers: lanes with this bit of their lane index set gather
+                          // their vector's elements in the order i ^ 2 (-1: none)
     FastDiv div_L, div_Hf, div_RP;
 };
 
@@ -154,9 +159,15 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
     uint4 *gv = reinterpret_cast<uint4 *>(win + a0);
     const int q_body = (int)(a0 - o0);
     const int Lw = p.ctiles == 1 ? L : Wc * H_f;  // window row length within the piece
+    // 16-bit elements: the lanes whose flip bit is set gather element i ^ 2 at step i,
+    // so that at each step the warp's 2-byte shared loads fall in fewer banks twice
+    // over; the word pairs of their vector are swapped back before the store
+    const bool flip = V == 8 && p.flip_bit >= 0 && ((threadIdx.x >> p.flip_bit) & 1) != 0;
+    const int fx = flip ? 2 : 0;
     for (int v = threadIdx.x; v < nbody; v += kThreads) {
         int idx = locate(q_body + v * V);
         uint32_t e[V];
+        bool swapped = false;  // e[] holds the elements in the flipped order
         if (TABLE && w * H_f + r + V <= Lw) {
             // the vector stays in one window row: element i is at a fixed offset from
             // the top of column w, given by the table row of r
@@ -170,8 +181,15 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
                 o[4 * j + 2] = t.z;
                 o[4 * j + 3] = t.w;
             }
+            if (V == 8) {
+                // element i ^ fx at step i (the offsets' order only)
 #pragma unroll
-            for (int i = 0; i < V; ++i) e[i] = (uint32_t)sl[top + o[i]];
+                for (int i = 0; i < V; ++i) e[i] = (uint32_t)sl[top + (fx ? o[i ^ 2] : o[i])];
+                swapped = fx != 0;
+            } else {
+#pragma unroll
+                for (int i = 0; i < V; ++i) e[i] = (uint32_t)sl[top + o[i]];
+            }
         } else if (!TABLE && H_f >= V && w * H_f + r + V <= Lw) {
             // H_f >= V and one window row: the vector is the rest of column w and at
             // most the start of column w + 1, so its elements' staged indices are
@@ -182,7 +200,11 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
             const int th = H_f - r;
             const E *s0 = sl + idx;
 #pragma unroll
-            for (int i = 0; i < V; ++i) e[i] = (uint32_t)s0[i * Wc - (i >= th ? wrap : 0)];
+            for (int i = 0; i < V; ++i) {
+                const int j = i ^ fx;  // the element gathered at step i
+                e[i] = (uint32_t)s0[j * Wc - (j >= th ? wrap : 0)];
+            }
+            swapped = fx != 0;
         } else {
 #pragma unroll
             for (int i = 0; i < V; ++i) {
@@ -204,11 +226,59 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
         if (V == 8) {
             out = make_uint4(__byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410),
                              __byte_perm(e[4], e[5], 0x5410), __byte_perm(e[6], e[7], 0x5410));
+            // flipped order: e[i] is element i ^ 2, i.e. the vector's words 0,1 and 2,3 swapped
+            if (swapped) out = make_uint4(out.y, out.x, out.w, out.z);
         } else {
             out = make_uint4(e[0], e[1], e[2], e[3]);
         }
         gv[v] = out;
     }
+}
+
+// The lane bit whose lanes gather in the flipped order (-1: none) for 16-bit
+// vectors over rows of pitch Wc and H_f rows: a model of the gather's
+// shared-memory wavefronts (most distinct 4-byte words one bank serves, per
+// warp and step) over 128 warps' worth of consecutive vectors, for no flip and
+// for a flip on each of the lane bits 0..4; the fewest wins (ties: no flip).
+static int flip_bit_for(int64_t Wc, int64_t H_f) {
+    static std::mutex mu;
+    static std::map<std::pair<int64_t, int64_t>, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(Wc, H_f);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    auto cost = [&](int bit) {
+        int64_t total = 0;
+        for (int64_t v0 = 0; v0 < 128 * 32; v0 += 32) {
+            for (int t = 0; t < 8; ++t) {
+                int64_t words[32];
+                int per_bank[32] = {0};
+                for (int l = 0; l < 32; ++l) {
+                    const int i = (bit >= 0 && ((l >> bit) & 1)) ? (t ^ 2) : t;
+                    const int64_t q = 8 * (v0 + l) + i;
+                    const int64_t w = q / H_f, r = q - w * H_f;
+                    words[l] = (r * Wc + w) / 2;
+                }
+                for (int l = 0; l < 32; ++l) {
+                    bool seen = false;
+                    for (int l2 = 0; l2 < l; ++l2) seen = seen || words[l2] == words[l];
+                    if (!seen) ++per_bank[words[l] % 32];
+                }
+                int mx = 0;
+                for (int b = 0; b < 32; ++b) mx = std::max(mx, per_bank[b]);
+                total += mx;
+            }
+        }
+        return total;
+    };
+    int best = -1;
+    int64_t best_cost = cost(-1);
+    for (int bit = 0; bit < 5; ++bit) {
+        const int64_t c = cost(bit);
+        if (c < best_cost) { best_cost = c; best = bit; }
+    }
+    cache[key] = best;
+    return best;
 }
 
 int sm_count() {
@@ -277,6 +347,7 @@ cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, 
     p.ctiles = (int)ctiles;
     p.L = (uint32_t)L;
     p.in_cap = (int)(staged / esz);
+    p.flip_bit = esz == 2 ? flip_bit_for(Wt, s.H_f) : -1;
     p.div_L = make_fastdiv((uint32_t)L);
     p.div_Hf = make_fastdiv((uint32_t)s.H_f);
     p.div_RP = make_fastdiv((uint32_t)T);
