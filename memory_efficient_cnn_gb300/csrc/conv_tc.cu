@@ -983,11 +983,43 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                                        e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
                     }
                 }
+            } else if (MODE == TAP_WW) {
+                // window rows staged contiguously: entry (c, q, m) is the 8 consecutive
+                // staged elements at q*L + m*S + 8c of window row q (zero past the row's
+                // end, and past b = S: the K padding). Position by position (one division),
+                // K chunk by K chunk, each element at a fixed offset from the chunk's start:
+                // the fill is bound by instruction issue, and this takes about a third of
+                // the instructions of gathering through the offset table.
+                const int SC = 2 * p.U;
+                const int per_c = Q * p.pitch;
+                const E16 *raw = raw_slot + raw_lead_of(tl, cc);
+                const int L = (int)p.L, S = p.S;
+                for (int i = pt; i < per_c; i += NPT) {
+                    const int q = (int)fdiv((uint32_t)i, p.div_pitch);
+                    const int m = i - q * p.pitch;
+                    const int mm = m * S;
+                    const int lim = min(S, L - mm);  // elements of the position that exist
+                    const E16 *rb = raw + q * L + mm;
+                    uint8_t *dst = slab + (size_t)i * 16;
+                    for (int c = 0; c < SC; ++c, rb += 8, dst += p.lbo) {
+                        const int rem = lim - 8 * c;
+                        uint32_t e16[8];
+                        if (rem >= 8) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) e16[e] = (uint32_t)rb[e];
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) e16[e] = e < rem ? (uint32_t)rb[e] : 0u;
+                        }
+                        *reinterpret_cast<uint4 *>(dst) =
+                            make_uint4(__byte_perm(e16[0], e16[1], 0x5410), __byte_perm(e16[2], e16[3], 0x5410),
+                                       __byte_perm(e16[4], e16[5], 0x5410), __byte_perm(e16[6], e16[7], 0x5410));
+                    }
+                }
             } else {
-                // window rows of channel cc, re-laid from the staged raw rows:
+                // TAP_WX: window rows of channel cc, re-laid from the staged input rows:
                 //   entry (c, q, m)[e] = window row q of the tile at m*S + 8c + e
-                // TAP_WX: that element is x[cc][(ho0+q)*s_h + r][m*s_w + jl] with 8c + e = jl*H_f + r
-                // TAP_WW: it is read straight from the staged window row
+                //   = x[cc][(ho0+q)*s_h + r][m*s_w + jl] with 8c + e = jl*H_f + r
                 // One K chunk c at a time, so that the 8 source offsets of an entry
                 // (and which of them exist) stay in registers; per entry one division.
                 const int SC = 2 * p.U;
