@@ -69,19 +69,21 @@ struct F32Params {
 // The filter is padded along K to a multiple of every chunk length (16, 24, 48).
 constexpr int K_ALIGN = 48;
 
-// Kernel configurations per channel tile: TM, KC (k per chunk), pipeline stages,
-// CTAs per SM the registers are budgeted for.
+// Kernel configurations per channel tile: TM, RI (channels per thread), KC (k
+// per chunk), pipeline stages, CTAs per SM the registers are budgeted for. The
+// 96-channel tile runs 6 x 8 register tiles in 256 threads: 16 warps per SM
+// instead of the 12 of 8 x 8 tiles in 192 threads.
 #ifndef F32_CFG_128
-#define F32_CFG_128 128, 16, 3, 2
+#define F32_CFG_128 128, 8, 16, 3, 2
 #endif
 #ifndef F32_CFG_96
-#define F32_CFG_96 96, 24, 3, 2
+#define F32_CFG_96 96, 6, 16, 3, 2
 #endif
 #ifndef F32_CFG_64
-#define F32_CFG_64 64, 16, 3, 3
+#define F32_CFG_64 64, 8, 16, 3, 3
 #endif
 #ifndef F32_CFG_32
-#define F32_CFG_32 32, 8, 3, 4
+#define F32_CFG_32 32, 8, 8, 3, 4
 #endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -100,8 +102,28 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// TM output channels x 128 pixels per CTA, 8 x 8 register tile per thread
-// (channels ty*8..+7, pixels tx*4..+3 and 64 + tx*4..+3). K is staged KC at a
+// The RI filter values of a thread's channels at one k: two 16-byte loads (RI =
+// 8) or three 8-byte loads (RI = 6: a 24-byte group, 8-byte aligned).
+template <int RI>
+__device__ __forceinline__ void load_b(const float *b, float (&bv)[RI]) {
+    if (RI == 8) {
+        const float4 b0 = *reinterpret_cast<const float4 *>(b);
+        const float4 b1 = *reinterpret_cast<const float4 *>(b + 4);
+        const float t[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int i = 0; i < RI; ++i) bv[i] = t[i];
+    } else {
+#pragma unroll
+        for (int i = 0; i < RI; i += 2) {
+            const float2 v = *reinterpret_cast<const float2 *>(b + i);
+            bv[i] = v.x;
+            bv[i + 1] = v.y;
+        }
+    }
+}
+
+// TM output channels x 128 pixels per CTA, RI x 8 register tile per thread
+// (channels ty*RI..+RI-1, pixels tx*4..+3 and 64 + tx*4..+3). K is staged KC at a
 // time through a STAGES-deep cp.async pipeline (gathers go straight to shared
 // memory, so no registers hold prefetched data). The filter slice arrives as
 // 16-byte vectors. The 4-byte gathers follow the contiguous direction of the
@@ -112,16 +134,17 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // w % (KC/8) and walks every (NW/(KC/8))-th group of 4 pixels. From the NCHW
 // input consecutive pixels of a row are (unit stride), so lane l of warp w
 // gathers pixels l + 32i at the KPT values of k w*KPT ...
-template <int TM, int KC, int STAGES, int MINB, bool FROM_X, bool CL, bool GEN>
-__global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
-    constexpr int NT = TM * 2;                 // (TM/8) x 16 threads
+template <int TM, int RI, int KC, int STAGES, int MINB, bool FROM_X, bool CL, bool GEN>
+__global__ void __launch_bounds__(TM / RI * 16, MINB) conv_f32_kernel(F32Params p) {
+    constexpr int NT = TM / RI * 16;           // (TM/RI) x 16 threads
     constexpr int NW = NT / 32;                           // warps
     constexpr int KG = KC / 8;                            // window path: 8-k groups per chunk
     constexpr int PPT = FROM_X ? TP / 32 : TP * KG / (4 * NW);  // pixels each thread gathers
     constexpr int KPT = FROM_X ? KC * 32 / NT : 1;        // k values each thread gathers
-    constexpr int B_VEC = KC * TM / 4 / NT;    // 16-byte filter vectors each thread stages
+    constexpr int B_N = KC * TM / 4;                      // 16-byte filter vectors of a chunk
+    constexpr int B_VEC = (B_N + NT - 1) / NT;            // ... each thread stages at most
     static_assert((FROM_X ? KPT * NW == KC : (KC % 8 == 0 && NW % KG == 0 && PPT * 4 * NW == TP * KG)) &&
-                      (KC * TM / 4) % NT == 0 && (TP + 4) % 32 == 4,
+                      (RI == 8 || RI == 6) && TM % RI == 0 && (TP + 4) % 32 == 4,
                   "tile");
     static_assert(K_ALIGN % KC == 0, "filter padding");
     extern __shared__ __align__(16) float smem_f[];
@@ -220,6 +243,7 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
 #pragma unroll
         for (int v = 0; v < B_VEC; ++v) {
             const int q = tid + v * NT;            // vector index in the KC x TM/4 slice
+            if (B_N % NT != 0 && q >= B_N) break;
             const int kr = q / (TM / 4), cv = q - kr * (TM / 4);
             cp_async16(b_dst + (kr * (TM + 4) + cv * 4) * 4, fcol + (int64_t)(c * KC + kr) * p.C_o_pad + cv * 4);
         }
@@ -227,12 +251,12 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
 
     // ---- compute coordinates: warps of 4 channel groups x 8 pixel groups
     const int warp = tid >> 5, lane = tid & 31;
-    const int ty = (warp >> 1) * 4 + (lane >> 3);  // channel group (8 channels)
+    const int ty = (warp >> 1) * 4 + (lane >> 3);  // channel group (RI channels)
     const int tx = (warp & 1) * 8 + (lane & 7);     // pixel group (2 x 4 pixels)
 
-    float acc[8][8];
+    float acc[RI][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < RI; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
@@ -298,12 +322,11 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
             for (int k = 0; k < KC; ++k) {
                 const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][k][tx * 4]);
                 const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][k][64 + tx * 4]);
-                const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8]);
-                const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8 + 4]);
                 const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                float bv[RI];
+                load_b<RI>(&Bs[buf][k][ty * RI], bv);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < RI; ++i)
 #pragma unroll
                     for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(bv[i], av[j], acc[i][j]);
             }
@@ -313,12 +336,11 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
             for (int k = 0; k < k_last; ++k) {
                 const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][k][tx * 4]);
                 const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][k][64 + tx * 4]);
-                const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8]);
-                const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][k][ty * 8 + 4]);
                 const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                float bv[RI];
+                load_b<RI>(&Bs[buf][k][ty * RI], bv);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < RI; ++i)
 #pragma unroll
                     for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(bv[i], av[j], acc[i][j]);
             }
@@ -338,28 +360,32 @@ __global__ void __launch_bounds__(TM * 2, MINB) conv_f32_kernel(F32Params p) {
     cp_async_commit();
     cp_async_wait<0>();
 
-    // ---- epilogue: out[n][co][p], or (CL) out[n][p][co] (8 consecutive channels per pixel)
+    // ---- epilogue: out[n][co][p], or (CL) out[n][p][co] (RI consecutive channels per pixel)
     if (CL) {
-        const int cb = co0 + ty * 8;
-        const bool vec = (p.C_o & 3) == 0 && cb + 8 <= p.C_o;
+        const int cb = co0 + ty * RI;
+        const bool vec = RI == 8 ? ((p.C_o & 3) == 0 && cb + 8 <= p.C_o) : ((p.C_o & 1) == 0 && cb + RI <= p.C_o);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int pg = p0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
             if (pg >= p.P) continue;
             float *d = p.out + ((int64_t)n * p.P + pg) * p.C_o + cb;
-            if (vec) {
+            if (vec && RI == 8) {
                 reinterpret_cast<float4 *>(d)[0] = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
-                reinterpret_cast<float4 *>(d)[1] = make_float4(acc[4][j], acc[5][j], acc[6][j], acc[7][j]);
+                reinterpret_cast<float4 *>(d)[1] = make_float4(acc[4 % RI][j], acc[5 % RI][j], acc[6 % RI][j],
+                                                               acc[7 % RI][j]);
+            } else if (vec) {
+#pragma unroll
+                for (int i = 0; i < RI; i += 2) reinterpret_cast<float2 *>(d)[i / 2] = make_float2(acc[i][j], acc[i + 1][j]);
             } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < RI; ++i)
                     if (cb + i < p.C_o) d[i] = acc[i][j];
             }
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int co = co0 + ty * 8 + i;
+        for (int i = 0; i < RI; ++i) {
+            const int co = co0 + ty * RI + i;
             if (co >= p.C_o) continue;
             float *orow = p.out + ((int64_t)n * p.C_o + co) * p.P;
 #pragma unroll
@@ -397,14 +423,14 @@ __global__ void relayout_filter_f32(const float *__restrict__ filt, float *__res
     }
 }
 
-template <int TM, int KC, int STAGES, int MINB, bool FROM_X, bool CL = false, bool GEN = false>
+template <int TM, int RI, int KC, int STAGES, int MINB, bool FROM_X, bool CL = false, bool GEN = false>
 cudaError_t launch_tm(const F32Params &p, int N, cudaStream_t st) {
     dim3 grid((unsigned)(p.pos_tiles * N), (unsigned)((p.C_o + TM - 1) / TM));
     constexpr size_t smem = f32_smem_bytes<TM, KC, STAGES>();
-    cudaError_t e = cudaFuncSetAttribute(conv_f32_kernel<TM, KC, STAGES, MINB, FROM_X, CL, GEN>,
+    cudaError_t e = cudaFuncSetAttribute(conv_f32_kernel<TM, RI, KC, STAGES, MINB, FROM_X, CL, GEN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    conv_f32_kernel<TM, KC, STAGES, MINB, FROM_X, CL, GEN><<<grid, TM * 2, smem, st>>>(p);
+    conv_f32_kernel<TM, RI, KC, STAGES, MINB, FROM_X, CL, GEN><<<grid, TM / RI * 16, smem, st>>>(p);
     return cudaGetLastError();
 }
 
