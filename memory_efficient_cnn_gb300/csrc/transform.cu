@@ -21,6 +21,11 @@
 //    vector straight to win (coalesced 128-bit stores across the warp). The
 //    unaligned head and tail of the range are written element by element, so
 //    neighbouring CTAs never overlap.
+//  * 16-bit elements in rows of whole 16-byte vectors (W_i a multiple of 8)
+//    skip the staging: a thread loads the H_f vectors under 8 columns of a
+//    window row and interleaves them in registers (transform_rows16), which
+//    replaces 8 gathered 2-byte shared-memory loads per output vector by two
+//    byte permutes per output word.
 // The element type is the raw bit pattern (uint16_t / uint32_t), so the copy
 // is bit-exact for every dtype.
 #include <algorithm>
@@ -235,6 +240,78 @@ __global__ void __launch_bounds__(kThreads) transform_kernel(TParams p) {
     }
 }
 
+// 16-bit elements, W_i a multiple of 8 (every input row and window row starts
+// on a 16-byte boundary) and H_f at most kMaxRowsHf: an item is one 8-column
+// group g of one window row (plane, ho). Its window positions are the 8*H_f
+// consecutive elements win[plane][ho][8g*H_f + e], e = c*H_f + r, holding
+// x[plane][ho*s_h + r][8g + c]: the H_f input vectors under the group, read
+// with one 16-byte load each, interleaved in registers (two elements per byte
+// permute, all indices fixed at compile time) into H_f output vectors.
+// Consecutive items are consecutive in win, so a warp's 32 items are one
+// contiguous range of 32*H_f vectors: each thread puts its vectors in the
+// warp's staging area, and the warp stores the range with 16-byte stores that
+// are contiguous across its lanes. For s_h = 1 the lanes' loads of one r are
+// contiguous too (the rows of a plane follow one another in x). (For 32-bit
+// elements the staged kernel below is as fast: its vectors need no gathers.)
+constexpr int kMaxRowsHf = 12;
+
+struct TRParams {
+    const uint4 *x;
+    uint4 *win;
+    int items;            // N * C_i * H_o * (W_i / 8)
+    int H_i, s_h;
+    int rvec;             // 16-byte vectors per input row (W_i / 8)
+    FastDiv div_G, div_Ho;  // column groups per window row, output rows per plane
+};
+
+template <int HF>
+__global__ void __launch_bounds__(kThreads) transform_rows16(TRParams p) {
+    extern __shared__ uint4 tr_stage[];  // [warp][32 * HF]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint4 *stage = tr_stage + warp * 32 * HF;
+    const int item0 = (blockIdx.x * (kThreads / 32) + warp) * 32;  // the warp's first item
+    if (item0 >= p.items) return;
+    const int item = item0 + lane;
+    uint32_t in[HF][4];
+    if (item < p.items) {
+        const int wr = (int)fdiv((uint32_t)item, p.div_G);  // window row = plane*H_o + ho
+        const int g = item - wr * (int)p.div_G.d;
+        const int plane = (int)fdiv((uint32_t)wr, p.div_Ho);
+        const int ho = wr - plane * (int)p.div_Ho.d;
+        const uint4 *src = p.x + ((int64_t)plane * p.H_i + (int64_t)ho * p.s_h) * p.rvec + g;
+#pragma unroll
+        for (int r = 0; r < HF; ++r) {
+            const uint4 v = __ldg(src + (int64_t)r * p.rvec);
+            in[r][0] = v.x;
+            in[r][1] = v.y;
+            in[r][2] = v.z;
+            in[r][3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < HF; ++r) in[r][0] = in[r][1] = in[r][2] = in[r][3] = 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < HF; ++i) {
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            // elements e = 8i + 2k and e + 1, element (c, r) being half c % 2 of word
+            // c / 2 of input vector r
+            const int e0 = 8 * i + 2 * k, e1 = e0 + 1;
+            const int c0 = e0 / HF, r0 = e0 % HF, c1 = e1 / HF, r1 = e1 % HF;
+            const uint32_t sel = (uint32_t)((2 * (c0 & 1)) | ((2 * (c0 & 1) + 1) << 4) |
+                                            ((4 + 2 * (c1 & 1)) << 8) | ((5 + 2 * (c1 & 1)) << 12));
+            o[k] = __byte_perm(in[r0][c0 >> 1], in[r1][c1 >> 1], sel);
+        }
+        stage[lane * HF + i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    __syncwarp();
+    const int nvec = min(32, p.items - item0) * HF;
+    uint4 *dst = p.win + (int64_t)item0 * HF;
+    for (int j = lane; j < nvec; j += 32) dst[j] = stage[j];
+}
+
 // The lane bit whose lanes gather in the flipped order (-1: none) for 16-bit
 // vectors over rows of pitch Wc and H_f rows: a model of the gather's
 // shared-memory wavefronts (most distinct 4-byte words one bank serves, per
@@ -290,8 +367,55 @@ int sm_count() {
 
 }  // namespace
 
+// Whether the register-interleave kernel covers the shape (and the buffers'
+// alignment).
+static bool rows16_covers(const void *x, const void *win, const Shape &s, int esz) {
+    if (esz != 2 || s.W_i % 8 != 0 || s.H_f < 1 || s.H_f > kMaxRowsHf) return false;
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(win)) & 15) return false;
+    const int64_t items = s.N * s.C_i * s.H_o * (s.W_i / 8);
+    return items + 256 < (1ll << 31) && s.N * s.C_i * s.H_o < (1ll << 31);
+}
+
+template <int HF>
+static cudaError_t launch_rows16_hf(const TRParams &p, cudaStream_t st) {
+    const size_t smem = (size_t)(kThreads / 32) * 32 * HF * 16;
+    const cudaError_t e = cudaFuncSetAttribute(transform_rows16<HF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+    if (e != cudaSuccess) return e;
+    const unsigned blocks = (unsigned)((p.items + kThreads - 1) / kThreads);
+    transform_rows16<HF><<<blocks, kThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+static cudaError_t launch_rows16(const void *x, void *win, const Shape &s, cudaStream_t st) {
+    TRParams p;
+    p.x = static_cast<const uint4 *>(x);
+    p.win = static_cast<uint4 *>(win);
+    p.items = (int)(s.N * s.C_i * s.H_o * (s.W_i / 8));
+    p.H_i = (int)s.H_i;
+    p.s_h = (int)s.s_h;
+    p.rvec = (int)(s.W_i / 8);
+    p.div_G = make_fastdiv((uint32_t)(s.W_i / 8));
+    p.div_Ho = make_fastdiv((uint32_t)s.H_o);
+    switch (s.H_f) {
+        case 1: return launch_rows16_hf<1>(p, st);
+        case 2: return launch_rows16_hf<2>(p, st);
+        case 3: return launch_rows16_hf<3>(p, st);
+        case 4: return launch_rows16_hf<4>(p, st);
+        case 5: return launch_rows16_hf<5>(p, st);
+        case 6: return launch_rows16_hf<6>(p, st);
+        case 7: return launch_rows16_hf<7>(p, st);
+        case 8: return launch_rows16_hf<8>(p, st);
+        case 9: return launch_rows16_hf<9>(p, st);
+        case 10: return launch_rows16_hf<10>(p, st);
+        case 11: return launch_rows16_hf<11>(p, st);
+        default: return launch_rows16_hf<12>(p, st);
+    }
+}
+
 cudaError_t launch_transform(const void *x, void *win, const Shape &s, int esz, cudaStream_t st) {
     if (s.N == 0) return cudaSuccess;
+    if (rows16_covers(x, win, s, esz)) return launch_rows16(x, win, s, st);
     const int64_t L = s.W_i * s.H_f;
     const int64_t NP = s.N * s.C_i;
     const int64_t full_rows = (s.H_o - 1) * s.s_h + s.H_f;  // input rows a plane's windows use

@@ -37,6 +37,9 @@ CASES = [  # N, C_i, H_i, W_i, H_f, s_h
     # plane, H_f >= 8, H_f = 1, many planes per CTA, stride = H_f, one output row
     (1, 3, 200, 64, 7, 1), (2, 4, 30, 16, 11, 3), (3, 5, 10, 8, 1, 1), (64, 32, 12, 8, 2, 2),
     (1, 2, 50, 96, 4, 4), (2, 3, 9, 40, 9, 1),
+    # 16-bit rows of whole 16-byte vectors, H_f up to 12, item counts not a multiple of 32
+    (2, 3, 20, 24, 12, 2), (1, 2, 14, 16, 6, 1), (1, 3, 12, 8, 8, 2), (2, 2, 15, 32, 10, 5),
+    (1, 1, 5, 8, 3, 1),
 ]
 
 
@@ -68,9 +71,25 @@ def test_transform_does_not_write_past_the_window(W_i):
     assert _raw(buf[:n]).tobytes() == oracle.im2win(_raw(x), H_f, s_h).tobytes()
 
 
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_transform_window_not_16_byte_aligned_is_refused(dt):
+    # the entry points take 16-byte aligned buffers; one element past a boundary is
+    # refused before any launch, and the buffer is left as it was
+    x = torch.zeros((2, 3, 20, 32), dtype=DT[dt], device="cuda")
+    H_f, s_h = 5, 2
+    H_o = (20 - H_f) // s_h + 1
+    n = 2 * 3 * H_o * 32 * H_f
+    buf = torch.full((n + 16,), 3, dtype=DT[dt], device="cuda")
+    with pytest.raises(mec.Im2winError, match="aligned"):
+        mec.im2win_transform(x, buf[1:n + 1], 1, H_f, 1, s_h, 1)
+    torch.cuda.synchronize()
+    assert torch.all(buf == 3)
+
+
 @pytest.mark.parametrize("layer,dt", [(wl.CV1, "f16"), (wl.CV1, "f32"), (wl.CV2, "f16"), (wl.CV3, "f32"),
                                       (wl.CV5, "bf16")]
-                         + [(l, "bf16") for l in wl.SWEEP], ids=lambda v: getattr(v, "name", v))
+                         + [(l, "bf16") for l in wl.SWEEP] + [(wl.SWEEP[1], "f32"), (wl.SWEEP[4], "f32")],
+                         ids=lambda v: getattr(v, "name", v))
 def test_transform_full_size_bit_exact(layer, dt):
     x, _ = wl.make_inputs(layer, dt)
     _check(x, layer.H_f, layer.s_h)
