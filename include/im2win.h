@@ -251,10 +251,12 @@ typedef struct {
                                    input), 1 window rows of one channel from the input, 2 window rows
                                    from the window tensor, 3 channel slab of a channels-last tensor;
                                    -1 for the other kernels */
-    int32_t stacked;            /* 1: two filter taps per MMA along M (C_o <= 64) */
+    int32_t stacked;            /* C_o <= 64: two filter taps per MMA; 1: along M, 2: along N
+                                   with the output positions along M (TMEM double-buffered) */
     int32_t rows_per_tile;      /* output rows per tile */
     int32_t pitch;              /* accumulator columns per output row */
-    int32_t tmem_columns;       /* accumulator columns of the widest tile (<= 512) */
+    int32_t tmem_columns;       /* accumulator columns of the widest tile (<= 512; stacked 2: one
+                                   past the last column of the second buffer) */
     int32_t tmem_read_end;      /* one past the highest accumulator column the epilogue reads */
     int32_t smem_bytes;         /* dynamic shared memory per CTA */
     int32_t filter_stage_taps;  /* filter taps per shared-memory stage */

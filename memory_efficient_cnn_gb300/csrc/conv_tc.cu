@@ -342,6 +342,13 @@ constexpr int TAP_EPI_BLOCK_WORDS = 32 * 33;
 __host__ __device__ constexpr uint32_t tap_epi_bytes(int blocks) {
     return (uint32_t)(TAP_EPI_WARPS * blocks * TAP_EPI_BLOCK_WORDS * 4);
 }
+// Transposed stacking (positions along M): the epilogue stages no outputs; its
+// only shared memory is the hand-over of each lane quarter's first row,
+// [tile parity][M block][lane quarter][channel half][32] fp32 values.
+constexpr uint32_t TAP_XB_BYTES = 2 * 2 * 4 * 2 * 32 * 4;
+__host__ __device__ constexpr uint32_t tap_epi_region(int blocks, int xpose) {
+    return xpose ? TAP_XB_BYTES : tap_epi_bytes(blocks);
+}
 
 struct TapParams {
     const uint16_t *src;   // NCHW input (CH, WX), window tensor (WW), NHWC input (CL)
@@ -375,6 +382,7 @@ struct TapParams {
     FastDiv div_cgs, div_sh, div_sw;  // CH: 8-column groups per row, strides
     FastDiv div_vpc;       // CH with ring: 16-byte vectors per channel of a full tile's rows
     int stack;             // CH, C_o <= 64: two taps per MMA, stacked along M (see below)
+    int xpose;             // stacked, transposed: positions along M, the two taps along N
     int Gr;                // stacked: tap groups per filter row
     int nhwc;              // output out[n][ho][wo][co] (else out[n][co][ho][wo])
     FastDiv div_wi;        // CL: positions of a slab row (W_i, or Wp when padded)
@@ -467,11 +475,12 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     uint16_t *sRaw = reinterpret_cast<uint16_t *>(sB + (size_t)p.BST * p.stage_b);
     uint32_t *sE = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(sRaw) +
                                                 ((size_t)p.raw_elems * 2 + 127) / 128 * 128);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sE) + tap_epi_bytes(p.epi_blocks));
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sE) + tap_epi_region(p.epi_blocks, p.xpose));
     // [A stages][slab stages][raw rows (W modes)][epilogue staging] then
-    // bars: full_a[AST] | empty_a[AST] | full_b[BST] | empty_b[BST] | tmem_full[2] | tmem_empty[2]
+    // bars: full_a[AST] | empty_a[AST] | full_b[BST] | empty_b[BST] | tmem_full[4] | tmem_empty[4]
     //       | drain | stacked hand-over: full[4] | empty[4] | raw slot full[2]
-    const int nb = 2 * p.AST + 2 * p.BST + 5 + 8 + 2;
+    const int nb = 2 * p.AST + 2 * p.BST + 9 + 8 + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + nb);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
     uint32_t *toff = reinterpret_cast<uint32_t *>(bars + nb + 1);  // [T] tap offsets (16-byte units)
@@ -503,14 +512,16 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
     auto full_b = [&](int s) { return smem_u32(bars + 2 * p.AST + s); };
     auto empty_b = [&](int s) { return smem_u32(bars + 2 * p.AST + p.BST + s); };
     // one full / empty pair per accumulator: the epilogue drains accumulator 0 and
-    // then 1, so each issuer restarts as soon as its own accumulator is drained
+    // then 1, so each issuer restarts as soon as its own accumulator is drained.
+    // Accumulator 2*buf + which: transposed stacking double-buffers (buf = tile
+    // parity), the other layouts use buf 0 only.
     auto tmem_full = [&](int a) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + a); };
-    auto tmem_empty = [&](int a) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 2 + a); };
-    const uint32_t drain = smem_u32(bars + 2 * p.AST + 2 * p.BST + 4);
-    auto xfull = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 5 + i); };
-    auto xempty = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 9 + i); };
+    auto tmem_empty = [&](int a) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 4 + a); };
+    const uint32_t drain = smem_u32(bars + 2 * p.AST + 2 * p.BST + 8);
+    auto xfull = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 9 + i); };
+    auto xempty = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 13 + i); };
     // raw staging slots (TAP_CH ring, TAP_WX, TAP_WW): their bulk copies complete here
-    auto raw_full = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 13 + i); };
+    auto raw_full = [&](int i) { return smem_u32(bars + 2 * p.AST + 2 * p.BST + 17 + i); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.AST; ++s) {
@@ -523,7 +534,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             mbar_init(full_b(s), one_group ? TAP_PROD_WARPS * 32 : TAP_PROD_WARPS * 16);
             mbar_init(empty_b(s), 2);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < 4; ++a) {
             mbar_init(tmem_full(a), 1);
             mbar_init(tmem_empty(a), TAP_EPI_WARPS);
         }
@@ -576,18 +587,35 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             TapTile tl;
             for (int64_t id = blockIdx.x; ok && id < p.tiles_total; id += gridDim.x) {
                 tile_at(p, id, tl);
-                if (k > 0) {
-                    // the previous tile's accumulators must be drained
-                    if (!(ok = bar_wait(tmem_empty(which), (k - 1) & 1, ctl, SITE_EMPTY_MMA))) break;
+                // transposed stacking: tile k uses TMEM buffer k & 1, last used by tile k - 2
+                const int buf = p.xpose ? (k & 1) : 0;
+                const int acc = 2 * buf + which;
+                if (p.xpose ? k >= 2 : k > 0) {
+                    // the accumulator's previous tile must be drained
+                    const uint32_t par = (uint32_t)(p.xpose ? (k >> 1) - 1 : k - 1) & 1u;
+                    if (!(ok = bar_wait(tmem_empty(acc), par, ctl, SITE_EMPTY_MMA))) break;
                     tc_fence_after();
                 }
-                // stacked: one more column, read by the epilogue for the shifted rows
-                const int NTp = (tl.Q * p.pitch + p.stack + 15) / 16 * 16;
-                const int N0 = tile_n0(p, NTp);
-                const int NW = which == 0 ? N0 : NTp - N0;          // this issuer's columns
-                const uint32_t col0 = which == 0 ? 0u : (uint32_t)N0;
-                const uint32_t idesc = make_idesc(p.bf16 != 0, BM, NW > 0 ? NW : 16);
-                const uint32_t d_tmem = tmem + col0;
+                int NW;          // this issuer's accumulator columns (0: none this tile)
+                uint32_t col0;   // first slab position its MMAs read, relative to the tile
+                uint32_t idesc, d_tmem;
+                if (p.xpose) {
+                    // M block `which` (positions which*128 ..) of the tile's Q*pitch + 1
+                    // positions; D = slab rows x filter rows, 128 x 128
+                    const int nmb = (tl.Q * p.pitch + 1 + 127) / 128;
+                    NW = which < nmb ? 128 : 0;
+                    col0 = (uint32_t)which * 128u;
+                    idesc = make_idesc(p.bf16 != 0, 128, 128);
+                    d_tmem = tmem + (uint32_t)(buf * 256 + which * 128);
+                } else {
+                    // stacked: one more column, read by the epilogue for the shifted rows
+                    const int NTp = (tl.Q * p.pitch + p.stack + 15) / 16 * 16;
+                    const int N0 = tile_n0(p, NTp);
+                    NW = which == 0 ? N0 : NTp - N0;
+                    col0 = which == 0 ? 0u : (uint32_t)N0;
+                    idesc = make_idesc(p.bf16 != 0, BM, NW > 0 ? NW : 16);
+                    d_tmem = tmem + col0;
+                }
                 for (int cc = 0; cc < p.NCH && ok; ++cc) {
                     if (!(ok = bar_wait(full_b(sb), phb, ctl, SITE_FULL_B))) break;
                     // CL: the slab was written by cp.async (generic proxy), the MMAs read
@@ -595,18 +623,31 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     if (MODE == TAP_CL) fence_async_smem();
                     const uint32_t b_lo_slab = b_lo_base + (uint32_t)sb * b_stage16 + col0;
                     for (int t0 = 0; t0 < p.T && ok; t0 += p.TG) {
+                        // (the filter tile arrived by a bulk copy completing on the barrier:
+                        // no tcgen05 fence is needed for the MMAs to read it, and one per
+                        // stage costs the issuer ~12% of the MMA rate)
                         if (!(ok = bar_wait(full_a(sa), pha, ctl, SITE_FULL_A))) break;
-                        tc_fence_after();
                         if (NW > 0) {
                             const int t_end = min(p.T, t0 + p.TG);
                             uint32_t a_lo = a_lo_base + (uint32_t)sa * a_stage16;
                             uint32_t off = toff[t0];
-                            for (int t = t0; t < t_end; ++t, a_lo += TAP_A_BYTES >> 4) {
-                                const uint32_t off_next = toff[t + 1 < t_end ? t + 1 : t];
-                                const uint64_t ad = ((uint64_t)a_hi << 32) | a_lo;
-                                const uint64_t bd = ((uint64_t)b_hi << 32) | (b_lo_slab + off);
-                                mma_f16(d_tmem, ad, bd, idesc, (cc | t) != 0);
-                                off = off_next;
+                            if (p.xpose) {
+                                // the slab is the M operand, the filter tile the N one
+                                for (int t = t0; t < t_end; ++t, a_lo += TAP_A_BYTES >> 4) {
+                                    const uint32_t off_next = toff[t + 1 < t_end ? t + 1 : t];
+                                    const uint64_t ad = ((uint64_t)a_hi << 32) | a_lo;
+                                    const uint64_t bd = ((uint64_t)b_hi << 32) | (b_lo_slab + off);
+                                    mma_f16(d_tmem, bd, ad, idesc, (cc | t) != 0);
+                                    off = off_next;
+                                }
+                            } else {
+                                for (int t = t0; t < t_end; ++t, a_lo += TAP_A_BYTES >> 4) {
+                                    const uint32_t off_next = toff[t + 1 < t_end ? t + 1 : t];
+                                    const uint64_t ad = ((uint64_t)a_hi << 32) | a_lo;
+                                    const uint64_t bd = ((uint64_t)b_hi << 32) | (b_lo_slab + off);
+                                    mma_f16(d_tmem, ad, bd, idesc, (cc | t) != 0);
+                                    off = off_next;
+                                }
                             }
                         }
                         mma_commit(empty_a(sa));
@@ -615,7 +656,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     if (ok) mma_commit(empty_b(sb));
                     if (++sb == p.BST) { sb = 0; phb ^= 1; }
                 }
-                if (ok) mma_commit(tmem_full(which));
+                if (ok) mma_commit(tmem_full(acc));
                 ++k;
             }
             // let every MMA in flight finish before the CTA tears down
@@ -1113,7 +1154,113 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                               : p.out + ((int64_t)tl.n * p.C_o + co0) * plane + (int64_t)tl.ho0 * p.W_o;
             };
             const int64_t ostride = p.nhwc ? (int64_t)p.C_o : plane;
-            if (!p.stack) {
+            if (p.xpose) {
+                // Transposed stacking: accumulator 2*buf + mb holds, in TMEM lane i,
+                // position mb*128 + i of the tile; columns 0..63 the first taps' sums
+                // for channel n, 64..127 the second taps' sums for channel n - 64,
+                // which belong to the position one to the left. So output (position
+                // pp, channel co) = D[pp][co] + D[pp + 1][64 + co]: the next lane of
+                // the same warp, except for a lane quarter's last row, whose partner
+                // is the next quarter's (or next M block's) first row. Each warp
+                // (lane quarter q4, channel half hh) first hands its first row's
+                // second-tap values over through shared memory; after the epilogue
+                // warps meet, it adds the next lane's values by a shuffle.
+                const int buf = k & 1;
+                const uint32_t par = (uint32_t)(k >> 1) & 1u;
+                const int NT = tl.Q * p.pitch;
+                const int nmb = (NT + 1 + 127) / 128;
+                float *xk = reinterpret_cast<float *>(sE) + (k & 1) * 512;  // [mb][q4][hh][32]
+                const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(buf * 256);
+                const bool okw = warp_bar_wait(tmem_full(2 * buf), par, ctl, SITE_DONE) &&
+                                 warp_bar_wait(tmem_full(2 * buf + 1), par, ctl, SITE_DONE);
+                if (okw) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int mb = 0; mb < nmb; ++mb) {
+                        uint32_t u[32];
+                        tmem_ld32(tq + (uint32_t)(mb * 128 + 64 + hh * 32), u);
+                        tmem_wait_ld();
+                        if (lane == 0) {
+                            float4 *d = reinterpret_cast<float4 *>(xk + ((mb * 4 + q4) * 2 + hh) * 32);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                d[i] = make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                                                   __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+                        }
+                    }
+                }
+                // every epilogue warp meets here once per tile; a failed wait in any
+                // of them ends all of them. The hand-over area alternates with the
+                // tile's parity: a warp writes the next tile's values only after
+                // every warp has passed this tile's meeting, so nobody still reads them.
+                ok = bar_red_and(5, TAP_EPI_WARPS * 32, okw);
+                if (ok) {
+                    const int pitch = p.pitch, W_o = p.W_o;
+                    const int c_base = hh * 32;
+                    const int nco = min(32, p.C_o - c_base);  // this warp's channels
+#pragma unroll 1
+                    for (int mb = 0; mb < nmb && nco > 0; ++mb) {
+                        // the row after the quarter's last: the next quarter's first, or the
+                        // next M block's (none after the last: that row is no output's)
+                        const float *nx = q4 < 3 ? xk + ((mb * 4 + q4 + 1) * 2 + hh) * 32
+                                                 : (mb + 1 < nmb ? xk + (((mb + 1) * 4) * 2 + hh) * 32 : nullptr);
+                        const int pp = mb * 128 + q4 * 32 + lane;
+                        const int qrow = pp / pitch;
+                        const int wo = pp - qrow * pitch;
+                        const bool valid = pp < NT && wo < W_o;
+                        uint16_t *o = p.nhwc ? p.out + (((int64_t)tl.n * p.H_o + tl.ho0 + qrow) * W_o + wo) * p.C_o +
+                                                   c_base
+                                             : p.out + ((int64_t)tl.n * p.C_o + c_base) * plane +
+                                                   (int64_t)(tl.ho0 + qrow) * W_o + wo;
+                        // two halves of 16 channels (registers)
+#pragma unroll 1
+                        for (int h2 = 0; h2 < 2 && 16 * h2 < nco; ++h2) {
+                            uint32_t t[16], u[16];
+                            const uint32_t col = (uint32_t)(mb * 128 + c_base + 16 * h2);
+                            tmem_ld16(tq + col, t);
+                            tmem_ld16(tq + col + 64, u);
+                            tmem_wait_ld();
+                            // the sums, in place
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                float nxt = __shfl_down_sync(0xffffffffu, __uint_as_float(u[c]), 1);
+                                if (lane == 31) nxt = nx ? nx[16 * h2 + c] : 0.f;
+                                t[c] = __float_as_uint(__uint_as_float(t[c]) + nxt);
+                            }
+                            if (!valid) continue;
+                            const int nc = min(16, nco - 16 * h2);
+                            auto f = [&](int c) { return __uint_as_float(t[c]); };
+                            if (p.nhwc) {
+                                uint16_t *oh = o + 16 * h2;
+                                if (nc == 16 && (p.C_o & 7) == 0) {
+#pragma unroll
+                                    for (int i = 0; i < 2; ++i)
+                                        reinterpret_cast<uint4 *>(oh)[i] =
+                                            make_uint4(pack2(f(8 * i), f(8 * i + 1), p.bf16),
+                                                       pack2(f(8 * i + 2), f(8 * i + 3), p.bf16),
+                                                       pack2(f(8 * i + 4), f(8 * i + 5), p.bf16),
+                                                       pack2(f(8 * i + 6), f(8 * i + 7), p.bf16));
+                                } else {
+#pragma unroll
+                                    for (int c = 0; c < 16; ++c)
+                                        if (c < nc) oh[c] = cvt16(f(c), p.bf16);
+                                }
+                            } else {
+                                uint16_t *oh = o + (int64_t)(16 * h2) * plane;
+#pragma unroll
+                                for (int c = 0; c < 16; ++c)
+                                    if (c < nc) oh[(int64_t)c * plane] = cvt16(f(c), p.bf16);
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(tmem_empty(2 * buf));
+                        mbar_arrive(tmem_empty(2 * buf + 1));
+                    }
+                }
+            } else if (!p.stack) {
                 const int co0 = tl.mt * BM + q4 * 32;
                 uint16_t *out_c = out_at(co0);
                 for (int a = 0; a < 2 && ok; ++a) {
@@ -1310,11 +1457,19 @@ static double tile_cost(int64_t NT) {
     return 2.0 * n / rate + 0.15;  // relative units
 }
 
+// The same for transposed stacking: one 128 x 128 MMA per M block and K step, the
+// M blocks on their own issuers (MAC/clk/SM measured for M = N = 128 with A and
+// B in shared memory: one issuer 2096, two 3210), in the units of tile_cost.
+static double tile_cost_xpose(int64_t NT) {
+    const int64_t nmb = (NT + 1 + 127) / 128;
+    return (nmb == 1 ? 128.0 / 2096.0 : 256.0 / 3210.0) + 0.15;
+}
+
 // Tiling of a tap kernel for a shape (mode TAP_CH / TAP_WX / TAP_WW) on `sms`
 // SMs, or !ok: the tiling with the least modelled time among those whose slab
 // stages fit shared memory. Whether a plan exists, and its filter layout, do
 // not depend on `sms`.
-TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks) {
+TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool xpose = false) {
     TapPlan pl{};
     pl.ok = false;
     pl.mode = mode;
@@ -1330,6 +1485,7 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks) {
     // counts tap groups
     const int stack = (chan && s.C_o <= 64 && s.W_f > s.s_w && s.d_h == 1 && s.d_w == 1) ? 1 : 0;
     const int Gr = stack ? stacked_groups_per_row((int)s.W_f, (int)s.s_w) : 0;
+    if (xpose && !stack) return pl;
     if (chan) {
         pitch = (Wp + s.s_w - 1) / s.s_w;
         T = stack ? s.H_f * Gr : s.H_f * s.W_f;
@@ -1345,8 +1501,9 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks) {
         if (s.H_o * s.W_i * s.H_f >= (1ll << 31)) return pl;
     }
     // stacked tiles need one more accumulator column, and the epilogue reads one
-    // column past a 64-column block: at most 448 columns
-    const int64_t max_nt = stack ? 448 - 1 : TAP_MAX_NT;
+    // column past a 64-column block: at most 448 columns; transposed stacking
+    // double-buffers at most two M blocks of 128 positions
+    const int64_t max_nt = xpose ? 2 * 128 - 1 : stack ? 448 - 1 : TAP_MAX_NT;
     if (pitch > max_nt || T > 4096) return pl;
     const int64_t Qcap = std::min<int64_t>(s.H_o, max_nt / pitch);
     const int64_t MT = (s.C_o + BM - 1) / BM;
@@ -1359,10 +1516,11 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks) {
             const int64_t q = (s.H_o + tps - 1) / tps;
             const int64_t tiles = s.N * MT * tps;
             const int64_t rounds = (tiles + sms - 1) / sms;
-            const double t = (double)rounds * tile_cost(q * pitch);
+            const double t = (double)rounds * (xpose ? tile_cost_xpose(q * pitch) : tile_cost(q * pitch));
             if (t < best * 0.99) { best = t; Q = q; }
         }
-        const int64_t NTp = (Q * pitch + stack + 15) / 16 * 16;
+        // positions the MMAs read from the slab (transposed: whole M blocks)
+        const int64_t NTp = xpose ? (Q * pitch + 1 + 127) / 128 * 128 : (Q * pitch + stack + 15) / 16 * 16;
         const int64_t RR = (Q - 1) * s.s_h + Hfe;  // slab rows under a tile of Q rows
         int64_t PB = 0, lbo, stage_b;
         if (chan) {
@@ -1409,7 +1567,7 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks) {
             for (int BST : {3, 2}) {
               for (int AST : {3, 2, 4}) {
                     int64_t total = (int64_t)AST * tg * TAP_A_BYTES + BST * stage_b + raw_e * 2 +
-                                    tap_epi_bytes(epi_blocks) + 512 + 4 * T + 16 + 128 * U;
+                                    tap_epi_region(epi_blocks, xpose) + 512 + 4 * T + 16 + 128 * U;
                     if (total > smem_max) continue;
                     // the 512-column TMEM accumulator needs the SM to itself
                     total = std::max<int64_t>(total, 120 * 1024);
@@ -1421,13 +1579,14 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks) {
                     p.NCH = (int)NCH;
                     p.T = (int)T;
                     p.stack = stack;
+                    p.xpose = xpose ? 1 : 0;
                     p.Gr = Gr;
                     p.p_h = (int)s.p_h; p.p_w = (int)s.p_w;
                     p.dil_h = (int)s.d_h; p.dil_w = (int)s.d_w; p.g_w = (int)s.g_w;
                     p.Hfe = (int)Hfe;
                     p.Wp = (int)Wp;
                     p.padded = (s.p_h > 0 || s.p_w > 0) ? 1 : 0;
-                    p.epi_blocks = epi_blocks;
+                    p.epi_blocks = xpose ? 0 : epi_blocks;
                     p.TG = tg;
                     p.ntg = (int)((T + tg - 1) / tg);
                     p.Qmax = (int)Q;
@@ -1467,6 +1626,9 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks) {
 // stages of at least min(T, 8) taps as with one block; one block otherwise, and
 // always with tap stacking (its drain goes block by block).
 TapPlan plan_tap(const Shape &s, int mode, int64_t sms) {
+    // tap stacking with rows of at most 255 positions: transposed, TMEM double-buffered
+    const TapPlan x = plan_tap_epi(s, mode, sms, 0, true);
+    if (x.ok) return x;
     const TapPlan one = plan_tap_epi(s, mode, sms, 1);
     if (!one.ok || one.p.stack) return one;
     const TapPlan two = plan_tap_epi(s, mode, sms, 2);
@@ -1606,10 +1768,24 @@ bool conv_tc_plan_info(const Shape &s, bool fused, int layout, int64_t sms, TcPl
     const TapParams &p = pl.p;
     info.kernel = 1;
     info.tap_mode = pl.mode;
-    info.stacked = p.stack;
+    info.stacked = p.stack ? (p.xpose ? 2 : 1) : 0;
     info.rows_per_tile = p.Qmax;
     info.pitch = p.pitch;
     const int NT = p.Qmax * p.pitch;  // the widest tile's positions
+    if (p.xpose) {
+        // two TMEM buffers of up to two 128-column M blocks; the MMAs write, and the
+        // epilogue reads, buffer 1 up to its last M block's end
+        const int nmb = (NT + 1 + 127) / 128;
+        info.tmem_columns = 256 + nmb * 128;
+        info.tmem_read_end = info.tmem_columns;
+        info.smem_bytes = (int)pl.smem;
+        info.filter_stage_taps = p.TG;
+        info.filter_stages = p.AST;
+        info.slab_stages = p.BST;
+        info.tiles = p.tiles_total;
+        info.grid = std::min<int64_t>(sms, p.tiles_total);
+        return true;
+    }
     const int NTp = (NT + p.stack + 15) / 16 * 16;
     info.tmem_columns = NTp;
     // The epilogue's column walk: the two warps of a lane quarter split a range in

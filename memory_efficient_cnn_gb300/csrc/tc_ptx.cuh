@@ -49,6 +49,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// The same with a suspend-time hint: a thread whose phase is not complete sleeps
+// in hardware until it completes or `ns` nanoseconds pass, instead of returning
+// at once; polling warps then take no issue slots from the warps they share a
+// scheduler with (the MMA issuers among them).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 // bulk copy global -> shared::cta, completion counted in bytes on `bar`
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
     asm volatile(
@@ -110,6 +124,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr)
         : "memory");
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t &r) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
 }
@@ -159,7 +183,7 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, const Ct
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (honour_abort && *c.abort_flag) return false;
         if ((spin & 255u) == 0 && globaltimer() - t0 > kTimeoutNs) {
             *c.abort_flag = 1;
@@ -178,6 +202,24 @@ __device__ __forceinline__ bool warp_bar_wait(uint32_t bar, uint32_t parity, con
     int ok = 0;
     if ((threadIdx.x & 31) == 0) ok = bar_wait(bar, parity, c, site) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Named barrier `id` over `count` threads (a multiple of 32) that also returns
+// whether `v` held in every one of them.
+__device__ __forceinline__ bool bar_red_and(int id, int count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// One fp32 value rounded to fp16 / bf16 (round to nearest even), as its bits.
+__device__ __forceinline__ uint16_t cvt16(float v, int bf16) {
+    return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int bf16) {

@@ -58,7 +58,13 @@ def test_conv_tc_exact_on_sparse_integers(dt, bound, fused):
 
 @pytest.mark.parametrize("fused", [False, True], ids=["window", "fused"])
 @pytest.mark.parametrize("case", [(2, 24, 30, 33, 40, 5, 3, 1, 2), (1, 40, 21, 29, 64, 7, 7, 2, 2),
-                                  (2, 17, 19, 40, 8, 3, 4, 1, 1)],
+                                  (2, 17, 19, 40, 8, 3, 4, 1, 1),
+                                  # tiles of two M blocks (positions past 128) with positions
+                                  # along M: the shifted add crosses lane quarters and blocks
+                                  (1, 24, 12, 150, 40, 5, 3, 1, 2), (2, 16, 9, 200, 64, 3, 4, 1, 1),
+                                  (1, 32, 17, 224, 64, 7, 7, 2, 2),
+                                  # 1120 tiles: every CTA reuses both TMEM buffers several times
+                                  (160, 8, 9, 200, 16, 3, 4, 1, 1)],
                          ids=lambda c: "x".join(map(str, c)))
 def test_conv_tc_stacked_taps_exact_on_integers(case, fused):
     """Output channels <= 64: two filter taps share one MMA (the second tap's sum is

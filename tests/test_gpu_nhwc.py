@@ -115,7 +115,10 @@ def test_conv_nhwc_small(case, dt, fused):
 
 @pytest.mark.parametrize("fused", [False, True], ids=["window", "fused"])
 @pytest.mark.parametrize("case", [(2, 24, 30, 31, 150, 5, 3, 1, 2), (2, 24, 30, 33, 40, 5, 3, 1, 2),
-                                  (1, 40, 21, 29, 64, 7, 7, 2, 2), (2, 12, 19, 40, 20, 3, 4, 1, 1)],
+                                  (1, 40, 21, 29, 64, 7, 7, 2, 2), (2, 12, 19, 40, 20, 3, 4, 1, 1),
+                                  # stacked tiles of two M blocks; many tiles per CTA
+                                  (1, 24, 12, 150, 48, 5, 3, 1, 2), (2, 16, 9, 200, 64, 3, 4, 1, 1),
+                                  (160, 8, 9, 200, 16, 3, 4, 1, 1)],
                          ids=lambda c: "x".join(map(str, c)))
 def test_conv_nhwc_exact_on_sparse_integers(case, fused):
     """Sparse +-1 inputs: every fp32 partial sum is an exact small integer and the

@@ -48,11 +48,18 @@ def check_plan(info, shape, pad=(0, 0), dil=(1, 1), layout=mec.NCHW, dtype=mec.F
     assert 0 < info["smem_bytes"] <= SMEM_PER_CTA
     assert 2 * info["smem_bytes"] > SMEM_PER_SM  # one CTA per SM: its 512 TMEM columns are the SM's
     assert info["rows_per_tile"] >= 1 and info["pitch"] >= 1
-    # the MMAs write, and the epilogue reads, every column of the widest tile (plus
-    # the shifted one when stacked), all inside the CTA's allocation
-    need = info["rows_per_tile"] * info["pitch"] + info["stacked"]
-    assert need <= info["tmem_columns"] <= TMEM_COLUMNS
-    assert need <= info["tmem_read_end"] <= TMEM_COLUMNS
+    if info["stacked"] == 2:
+        # transposed stacking: the tile's positions (plus the shifted one) in M blocks
+        # of 128 TMEM lanes, two buffers of 256 columns (128 per M block)
+        nmb = math.ceil((info["rows_per_tile"] * info["pitch"] + 1) / 128)
+        assert nmb <= 2
+        assert info["tmem_columns"] == info["tmem_read_end"] == 256 + 128 * nmb <= TMEM_COLUMNS
+    else:
+        # the MMAs write, and the epilogue reads, every column of the widest tile (plus
+        # the shifted one when stacked), all inside the CTA's allocation
+        need = info["rows_per_tile"] * info["pitch"] + info["stacked"]
+        assert need <= info["tmem_columns"] <= TMEM_COLUMNS
+        assert need <= info["tmem_read_end"] <= TMEM_COLUMNS
     assert info["tiles"] == N * math.ceil(C_o / 128) * math.ceil(H_o / info["rows_per_tile"])
     assert info["grid"] == min(sms, info["tiles"])
     assert info["filter_stage_taps"] >= 1 and info["filter_stages"] >= 2 and info["slab_stages"] >= 2
@@ -85,7 +92,7 @@ def test_large_channel_layers_run_the_tap_kernel(layer):
             info = mec.im2win_plan(op, *layer.shape_args, layout=layout, dtype=mec.BF16, sms=SMS)
             assert info["kernel"] == mec.KERNEL_TAP
             assert info["grid"] == SMS
-            assert info["stacked"] == (1 if layer.C_o <= 64 else 0)
+            assert (info["stacked"] > 0) == (layer.C_o <= 64)
 
 
 def test_default_sm_count_without_a_device_is_a_full_grid():
