@@ -1556,16 +1556,30 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
         // slots (the next chunk's copy in flight) before one slot (TAP_W*) or none
         // (TAP_CH); then larger filter stages, then three slab stages, then three
         // filter stages
+        // Transposed stacking issues 128 x 128 MMAs, for which the issuers' fixed cost
+        // per filter stage is large: there the candidates are the fewest stages per
+        // chunk that fit (the smallest stage for each count), two stages first.
+        int tg_list[64], n_tg = 0;
+        if (xpose) {
+            for (int64_t ns = 1; ns <= T && n_tg < 64; ++ns) {
+                const int tg = (int)((T + ns - 1) / ns);
+                if (n_tg == 0 || tg_list[n_tg - 1] != tg) tg_list[n_tg++] = tg;
+            }
+        } else {
+            for (int v : {9, 8, 6, 5, 4, 3, 2, 1}) tg_list[n_tg++] = v;
+        }
+        const int ast_list[3] = {xpose ? 2 : 3, xpose ? 3 : 2, 4};
         for (int pass = 0; pass < 2; ++pass)
         for (int ring : {1, 0}) {
           const int64_t raw_e = chan ? (ring ? 2 * slot_e : 0) : (ring ? 2 : 1) * slot_e;
           if (ring && slot_e == 0) continue;
-          for (int TG : {9, 8, 6, 5, 4, 3, 2, 1}) {
+          for (int ti = 0; ti < n_tg; ++ti) {
+            const int TG = tg_list[ti];
             const int tg = (int)std::min<int64_t>(TG, T);
             if (TG > T && TG != 1) continue;
-            if (pass == 0 && tg < std::min<int64_t>(T, 8)) continue;
+            if (pass == 0 && !xpose && tg < std::min<int64_t>(T, 8)) continue;
             for (int BST : {3, 2}) {
-              for (int AST : {3, 2, 4}) {
+              for (int AST : ast_list) {
                     int64_t total = (int64_t)AST * tg * TAP_A_BYTES + BST * stage_b + raw_e * 2 +
                                     tap_epi_region(epi_blocks, xpose) + 512 + 4 * T + 16 + 128 * U;
                     if (total > smem_max) continue;
