@@ -35,6 +35,8 @@
 // copies and MMAs, frees TMEM and exits.
 #include <algorithm>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -351,6 +353,10 @@ __host__ __device__ constexpr uint32_t tap_epi_region(int blocks, int xpose) {
 }
 
 struct TapParams {
+    // CH with a raw ring: the input as a 4-D tensor (W_i, H_i, C_i, N) whose box
+    // (W_i, raw rows, 16 channels, 1) is one chunk's raw rows (tma_raw)
+    alignas(64) CUtensorMap tmap_x;
+    int tma_raw;
     const uint16_t *src;   // NCHW input (CH, WX), window tensor (WW), NHWC input (CL)
     const uint16_t *fa;
     uint16_t *out;
@@ -728,7 +734,17 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         };
         auto issue_raw = [&](const TapTile &t, int cc, int slot) {
             const uint32_t dst0 = smem_u32(sRaw + (size_t)slot * p.raw_slot);
-            if (MODE == TAP_CH) {
+            if (MODE == TAP_CH && p.tma_raw) {
+                // Raw row lr of channel k is input row ho0*s_h - p_h + lr of channel
+                // cc*16 + k: one tensor copy of the box at (0, ho0*s_h - p_h, cc*16, n),
+                // rows outside the input and channels past C_i read as zero. (One copy:
+                // the copy engine takes bulk copies one at a time, at a fixed cost each.)
+                if (pt == 0) {
+                    const uint32_t bar = raw_full(slot);
+                    mbar_arrive_expect_tx(bar, (uint32_t)(16 * p.raw_ch) * 2u);
+                    tma_load_4d(dst0, &p.tmap_x, 0, t.ho0 * p.s_h - p.p_h, cc * 16, t.n, bar);
+                }
+            } else if (MODE == TAP_CH) {
                 // Raw row lr of channel k is input row ho0*s_h - p_h + lr of channel
                 // cc*16 + k. The rows that exist are one contiguous, 16-byte aligned range
                 // of each channel plane: one bulk copy per channel, completing on the
@@ -1833,6 +1849,42 @@ bool conv_tc_plan_info(const Shape &s, bool fused, int layout, int64_t sms, TcPl
     return true;
 }
 
+// cuTensorMapEncodeTiled, from the driver through the runtime (no link to the
+// driver library); null when the driver does not provide it.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// The tensor map of TAP_CH's raw rows: the kernel's input (16-bit elements; the
+// window tensor when it is read as one) as a 4-D tensor (W_i, H_i, C_i, N) of
+// the kernel's shape, box (W_i, raw rows, 16, 1), zero fill outside. False when
+// the box is out of the copy engine's limits (at most 256 per dimension) or the
+// encoder refuses it; the per-channel bulk copies then stage the rows.
+static bool encode_raw_map(TapParams &p, const void *src) {
+    const int64_t rows = p.raw_ch / p.W_i;
+    if (p.W_i > 256 || rows > 256 || (reinterpret_cast<uintptr_t>(src) & 15) != 0) return false;
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t W = (cuuint64_t)p.W_i, H = (cuuint64_t)p.H_i, C = (cuuint64_t)p.C_i;
+    const cuuint64_t dims[4] = {W, H, C, (cuuint64_t)p.N_img};
+    const cuuint64_t strides[3] = {W * 2, H * W * 2, C * H * W * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)W, (cuuint32_t)rows, 16u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = enc(&p.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(src), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *filt, void *out,
                               void *ws, const Shape &s, int layout, bool bf16, cudaStream_t st) {
     TapParams p = pl.p;
@@ -1859,6 +1911,7 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
     if (pl.mode == TAP_CL)  // 16-byte entries: 8 channels of one position
         p.vec = (p.C_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
     if (pl.mode == TAP_CH && !p.vec) p.ring = 0;  // 16-byte copies need 16-byte rows
+    p.tma_raw = (pl.mode == TAP_CH && p.ring && encode_raw_map(p, src)) ? 1 : 0;
     p.div_pitch = make_fastdiv((uint32_t)p.pitch);
     p.div_cgs = make_fastdiv((uint32_t)std::max(1, p.W_i / 8));
     p.div_sh = make_fastdiv((uint32_t)p.s_h);

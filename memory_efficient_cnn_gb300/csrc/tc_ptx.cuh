@@ -63,6 +63,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
         : "memory");
     return ok != 0;
 }
+// TMA tensor copy of one 4-D box (tile mode) global -> shared::cta at box
+// coordinates (x, y, z, w), completion counted in bytes on `bar`; elements
+// outside the tensor read as zero. `tmap` is the generic address of a tensor
+// map in kernel parameter space.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int x, int y, int z, int w,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+        : "memory");
+}
 // bulk copy global -> shared::cta, completion counted in bytes on `bar`
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
     asm volatile(
