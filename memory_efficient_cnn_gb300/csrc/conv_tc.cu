@@ -354,9 +354,13 @@ __host__ __device__ constexpr uint32_t tap_epi_region(int blocks, int xpose) {
 
 struct TapParams {
     // CH with a raw ring: the input as a 4-D tensor (W_i, H_i, C_i, N) whose box
-    // (W_i, raw rows, 16 channels, 1) is one chunk's raw rows (tma_raw)
+    // (W_i, raw rows, 16 channels, 1) is one chunk's raw rows (tma_raw). CL with
+    // whole 16-byte entries: the input as (C_i, W_i, H_i, N), box (8, pitch*s_w,
+    // rows per phase*s_h, 1) traversed with element strides (1, s_w, s_h, 1): one
+    // polyphase block of one 8-channel half of a chunk's slab (tma_slab).
     alignas(64) CUtensorMap tmap_x;
-    int tma_raw;
+    int tma_raw, tma_slab;
+    int slab_hh;           // CL with tma_slab: rows of a polyphase block
     const uint16_t *src;   // NCHW input (CH, WX), window tensor (WW), NHWC input (CL)
     const uint16_t *fa;
     uint16_t *out;
@@ -535,9 +539,12 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             mbar_init(empty_a(s), 2);  // both MMA issuers commit
         }
         // a slab stage is filled by one producer group (all producers when there is one)
+        // (with tma_slab one thread completes a stage: its arrival and the copies' bytes)
         const bool one_group = !(MODE == TAP_CH && (p.ring || p.stack));
         for (int s = 0; s < p.BST; ++s) {
-            mbar_init(full_b(s), one_group ? TAP_PROD_WARPS * 32 : TAP_PROD_WARPS * 16);
+            mbar_init(full_b(s), (MODE == TAP_CL && p.tma_slab) ? 1
+                                 : one_group                     ? TAP_PROD_WARPS * 32
+                                                                 : TAP_PROD_WARPS * 16);
             mbar_init(empty_b(s), 2);
         }
         for (int a = 0; a < 4; ++a) {
@@ -841,7 +848,45 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             fence_async_smem();
             asm volatile("bar.sync %0, %1;" ::"r"(3), "r"(TAP_PROD_WARPS * 32) : "memory");
         }
-        int64_t id = blockIdx.x;
+        if (MODE == TAP_CL && p.tma_slab && warp == 2) {
+            // Channels-last input in whole 16-byte entries: each polyphase block (ph_r,
+            // ph_c) of each 8-channel half of a chunk's slab is one tensor copy, entry
+            // (q, m) being input (row R0 + ph_r + q*s_h, column ph_c + m*s_w - p_w),
+            // zero outside the input. One thread issues them all on the stage's barrier;
+            // the other producer warps have nothing to do.
+            int sbt = 0;
+            uint32_t pht = 0;
+            bool ok2 = true;
+            int pend[3] = {-1, -1, -1};  // per stage: parity of a copy not yet seen landed
+            const uint32_t bytes = 2u * (uint32_t)(p.s_h * p.s_w * p.slab_hh * p.pitch) * 16u;
+            TapTile t2;
+            for (int64_t id2 = blockIdx.x; ok2 && id2 < p.tiles_total; id2 += gridDim.x) {
+                tile_at(p, id2, t2);
+                const int R0 = t2.ho0 * p.s_h - p.p_h;
+                for (int c2 = 0; c2 < p.NCH; ++c2) {
+                    if (!(ok2 = warp_bar_wait(empty_b(sbt), pht ^ 1, ctl, SITE_EMPTY_PROD))) break;
+                    if (lane == 0) {
+                        const uint32_t slab = smem_u32(sB + (size_t)sbt * p.stage_b);
+                        mbar_arrive_expect_tx(full_b(sbt), bytes);
+                        for (int c8 = 0; c8 < 2; ++c8)
+                            for (int pr = 0; pr < p.s_h; ++pr)
+                                for (int pc = 0; pc < p.s_w; ++pc)
+                                    tma_load_4d(slab + (uint32_t)c8 * p.lbo + (uint32_t)(pr * p.s_w + pc) * p.PB,
+                                                &p.tmap_x, c2 * 16 + c8 * 8, pc - p.p_w, R0 + pr, t2.n, full_b(sbt));
+                    }
+                    __syncwarp();
+                    pend[sbt] = (int)pht;
+                    if (++sbt == p.BST) { sbt = 0; pht ^= 1; }
+                }
+            }
+            // after a wait gave up, copies still in flight land before the CTA exits
+            if (!ok2 && lane == 0)
+                for (int s2 = 0; s2 < p.BST; ++s2)
+                    if (pend[s2] >= 0) bar_wait(full_b(s2), (uint32_t)pend[s2], ctl, SITE_DRAIN, false);
+            __syncwarp();
+        }
+        // (with tma_slab the loop below has nothing to do)
+        int64_t id = (MODE == TAP_CL && p.tma_slab) ? p.tiles_total : (int64_t)blockIdx.x;
         int cc = 0;
         TapTile tl;
         // raw staging (TAP_CH ring, TAP_WX, TAP_WW): parity of each slot's next
@@ -1541,7 +1586,9 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
         int64_t PB = 0, lbo, stage_b;
         if (chan) {
             const int64_t HH = (RR + s.s_h - 1) / s.s_h;
-            PB = HH * pitch * 16;
+            // a multiple of 128 bytes, so that every polyphase block of a stage can be the
+            // destination of a tensor copy (its tail past the block's rows is never written)
+            PB = (HH * pitch * 16 + 127) / 128 * 128;
             lbo = s.s_h * s.s_w * PB;
             int64_t max_tap = 0;
             for (int64_t r = 0; r < s.H_f; ++r)
@@ -1885,6 +1932,35 @@ static bool encode_raw_map(TapParams &p, const void *src) {
     return r == CUDA_SUCCESS;
 }
 
+// The tensor map of TAP_CL's slab: the kernel's channels-last input as a 4-D
+// tensor (C_i, W_i, H_i, N), box (8 channels, pitch*s_w columns, rows per
+// polyphase block * s_h, 1) traversed with element strides (1, s_w, s_h, 1), so
+// that one copy writes one polyphase block of one 8-channel half as its dense
+// [row][column][8 channels] entries; zero fill outside. False when out of the
+// copy engine's limits (box at most 256 and element strides at most 8 per
+// dimension) or the encoder refuses it; the producers' 16-byte copies fill the
+// slab instead.
+static bool encode_slab_map(TapParams &p, const void *src) {
+    const int64_t HH = ((int64_t)(p.Qmax - 1) * p.s_h + p.Hfe + p.s_h - 1) / p.s_h;  // rows of a polyphase block
+    // every block starts a multiple of PB into a 128-byte aligned stage: the copies'
+    // shared-memory destinations are 128-byte aligned only when PB is
+    if ((int64_t)p.pitch * p.s_w > 256 || HH * p.s_h > 256 || p.s_w > 8 || p.s_h > 8 || p.PB % 128 != 0 ||
+        p.stage_b % 128 != 0 || (reinterpret_cast<uintptr_t>(src) & 15) != 0)
+        return false;
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t W = (cuuint64_t)p.W_i, H = (cuuint64_t)p.H_i, C = (cuuint64_t)p.C_i;
+    const cuuint64_t dims[4] = {C, W, H, (cuuint64_t)p.N_img};
+    const cuuint64_t strides[3] = {C * 2, W * C * 2, H * W * C * 2};
+    const cuuint32_t box[4] = {8u, (cuuint32_t)(p.pitch * p.s_w), (cuuint32_t)(HH * p.s_h), 1u};
+    const cuuint32_t estr[4] = {1u, (cuuint32_t)p.s_w, (cuuint32_t)p.s_h, 1u};
+    const CUresult r = enc(&p.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(src), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    p.slab_hh = (int)HH;
+    return r == CUDA_SUCCESS;
+}
+
 static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *filt, void *out,
                               void *ws, const Shape &s, int layout, bool bf16, cudaStream_t st) {
     TapParams p = pl.p;
@@ -1912,6 +1988,7 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
         p.vec = (p.C_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
     if (pl.mode == TAP_CH && !p.vec) p.ring = 0;  // 16-byte copies need 16-byte rows
     p.tma_raw = (pl.mode == TAP_CH && p.ring && encode_raw_map(p, src)) ? 1 : 0;
+    p.tma_slab = (pl.mode == TAP_CL && p.vec && encode_slab_map(p, src)) ? 1 : 0;
     p.div_pitch = make_fastdiv((uint32_t)p.pitch);
     p.div_cgs = make_fastdiv((uint32_t)std::max(1, p.W_i / 8));
     p.div_sh = make_fastdiv((uint32_t)p.s_h);
