@@ -33,7 +33,11 @@
 #include <mutex>
 #include <utility>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "im2win_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace im2win {
 namespace {
@@ -688,9 +692,148 @@ __global__ void __launch_bounds__(256) transform_nhwc_staged(TNParams p) {
 
 constexpr int kNhwcStageBudget = 48 * 1024;  // staged input rows per CTA
 
+// Channels-last with C_i*esz a multiple of 16: window row (n, ho) is, for w in
+// [0, W_i), the H_f input positions (ho*s_h + r, w) of C_i contiguous elements.
+// Seen as a 4-D tensor of dimensions (C_i, rows, columns, N) — strides 1,
+// W_i*C_i, C_i and H_i*W_i*C_i elements — the box (C_i, H_f, Wc, 1) at
+// (0, ho*s_h, w0, n) lands in shared memory as [column][row][channel]: exactly
+// the window row's elements [w0*H_f*C_i, (w0 + Wc)*H_f*C_i). So a unit (n, ho,
+// column chunk) is one TMA tensor load and one bulk store of the same bytes;
+// columns past W_i (a short last chunk) read as zero and are not stored. Each
+// CTA is persistent: one thread cycles its units through a ring of kNhwcRing
+// shared-memory buffers, the loads of the next units in flight while a unit is
+// stored. The waits for the loads give up after 2 s (the CTA then stops; the
+// copy engine completes every load it accepted, so none is expected).
+constexpr int kNhwcRing = 3;
+constexpr int kNhwcBoxBytes = 32 * 1024;
+
+struct TTParams {
+    alignas(64) CUtensorMap tmap;
+    uint8_t *win;
+    int64_t units;        // N * H_o * chunks
+    int chunks, Wc;       // column chunks per window row, columns per chunk
+    int H_o, W_i, s_h;
+    uint32_t box_bytes;   // C_i * H_f * Wc * esz
+    uint32_t buf_bytes;   // box_bytes rounded up to 128 (each buffer 128-byte aligned)
+    uint32_t col_bytes;   // H_f * C_i * esz: one column of a window row
+};
+
+__global__ void __launch_bounds__(32, 1) transform_nhwc_tma(const __grid_constant__ TTParams p) {
+    extern __shared__ __align__(128) uint8_t tt_smem[];
+    __shared__ uint64_t full[kNhwcRing];
+    if (threadIdx.x != 0) return;
+    using namespace tc;
+    for (int b = 0; b < kNhwcRing; ++b) mbar_init(smem_u32(&full[b]), 1);
+    fence_mbar_init();
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t mine = first < p.units ? (p.units - first + step - 1) / step : 0;
+    auto load = [&](int64_t k) {  // the k-th unit of this CTA into buffer k % kNhwcRing
+        const int64_t u = first + k * step;
+        const int ch = (int)(u % p.chunks);
+        const int64_t r = u / p.chunks;
+        const int ho = (int)(r % p.H_o), n = (int)(r / p.H_o);
+        const int b = (int)(k % kNhwcRing);
+        const uint32_t bar = smem_u32(&full[b]);
+        mbar_arrive_expect_tx(bar, p.box_bytes);
+        tma_load_4d(smem_u32(tt_smem + (size_t)b * p.buf_bytes), &p.tmap, 0, ho * p.s_h, ch * p.Wc, n, bar);
+    };
+    for (int64_t k = 0; k < kNhwcRing - 1 && k < mine; ++k) load(k);
+    for (int64_t k = 0; k < mine; ++k) {
+        const int b = (int)(k % kNhwcRing);
+        // wait (bounded) for the unit's load
+        const uint32_t bar = smem_u32(&full[b]), par = (uint32_t)((k / kNhwcRing) & 1);
+        bool ok = mbar_try_wait(bar, par);
+        const uint64_t t0 = globaltimer();
+        while (!ok && globaltimer() - t0 < kTimeoutNs) ok = mbar_try_wait(bar, par);
+        if (!ok) break;
+        const int64_t u = first + k * step;
+        const int ch = (int)(u % p.chunks);
+        const int64_t r = u / p.chunks;
+        const int w0 = ch * p.Wc;
+        const int ncols = min(p.Wc, p.W_i - w0);
+        uint8_t *dst = p.win + ((r * p.W_i) + w0) * (int64_t)p.col_bytes;  // r = n*H_o + ho
+        fence_async_smem();
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                     "r"(smem_u32(tt_smem + (size_t)b * p.buf_bytes)), "r"((uint32_t)ncols * p.col_bytes)
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        // the next load reuses the buffer of the previous unit's store: wait until that
+        // store has read it (this unit's store may still be in flight)
+        if (k + kNhwcRing - 1 < mine) {
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            load(k + kNhwcRing - 1);
+        }
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// The channels-last TMA transform's tensor map, or false when it does not cover
+// the shape (box limits: at most 256 per dimension).
+static PFN_cuTensorMapEncodeTiled_v12000 transform_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+static bool nhwc_tma_params(TTParams &p, const void *x, void *win, const Shape &s, int esz) {
+    if ((s.C_i * esz) % 16 != 0 || s.C_i > 256 || s.H_f > 256) return false;
+    if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(win)) & 15) != 0) return false;
+    const int64_t col_bytes = s.H_f * s.C_i * esz;
+    if (col_bytes > kNhwcBoxBytes) return false;
+    const int64_t wmax = std::min<int64_t>(256, kNhwcBoxBytes / col_bytes);
+    const int64_t chunks = (s.W_i + wmax - 1) / wmax;
+    const int64_t Wc = (s.W_i + chunks - 1) / chunks;
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = transform_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t C = (cuuint64_t)s.C_i, W = (cuuint64_t)s.W_i, H = (cuuint64_t)s.H_i;
+    const cuuint64_t e = (cuuint64_t)esz;
+    const cuuint64_t dims[4] = {C, H, W, (cuuint64_t)s.N};
+    const cuuint64_t strides[3] = {W * C * e, C * e, H * W * C * e};
+    const cuuint32_t box[4] = {(cuuint32_t)C, (cuuint32_t)s.H_f, (cuuint32_t)Wc, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = enc(&p.tmap, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, 4,
+                           const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    p.win = static_cast<uint8_t *>(win);
+    p.chunks = (int)chunks;
+    p.Wc = (int)Wc;
+    p.units = s.N * s.H_o * chunks;
+    p.H_o = (int)s.H_o;
+    p.W_i = (int)s.W_i;
+    p.s_h = (int)s.s_h;
+    p.col_bytes = (uint32_t)col_bytes;
+    p.box_bytes = (uint32_t)(col_bytes * Wc);
+    p.buf_bytes = (p.box_bytes + 127u) / 128u * 128u;
+    return true;
+}
+
 }  // namespace
 
 cudaError_t launch_transform_nhwc(const void *x, void *win, const Shape &s, int esz, cudaStream_t st) {
+    if (s.N > 0 && s.H_o > 0) {
+        TTParams tp;
+        if (nhwc_tma_params(tp, x, win, s, esz)) {
+            int dev = 0, sms = 148;
+            if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            const size_t smem = (size_t)kNhwcRing * tp.buf_bytes;
+            const cudaError_t e =
+                cudaFuncSetAttribute(transform_nhwc_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(8, (200 * 1024) / smem));
+            const unsigned blocks = (unsigned)std::min<int64_t>(tp.units, (int64_t)sms * per_sm);
+            transform_nhwc_tma<<<blocks, 32, smem, st>>>(tp);
+            return cudaGetLastError();
+        }
+    }
     TNParams p;
     p.x = x;
     p.win = win;

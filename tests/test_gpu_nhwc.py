@@ -48,6 +48,9 @@ T_CASES = [  # N, C_i, H_i, W_i, H_f, s_h
     (2, 12, 9, 13, 9, 1), (1, 1, 40, 5, 1, 1), (2, 4, 50, 17, 3, 5), (1, 96, 24, 24, 5, 1),
     # input rows too long to stage a band in shared memory: element-wise path
     (1, 3, 12, 12000, 3, 2),
+    # channel runs of whole 16-byte vectors, window rows in several column chunks
+    # with a short last one (tensor-copy path)
+    (1, 64, 12, 301, 5, 2), (2, 32, 9, 130, 3, 1),
 ]
 
 
