@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         }
         // a slab stage is filled by one producer group (all producers when there is one)
         // (with tma_slab one thread completes a stage: its arrival and the copies' bytes)
-        const bool one_group = !(MODE == TAP_CH && (p.ring || p.stack));
+        const bool one_group = !(MODE == TAP_CH && p.ring);
         for (int s = 0; s < p.BST; ++s) {
             mbar_init(full_b(s), (MODE == TAP_CL && p.tma_slab) ? 1
                                  : one_group                     ? TAP_PROD_WARPS * 32
@@ -714,15 +714,17 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         // copied there by bulk copies (completing on the slot's barrier) and the slab
         // is built from shared memory. Without one (TAP_CH whose rows are not 16-byte
         // aligned, or whose staging does not fit) the slab is gathered straight from
-        // global memory; TAP_CL copies its entries with cp.async. For TAP_CH with a
-        // raw ring or with tap stacking a chunk's fill is mostly latency (copy,
-        // barriers, shared-memory round trips), so the producers form two groups of
-        // four warps that fill alternate chunks at the same time, each with its own
-        // raw slot and named barrier. Otherwise all eight warps fill every chunk, and
-        // with two raw slots the next chunk's copy is in flight while this one is
-        // re-laid.
+        // global memory; TAP_CL copies its entries by TMA (or cp.async). For TAP_CH
+        // with a raw ring a chunk's fill is mostly latency (copy, barriers,
+        // shared-memory round trips), so the producers form two groups of four warps
+        // that fill alternate chunks at the same time, each with its own raw slot and
+        // named barrier. Otherwise all eight warps fill every chunk (with two slab
+        // stages only one chunk can be filled at a time: the other stage is being
+        // read by the MMAs, so eight warps halve the fill's latency — cv4 fused 810
+        // → 717 µs against two groups), and with two raw slots the next chunk's copy
+        // is in flight while this one is re-laid.
         const bool staged = !CHAN || (MODE == TAP_CH && p.ring);
-        const int ngroups = (MODE == TAP_CH && (p.ring || p.stack)) ? 2 : 1;
+        const int ngroups = (MODE == TAP_CH && p.ring) ? 2 : 1;
         const bool prefetch = ngroups == 1 && staged && p.ring;
         const int grp = ngroups == 2 ? (warp - 2) / (TAP_PROD_WARPS / 2) : 0;
         const int NPT = TAP_PROD_WARPS * 32 / ngroups;  // threads of the group
