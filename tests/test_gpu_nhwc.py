@@ -51,6 +51,8 @@ T_CASES = [  # N, C_i, H_i, W_i, H_f, s_h
     # channel runs of whole 16-byte vectors, window rows in several column chunks
     # with a short last one (tensor-copy path)
     (1, 64, 12, 301, 5, 2), (2, 32, 9, 130, 3, 1),
+    # more channels than a tensor copy's box holds (256): the vector-copy kernel
+    (1, 264, 6, 8, 3, 1),
 ]
 
 
