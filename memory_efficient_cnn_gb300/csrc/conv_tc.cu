@@ -383,14 +383,15 @@ struct TapParams {
     int raw_elems;         // elements of the raw staging area (all slots)
     int ring;              // 1: raw chunks staged two deep (next chunk's bulk copy in flight)
     int raw_slot;          // elements of one raw slot (a multiple of 64)
-    int raw_ch;            // CH with ring: elements per channel in a slot (rows x W_i)
+    int raw_ch;            // CH with ring: elements per channel plane of a slot (raw_rows x raw_w, padded)
+    int raw_rows, raw_w;   // CH with ring: rows of a plane, elements per raw row (the tensor copy's
+                           // box; W_i when per-channel bulk copies stage the rows)
     uint32_t stage_b;      // bytes of one slab stage
     int BST, AST;          // slab stages, filter stages
     int vec;               // CH: 16-byte row loads possible
     int bf16;
     FastDiv div_pitch;     // W*: positions -> (output row, column group)
     FastDiv div_cgs, div_sh, div_sw;  // CH: 8-column groups per row, strides
-    FastDiv div_vpc;       // CH with ring: 16-byte vectors per channel of a full tile's rows
     int stack;             // CH, C_o <= 64: two taps per MMA, stacked along M (see below)
     int xpose;             // stacked, transposed: positions along M, the two taps along N
     int Gr;                // stacked: tap groups per filter row
@@ -1012,9 +1013,38 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                             make_uint4(e16[0] | (e16[1] << 16), e16[2] | (e16[3] << 16),
                                        e16[4] | (e16[5] << 16), e16[6] | (e16[7] << 16));
                     }
+                } else if (p.vec && p.ring) {
+                    // A block is 8 channels x 8 columns of one raw row. A warp moves four
+                    // blocks per step: one matrix load (lane 8q + i gives channel row i of
+                    // block q) and one transposing matrix store (lane 8q + i gives the slab
+                    // entry of column i of block q: that column's 8 channels, 16 bytes).
+                    // Raw planes lie an odd number of 16-byte units apart, so a load's eight
+                    // rows hit eight bank groups; a store's eight entries are consecutive.
+                    // A step's blocks past the last repeat the last one (the same values to
+                    // the same addresses).
+                    const int cgs = p.W_i / 8;
+                    const int nblk = 2 * rows * cgs;
+                    const int wq = lane >> 3, wi = lane & 7;
+                    for (int b0 = (pt >> 5) * 4; b0 < nblk; b0 += NPT / 8) {
+                        const int blk = min(b0 + wq, nblk - 1);
+                        const int t2 = (int)fdiv((uint32_t)blk, p.div_cgs);
+                        const int cg = blk - t2 * cgs;
+                        const int c8 = t2 >= rows ? 1 : 0;
+                        const int lr = t2 - c8 * rows;
+                        uint32_t r0, r1, r2, r3;
+                        ldsm_x4(smem_u32(raw_slot + (size_t)(c8 * 8 + wi) * p.raw_ch + lr * p.raw_w + cg * 8), r0, r1,
+                                r2, r3);
+                        const int lq = (int)fdiv((uint32_t)lr, p.div_sh);
+                        const int col = p.p_w + cg * 8 + wi;
+                        const int cq = (int)fdiv((uint32_t)col, p.div_sw);
+                        uint8_t *dst = slab + (size_t)c8 * p.lbo +
+                                       (size_t)((lr - lq * p.s_h) * p.s_w + (col - cq * p.s_w)) * p.PB +
+                                       (size_t)(lq * p.pitch + cq) * 16;
+                        stsm_x4_trans(smem_u32(dst), r0, r1, r2, r3);
+                    }
                 } else if (p.vec) {
-                    // 8 channels x 8 columns per item: 8 16-byte loads (from the raw slot or
-                    // global memory), 8x8 transpose, 8 16-byte stores
+                    // 8 channels x 8 columns per item: 8 16-byte loads from global memory,
+                    // 8x8 transpose, 8 16-byte stores
                     const int cgs = p.W_i / 8;
                     const int items = 2 * rows * cgs;
                     for (int it = pt; it < items; it += NPT) {
@@ -1024,11 +1054,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                         const int lr = t2 - c8 * rows;
                         const int ci0 = cc * 16 + c8 * 8;
                         uint4 v[8];
-                        if (p.ring) {
-                            const E16 *src = raw_slot + (size_t)(c8 * 8) * p.raw_ch + lr * p.W_i + cg * 8;
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] = *reinterpret_cast<const uint4 *>(src + (size_t)e * p.raw_ch);
-                        } else {
+                        {
                             // input row R0 - p_h + lr (zero outside the input)
                             const int h = R0 - p.p_h + lr;
                             const bool rok = (unsigned)h < (unsigned)p.H_i;
@@ -1607,15 +1633,22 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
             stage_b = std::max(2 * U * lbo, (2 * U - 1) * lbo + (A - 1 + NTp) * 16);
         }
         stage_b = (stage_b + 127) / 128 * 128;
-        // raw staging slot (elements, a multiple of 64): TAP_CH 16 channels of the tile's
-        // input rows (only when rows are whole 16-byte vectors), TAP_WX one channel's
-        // input rows, TAP_WW its window rows, each with room for the alignment lead;
-        // TAP_CL copies straight into the slab
-        const int64_t slot = mode == TAP_CL ? 0
-                             : mode == TAP_CH ? (s.W_i % 8 == 0 ? 16 * RR * s.W_i : 0)
-                             : mode == TAP_WX ? RR * s.W_i + 16
-                                              : Q * s.W_i * s.H_f + 16;
-        const int64_t slot_e = (slot + 63) / 64 * 64;
+        // raw staging slot (elements, a multiple of 64): TAP_CH 16 channel planes of the
+        // tile's input rows (only when rows are whole 16-byte vectors), TAP_WX one
+        // channel's input rows, TAP_WW its window rows, each with room for the alignment
+        // lead; TAP_CL copies straight into the slab. A TAP_CH plane is RR rows of W_i
+        // elements or, where it fits (tried first at each pipeline depth), Rb rows of Wb
+        // elements, Rb in {RR, RR + 1} and Wb in {W_i, W_i + 8} both odd in 8-element
+        // units, so that planes lie an odd number of 16-byte units apart: the eight
+        // channel rows of a matrix load then fall in eight different bank groups.
+        const int64_t Wb = (s.W_i / 8) % 2 ? s.W_i : s.W_i + 8, Rb = RR % 2 ? RR : RR + 1;
+        auto slot_elems = [&](bool pad) -> int64_t {
+            const int64_t slot = mode == TAP_CL ? 0
+                                 : mode == TAP_CH ? (s.W_i % 8 == 0 ? 16 * (pad ? Rb * Wb : RR * s.W_i) : 0)
+                                 : mode == TAP_WX ? RR * s.W_i + 16
+                                                  : Q * s.W_i * s.H_f + 16;
+            return (slot + 63) / 64 * 64;
+        };
         // search: filter stages of at least 8 taps (or all of them) first, since every
         // stage costs the MMA issuers a fixed overhead; within that a ring of two raw
         // slots (the next chunk's copy in flight) before one slot (TAP_W*) or none
@@ -1636,8 +1669,7 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
         const int ast_list[3] = {xpose ? 2 : 3, xpose ? 3 : 2, 4};
         for (int pass = 0; pass < 2; ++pass)
         for (int ring : {1, 0}) {
-          const int64_t raw_e = chan ? (ring ? 2 * slot_e : 0) : (ring ? 2 : 1) * slot_e;
-          if (ring && slot_e == 0) continue;
+          if (ring && slot_elems(false) == 0) continue;
           for (int ti = 0; ti < n_tg; ++ti) {
             const int TG = tg_list[ti];
             const int tg = (int)std::min<int64_t>(TG, T);
@@ -1645,6 +1677,10 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
             if (pass == 0 && !xpose && tg < std::min<int64_t>(T, 8)) continue;
             for (int BST : {3, 2}) {
               for (int AST : ast_list) {
+                for (int pad : {1, 0}) {
+                    if (pad && !(mode == TAP_CH && ring)) continue;
+                    const int64_t slot_e = slot_elems(pad != 0);
+                    const int64_t raw_e = chan ? (ring ? 2 * slot_e : 0) : (ring ? 2 : 1) * slot_e;
                     int64_t total = (int64_t)AST * tg * TAP_A_BYTES + BST * stage_b + raw_e * 2 +
                                     tap_epi_region(epi_blocks, xpose) + 512 + 4 * T + 16 + 128 * U;
                     if (total > smem_max) continue;
@@ -1683,7 +1719,9 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
                     p.raw_elems = (int)raw_e;
                     p.ring = ring;
                     p.raw_slot = (int)slot_e;
-                    p.raw_ch = (int)(RR * s.W_i);
+                    p.raw_rows = (int)(pad ? Rb : RR);
+                    p.raw_w = (int)(pad ? Wb : s.W_i);
+                    p.raw_ch = p.raw_rows * p.raw_w;
                     p.stage_b = (uint32_t)stage_b;
                     p.BST = BST;
                     p.AST = AST;
@@ -1692,6 +1730,7 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
                     pl.kslots = NCH * T * 16;
                     pl.ok = p.tiles_total < (1ll << 40) && s.N < (1ll << 31) && raw_e < (1ll << 30);
                     return pl;
+                }
               }
             }
           }
@@ -1915,18 +1954,18 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // The tensor map of TAP_CH's raw rows: the kernel's input (16-bit elements; the
 // window tensor when it is read as one) as a 4-D tensor (W_i, H_i, C_i, N) of
-// the kernel's shape, box (W_i, raw rows, 16, 1), zero fill outside. False when
-// the box is out of the copy engine's limits (at most 256 per dimension) or the
-// encoder refuses it; the per-channel bulk copies then stage the rows.
+// the kernel's shape, box (raw_w, raw_rows, 16, 1), zero fill outside (the
+// padding columns and row of a raw plane). False when the box is out of the
+// copy engine's limits (at most 256 per dimension) or the encoder refuses it;
+// the per-channel bulk copies then stage the rows.
 static bool encode_raw_map(TapParams &p, const void *src) {
-    const int64_t rows = p.raw_ch / p.W_i;
-    if (p.W_i > 256 || rows > 256 || (reinterpret_cast<uintptr_t>(src) & 15) != 0) return false;
+    if (p.raw_w > 256 || p.raw_rows > 256 || (reinterpret_cast<uintptr_t>(src) & 15) != 0) return false;
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t W = (cuuint64_t)p.W_i, H = (cuuint64_t)p.H_i, C = (cuuint64_t)p.C_i;
     const cuuint64_t dims[4] = {W, H, C, (cuuint64_t)p.N_img};
     const cuuint64_t strides[3] = {W * 2, H * W * 2, C * H * W * 2};
-    const cuuint32_t box[4] = {(cuuint32_t)W, (cuuint32_t)rows, 16u, 1u};
+    const cuuint32_t box[4] = {(cuuint32_t)p.raw_w, (cuuint32_t)p.raw_rows, 16u, 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     const CUresult r = enc(&p.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(src), dims, strides,
                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1990,12 +2029,12 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
         p.vec = (p.C_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
     if (pl.mode == TAP_CH && !p.vec) p.ring = 0;  // 16-byte copies need 16-byte rows
     p.tma_raw = (pl.mode == TAP_CH && p.ring && encode_raw_map(p, src)) ? 1 : 0;
+    if (!p.tma_raw) p.raw_w = p.W_i;  // per-channel bulk copies: contiguous rows
     p.tma_slab = (pl.mode == TAP_CL && p.vec && encode_slab_map(p, src)) ? 1 : 0;
     p.div_pitch = make_fastdiv((uint32_t)p.pitch);
     p.div_cgs = make_fastdiv((uint32_t)std::max(1, p.W_i / 8));
     p.div_sh = make_fastdiv((uint32_t)p.s_h);
     p.div_sw = make_fastdiv((uint32_t)p.s_w);
-    p.div_vpc = make_fastdiv((uint32_t)std::max(1, ((p.Qmax - 1) * p.s_h + p.Hfe) * p.W_i / 8));
     p.div_wi = make_fastdiv((uint32_t)p.Wp);
     p.nhwc = layout == LAYOUT_NHWC ? 1 : 0;
     p.bf16 = bf16 ? 1 : 0;

@@ -91,6 +91,23 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Warp-wide loads and stores of four 8 x 8 matrices of 16-bit elements in
+// shared memory. Lane 8q + i gives the 16-byte aligned address of row i of
+// matrix q. In registers, lane t holds in r_q elements (t / 4, 2(t % 4)) (low
+// half) and (t / 4, 2(t % 4) + 1) of matrix q. The transposing store writes
+// matrix q's column i, as 8 consecutive elements, at the row address of lane
+// 8q + i.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void stsm_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0),
+                 "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
