@@ -388,6 +388,9 @@ struct TapParams {
                            // box; W_i when per-channel bulk copies stage the rows)
     uint32_t stage_b;      // bytes of one slab stage
     int BST, AST;          // slab stages, filter stages
+    int merge;             // one filter stage per chunk and AST == BST: a chunk's filter copy
+                           // completes on its slab stage's full barrier and the stage's release
+                           // is the slab's (one wait and one commit per chunk for the issuers)
     int vec;               // CH: 16-byte row loads possible
     int bf16;
     FastDiv div_pitch;     // W*: positions -> (output row, column group)
@@ -543,9 +546,10 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         // (with tma_slab one thread completes a stage: its arrival and the copies' bytes)
         const bool one_group = !(MODE == TAP_CH && p.ring);
         for (int s = 0; s < p.BST; ++s) {
-            mbar_init(full_b(s), (MODE == TAP_CL && p.tma_slab) ? 1
-                                 : one_group                     ? TAP_PROD_WARPS * 32
-                                                                 : TAP_PROD_WARPS * 16);
+            mbar_init(full_b(s), ((MODE == TAP_CL && p.tma_slab) ? 1
+                                  : one_group                     ? TAP_PROD_WARPS * 32
+                                                                  : TAP_PROD_WARPS * 16) +
+                                     (p.merge ? 1 : 0));
             mbar_init(empty_b(s), 2);
         }
         for (int a = 0; a < 4; ++a) {
@@ -640,7 +644,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                         // (the filter tile arrived by a bulk copy completing on the barrier:
                         // no tcgen05 fence is needed for the MMAs to read it, and one per
                         // stage costs the issuer ~12% of the MMA rate)
-                        if (!(ok = bar_wait(full_a(sa), pha, ctl, SITE_FULL_A))) break;
+                        if (!p.merge && !(ok = bar_wait(full_a(sa), pha, ctl, SITE_FULL_A))) break;
                         if (NW > 0) {
                             const int t_end = min(p.T, t0 + p.TG);
                             uint32_t a_lo = a_lo_base + (uint32_t)sa * a_stage16;
@@ -664,7 +668,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                                 }
                             }
                         }
-                        mma_commit(empty_a(sa));
+                        if (!p.merge) mma_commit(empty_a(sa));
                         if (++sa == p.AST) { sa = 0; pha ^= 1; }
                     }
                     if (ok) mma_commit(empty_b(sb));
@@ -690,21 +694,24 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                 for (int cc = 0; cc < p.NCH && ok; ++cc) {
                     for (int tg = 0; tg < p.ntg; ++tg) {
                         const int sa = issued % p.AST;
-                        if (!(ok = bar_wait(empty_a(sa), ((issued / p.AST) & 1) ^ 1, ctl, SITE_EMPTY_LOAD)))
-                            break;
+                        // merged: filter stage sa is the chunk's slab stage
+                        const uint32_t ebar = p.merge ? empty_b(sa) : empty_a(sa);
+                        const uint32_t fbar = p.merge ? full_b(sa) : full_a(sa);
+                        if (!(ok = bar_wait(ebar, ((issued / p.AST) & 1) ^ 1, ctl, SITE_EMPTY_LOAD))) break;
                         const int t0 = tg * p.TG;
                         const uint32_t bytes = (uint32_t)(min(p.T, t0 + p.TG) - t0) * TAP_A_BYTES;
                         const uint16_t *src =
                             p.fa + (((int64_t)tl.mt * p.NCH + cc) * p.T + t0) * (TAP_A_BYTES / 2);
-                        mbar_arrive_expect_tx(full_a(sa), bytes);
-                        bulk_g2s(smem_u32(sA + (size_t)sa * a_stage), src, bytes, full_a(sa));
+                        mbar_arrive_expect_tx(fbar, bytes);
+                        bulk_g2s(smem_u32(sA + (size_t)sa * a_stage), src, bytes, fbar);
                         ++issued;
                     }
                 }
             }
             if (!ok) {
                 for (int it = (issued > p.AST ? issued - p.AST : 0); it < issued; ++it)
-                    bar_wait(full_a(it % p.AST), (it / p.AST) & 1, ctl, SITE_DRAIN, false);
+                    bar_wait(p.merge ? full_b(it % p.AST) : full_a(it % p.AST), (it / p.AST) & 1, ctl, SITE_DRAIN,
+                             false);
             }
         }
         __syncwarp();
@@ -1725,6 +1732,7 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
                     p.stage_b = (uint32_t)stage_b;
                     p.BST = BST;
                     p.AST = AST;
+                    p.merge = (p.ntg == 1 && AST == BST) ? 1 : 0;
                     pl.smem = (size_t)total;
                     pl.mtiles = p.MT;
                     pl.kslots = NCH * T * 16;
