@@ -358,7 +358,7 @@ struct TapParams {
     // whole 16-byte entries: the input as (C_i, W_i, H_i, N), box (8, pitch*s_w,
     // rows per phase*s_h, 1) traversed with element strides (1, s_w, s_h, 1): one
     // polyphase block of one 8-channel half of a chunk's slab (tma_slab).
-    alignas(64) CUtensorMap tmap_x;
+    CUtensorMap tmap_x;    // (the type is 128-byte aligned)
     int tma_raw, tma_slab;
     int slab_hh;           // CL with tma_slab: rows of a polyphase block
     const uint16_t *src;   // NCHW input (CH, WX), window tensor (WW), NHWC input (CL)

@@ -708,7 +708,7 @@ constexpr int kNhwcRing = 3;
 constexpr int kNhwcBoxBytes = 32 * 1024;
 
 struct TTParams {
-    alignas(64) CUtensorMap tmap;
+    CUtensorMap tmap;  // (the type is 128-byte aligned)
     uint8_t *win;
     int64_t units;        // N * H_o * chunks
     int chunks, Wc;       // column chunks per window row, columns per chunk
