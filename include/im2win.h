@@ -296,11 +296,10 @@ im2win_status im2win_device_status(const void *ws, size_t ws_bytes, void *stream
  * every GPU that loads it, held until the process exits). A problem whose
  * fused workspace (im2win_workspace_size(IM2WIN_OP_CONV_FUSED, ...)) exceeds
  * that size is rejected with IM2WIN_ERR_WORKSPACE before any work is queued.
- * The first call on a device, with that device current, looks up the array's
- * device address (cudaGetSymbolAddress); make it before any stream capture.
- * The address is kept for the life of the process: after cudaDeviceReset on
- * that device the array may move and this call must not be used again in the
- * process.
+ * Every call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress), so a device reset, which may move the array, does
+ * not leave a stale address; the first call on a device loads the library's
+ * module there, so make one call before any stream capture.
  * All calls share the array and it keeps the last call's contents (each call
  * re-lays the filter and clears the status word itself): calls whose work can
  * overlap on the GPU race and may return wrong results. Calls no cudaMalloc,

@@ -13,20 +13,15 @@
 //  * the array holds IM2WIN_NOALLOC_SCRATCH_BYTES; problems whose fused
 //    workspace is larger are rejected with IM2WIN_ERR_WORKSPACE before any
 //    work is queued;
-//  * the device address of the array is looked up once per device, on the
-//    first call made while that device is current (cudaGetSymbolAddress);
-//    make that first call before capturing the stream into a graph. The
-//    address is kept until the process exits: cudaDeviceReset unloads the
-//    library's module on that device, the array may come back elsewhere, and
-//    the kept address would then be stale, so this entry point must not be
-//    called on a device after it has been reset;
+//  * every call looks up the array's device address on the current device
+//    (cudaGetSymbolAddress), so a device reset, which may move the array, is
+//    harmless; the first call on a device loads the library's module there:
+//    make one call before capturing the stream into a graph;
 //  * all calls share the array, which keeps whatever the last call left in
 //    it: every call re-lays the filter and clears the status word itself, and
 //    two calls whose kernels overlap on the GPU (different streams, no
 //    ordering) race on it and may produce wrong results;
 //  * nothing here calls cudaMalloc, cudaFree or any allocating routine.
-#include <mutex>
-
 #include "im2win_internal.cuh"
 
 namespace {
@@ -36,23 +31,12 @@ static_assert(kScratchBytes % 256 == 0, "scratch size");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void *g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up once).
+// Device address of the scratch array on the current device.
 im2win_status scratch_on_current_device(void **addr) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return IM2WIN_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return IM2WIN_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) return IM2WIN_ERR_CUDA;
-        g_scratch_addr[dev] = p;
-    }
-    *addr = g_scratch_addr[dev];
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return IM2WIN_ERR_CUDA;
+    *addr = p;
     return IM2WIN_OK;
 }
 
