@@ -332,6 +332,7 @@ __host__ __device__ inline int stacked_groups_per_row(int W_f, int s_w) {
 }
 
 constexpr int TAP_PROD_WARPS = 8;
+constexpr int kMaxSlabStages = 6;
 constexpr int TAP_EPI_WARPS = 8;
 constexpr int TAP_ISSUER1_WARP = 2 + TAP_PROD_WARPS + TAP_EPI_WARPS;  // the second MMA issuer
 constexpr int TAP_THREADS = (3 + TAP_PROD_WARPS + TAP_EPI_WARPS) * 32;
@@ -361,6 +362,12 @@ struct TapParams {
     CUtensorMap tmap_x;    // (the type is 128-byte aligned)
     int tma_raw, tma_slab;
     int slab_hh;           // CL with tma_slab: rows of a polyphase block
+    // CH, 1x1 filter at stride 1 without padding (the input is its own window): the
+    // slab is the tile's input positions x 16 channels held MN-major (8 positions x
+    // 8 channels per 128-byte core matrix, [position group][channel][position]), one
+    // tensor copy per chunk of the input seen as (8, C_i, H_i*W_i/8, N) with box
+    // (8, 16, mn_box/8, 1); the MMAs read it with the B transpose bit set
+    int mnb, mn_box;
     const uint16_t *src;   // NCHW input (CH, WX), window tensor (WW), NHWC input (CL)
     const uint16_t *fa;
     uint16_t *out;
@@ -546,7 +553,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         // (with tma_slab one thread completes a stage: its arrival and the copies' bytes)
         const bool one_group = !(MODE == TAP_CH && p.ring);
         for (int s = 0; s < p.BST; ++s) {
-            mbar_init(full_b(s), ((MODE == TAP_CL && p.tma_slab) ? 1
+            mbar_init(full_b(s), (((MODE == TAP_CL && p.tma_slab) || (MODE == TAP_CH && p.mnb)) ? 1
                                   : one_group                     ? TAP_PROD_WARPS * 32
                                                                   : TAP_PROD_WARPS * 16) +
                                      (p.merge ? 1 : 0));
@@ -597,7 +604,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             int k = 0;
             int sb = 0, sa = 0;
             uint32_t phb = 0, pha = 0;
-            const uint64_t adesc0 = smem_desc(0, 128, 256), bdesc0 = smem_desc(0, p.lbo, 128);
+            // (an MN-major slab: K halves lbo = 128 bytes apart, position groups 256)
+            const uint64_t adesc0 = smem_desc(0, 128, 256), bdesc0 = smem_desc(0, p.lbo, p.mnb ? 256 : 128);
             const uint32_t a_hi = (uint32_t)(adesc0 >> 32), b_hi = (uint32_t)(bdesc0 >> 32);
             const uint32_t a_lo_base = (uint32_t)adesc0 + (smem_u32(sA) >> 4);
             const uint32_t b_lo_base = (uint32_t)bdesc0 + (smem_u32(sB) >> 4);
@@ -630,9 +638,11 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     const int NTp = (tl.Q * p.pitch + p.stack + 15) / 16 * 16;
                     const int N0 = tile_n0(p, NTp);
                     NW = which == 0 ? N0 : NTp - N0;
-                    col0 = which == 0 ? 0u : (uint32_t)N0;
-                    idesc = make_idesc(p.bf16 != 0, BM, NW > 0 ? NW : 16);
-                    d_tmem = tmem + col0;
+                    // slab offset of the issuer's first position, in 16-byte units (MN-major:
+                    // 32 bytes per position)
+                    col0 = which == 0 ? 0u : (uint32_t)N0 * (p.mnb ? 2u : 1u);
+                    idesc = make_idesc(p.bf16 != 0, BM, NW > 0 ? NW : 16) | (p.mnb ? 1u << 16 : 0u);
+                    d_tmem = tmem + (which == 0 ? 0u : (uint32_t)N0);
                 }
                 for (int cc = 0; cc < p.NCH && ok; ++cc) {
                     if (!(ok = bar_wait(full_b(sb), phb, ctl, SITE_FULL_B))) break;
@@ -858,24 +868,33 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             fence_async_smem();
             asm volatile("bar.sync %0, %1;" ::"r"(3), "r"(TAP_PROD_WARPS * 32) : "memory");
         }
-        if (MODE == TAP_CL && p.tma_slab && warp == 2) {
+        const bool copy_slab = (MODE == TAP_CL && p.tma_slab) || (MODE == TAP_CH && p.mnb);
+        if (copy_slab && warp == 2) {
             // Channels-last input in whole 16-byte entries: each polyphase block (ph_r,
             // ph_c) of each 8-channel half of a chunk's slab is one tensor copy, entry
             // (q, m) being input (row R0 + ph_r + q*s_h, column ph_c + m*s_w - p_w),
-            // zero outside the input. One thread issues them all on the stage's barrier;
+            // zero outside the input. An MN-major 1x1 slab (mnb) is one tensor copy of
+            // the chunk's 16 channels at the tile's positions (zero past the plane's
+            // end or channel C_i). One thread issues them all on the stage's barrier;
             // the other producer warps have nothing to do.
             int sbt = 0;
             uint32_t pht = 0;
             bool ok2 = true;
-            int pend[3] = {-1, -1, -1};  // per stage: parity of a copy not yet seen landed
-            const uint32_t bytes = 2u * (uint32_t)(p.s_h * p.s_w * p.slab_hh * p.pitch) * 16u;
+            int pend[kMaxSlabStages];  // per stage: parity of a copy not yet seen landed
+            for (int s2 = 0; s2 < kMaxSlabStages; ++s2) pend[s2] = -1;
+            const uint32_t bytes = MODE == TAP_CH ? (uint32_t)p.mn_box * 32u
+                                                  : 2u * (uint32_t)(p.s_h * p.s_w * p.slab_hh * p.pitch) * 16u;
             TapTile t2;
             for (int64_t id2 = blockIdx.x; ok2 && id2 < p.tiles_total; id2 += gridDim.x) {
                 tile_at(p, id2, t2);
                 const int R0 = t2.ho0 * p.s_h - p.p_h;
                 for (int c2 = 0; c2 < p.NCH; ++c2) {
                     if (!(ok2 = warp_bar_wait(empty_b(sbt), pht ^ 1, ctl, SITE_EMPTY_PROD))) break;
-                    if (lane == 0) {
+                    if (lane == 0 && MODE == TAP_CH) {
+                        const uint32_t slab = smem_u32(sB + (size_t)sbt * p.stage_b);
+                        mbar_arrive_expect_tx(full_b(sbt), bytes);
+                        tma_load_4d(slab, &p.tmap_x, 0, c2 * 16, (t2.ho0 * p.W_o) >> 3, t2.n, full_b(sbt));
+                    } else if (lane == 0) {
                         const uint32_t slab = smem_u32(sB + (size_t)sbt * p.stage_b);
                         mbar_arrive_expect_tx(full_b(sbt), bytes);
                         for (int c8 = 0; c8 < 2; ++c8)
@@ -895,8 +914,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     if (pend[s2] >= 0) bar_wait(full_b(s2), (uint32_t)pend[s2], ctl, SITE_DRAIN, false);
             __syncwarp();
         }
-        // (with tma_slab the loop below has nothing to do)
-        int64_t id = (MODE == TAP_CL && p.tma_slab) ? p.tiles_total : (int64_t)blockIdx.x;
+        // (with tensor-copied slabs the loop below has nothing to do)
+        int64_t id = copy_slab ? p.tiles_total : (int64_t)blockIdx.x;
         int cc = 0;
         TapTile tl;
         // raw staging (TAP_CH ring, TAP_WX, TAP_WW): parity of each slot's next
@@ -1618,8 +1637,15 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
         // positions the MMAs read from the slab (transposed: whole M blocks)
         const int64_t NTp = xpose ? (Q * pitch + 1 + 127) / 128 * 128 : (Q * pitch + stack + 15) / 16 * 16;
         const int64_t RR = (Q - 1) * s.s_h + Hfe;  // slab rows under a tile of Q rows
+        // a 1x1 filter at stride 1 without padding on rows of whole position groups: the
+        // input is its own window, copied MN-major into the slab by one tensor copy
+        const bool mnb = mode == TAP_CH && s.H_f == 1 && s.W_f == 1 && s.s_h == 1 && s.s_w == 1 && plain(s) &&
+                         s.W_o % 8 == 0 && NTp / 8 <= 256;
         int64_t PB = 0, lbo, stage_b;
-        if (chan) {
+        if (mnb) {
+            lbo = 128;  // the two 8-channel core matrices of a position group
+            stage_b = NTp * 32;
+        } else if (chan) {
             const int64_t HH = (RR + s.s_h - 1) / s.s_h;
             // a multiple of 128 bytes, so that every polyphase block of a stage can be the
             // destination of a tensor copy (its tail past the block's rows is never written)
@@ -1650,7 +1676,7 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
         // channel rows of a matrix load then fall in eight different bank groups.
         const int64_t Wb = (s.W_i / 8) % 2 ? s.W_i : s.W_i + 8, Rb = RR % 2 ? RR : RR + 1;
         auto slot_elems = [&](bool pad) -> int64_t {
-            const int64_t slot = mode == TAP_CL ? 0
+            const int64_t slot = (mode == TAP_CL || mnb) ? 0
                                  : mode == TAP_CH ? (s.W_i % 8 == 0 ? 16 * (pad ? Rb * Wb : RR * s.W_i) : 0)
                                  : mode == TAP_WX ? RR * s.W_i + 16
                                                   : Q * s.W_i * s.H_f + 16;
@@ -1673,7 +1699,7 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
         } else {
             for (int v : {9, 8, 6, 5, 4, 3, 2, 1}) tg_list[n_tg++] = v;
         }
-        const int ast_list[3] = {xpose ? 2 : 3, xpose ? 3 : 2, 4};
+        const int ast_list[5] = {xpose ? 2 : 3, xpose ? 3 : 2, 4, 6, 0};
         for (int pass = 0; pass < 2; ++pass)
         for (int ring : {1, 0}) {
           if (ring && slot_elems(false) == 0) continue;
@@ -1682,8 +1708,13 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
             const int tg = (int)std::min<int64_t>(TG, T);
             if (TG > T && TG != 1) continue;
             if (pass == 0 && !xpose && tg < std::min<int64_t>(T, 8)) continue;
-            for (int BST : {3, 2}) {
+            // an MN-major 1x1 slab is small and each stage is one tensor copy in flight:
+            // up to six stages, as many filter stages (one tap each)
+            const int bst_list[4] = {mnb ? 6 : 3, mnb ? 4 : 2, mnb ? 3 : 0, mnb ? 2 : 0};
+            for (int BST : bst_list) {
+              if (BST == 0) continue;
               for (int AST : ast_list) {
+                if (AST == 0 || (mnb ? AST != BST : AST == 6)) continue;
                 for (int pad : {1, 0}) {
                     if (pad && !(mode == TAP_CH && ring)) continue;
                     const int64_t slot_e = slot_elems(pad != 0);
@@ -1726,6 +1757,8 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
                     p.raw_elems = (int)raw_e;
                     p.ring = ring;
                     p.raw_slot = (int)slot_e;
+                    p.mnb = mnb ? 1 : 0;
+                    p.mn_box = (int)NTp;
                     p.raw_rows = (int)(pad ? Rb : RR);
                     p.raw_w = (int)(pad ? Wb : s.W_i);
                     p.raw_ch = p.raw_rows * p.raw_w;
@@ -2010,6 +2043,27 @@ static bool encode_slab_map(TapParams &p, const void *src) {
     return r == CUDA_SUCCESS;
 }
 
+// The tensor map of an MN-major 1x1 slab (mnb): the input as a 4-D tensor (8,
+// C_i, H_i*W_i/8, N) — eight consecutive positions, channels, position groups,
+// images — box (8, 16, mn_box/8, 1), zero fill outside (past the plane's last
+// group, channels past C_i). The planner chose mnb only where the plane is whole
+// groups; false when the encoder refuses it.
+static bool encode_mn_map(TapParams &p, const void *src) {
+    const int64_t P = (int64_t)p.H_i * p.W_i;
+    if (P % 8 != 0 || p.mn_box % 8 != 0 || p.mn_box / 8 > 256 || (reinterpret_cast<uintptr_t>(src) & 15) != 0)
+        return false;
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {8, (cuuint64_t)p.C_i, (cuuint64_t)(P / 8), (cuuint64_t)p.N_img};
+    const cuuint64_t strides[3] = {(cuuint64_t)P * 2, 16, (cuuint64_t)p.C_i * P * 2};
+    const cuuint32_t box[4] = {8u, 16u, (cuuint32_t)(p.mn_box / 8), 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = enc(&p.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(src), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *filt, void *out,
                               void *ws, const Shape &s, int layout, bool bf16, cudaStream_t st) {
     TapParams p = pl.p;
@@ -2036,7 +2090,8 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
     if (pl.mode == TAP_CL)  // 16-byte entries: 8 channels of one position
         p.vec = (p.C_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
     if (pl.mode == TAP_CH && !p.vec) p.ring = 0;  // 16-byte copies need 16-byte rows
-    p.tma_raw = (pl.mode == TAP_CH && p.ring && encode_raw_map(p, src)) ? 1 : 0;
+    p.tma_raw = (pl.mode == TAP_CH && p.ring && !p.mnb && encode_raw_map(p, src)) ? 1 : 0;
+    if (p.mnb && !encode_mn_map(p, src)) return cudaErrorInvalidValue;
     if (!p.tma_raw) p.raw_w = p.W_i;  // per-channel bulk copies: contiguous rows
     p.tma_slab = (pl.mode == TAP_CL && p.vec && encode_slab_map(p, src)) ? 1 : 0;
     p.div_pitch = make_fastdiv((uint32_t)p.pitch);

@@ -19,6 +19,9 @@ SMALL = [  # N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w
     # one or two MMA halves, several row tiles, strides 1-3, channel counts not a multiple of 16)
     (2, 32, 30, 64, 128, 3, 5, 3, 2), (1, 48, 60, 56, 64, 11, 11, 1, 1), (2, 128, 30, 56, 128, 3, 3, 1, 1),
     (1, 24, 100, 16, 40, 2, 2, 2, 2), (2, 40, 33, 35, 136, 4, 3, 2, 1), (1, 64, 9, 600, 16, 3, 3, 1, 2),
+    # 1x1 filters at stride 1 on rows of whole 8-position groups: the input tile copied
+    # MN-major into the slab (channels past C_i and positions past the plane read as zero)
+    (2, 40, 12, 16, 72, 1, 1, 1, 1), (1, 32, 40, 24, 64, 1, 1, 1, 1), (1, 16, 5, 8, 128, 1, 1, 1, 1),
 ]
 
 
