@@ -333,6 +333,7 @@ __host__ __device__ inline int stacked_groups_per_row(int W_f, int s_w) {
 
 constexpr int TAP_PROD_WARPS = 8;
 constexpr int kMaxSlabStages = 6;
+constexpr int kMnK = 2;  // 16-channel K steps per chunk of an MN-major 1x1 slab
 constexpr int TAP_EPI_WARPS = 8;
 constexpr int TAP_ISSUER1_WARP = 2 + TAP_PROD_WARPS + TAP_EPI_WARPS;  // the second MMA issuer
 constexpr int TAP_THREADS = (3 + TAP_PROD_WARPS + TAP_EPI_WARPS) * 32;
@@ -362,12 +363,14 @@ struct TapParams {
     CUtensorMap tmap_x;    // (the type is 128-byte aligned)
     int tma_raw, tma_slab;
     int slab_hh;           // CL with tma_slab: rows of a polyphase block
-    // CH, 1x1 filter at stride 1 without padding (the input is its own window): the
-    // slab is the tile's input positions x 16 channels held MN-major (8 positions x
-    // 8 channels per 128-byte core matrix, [position group][channel][position]), one
-    // tensor copy per chunk of the input seen as (8, C_i, H_i*W_i/8, N) with box
-    // (8, 16, mn_box/8, 1); the MMAs read it with the B transpose bit set
-    int mnb, mn_box;
+    // CH, 1x1 filter at stride 1 without padding (the input is its own window): a
+    // chunk is 16*mn_k channels, its slab the tile's input positions x those channels
+    // held MN-major (8 positions x 8 channels per 128-byte core matrix, [position
+    // group][channel][position]), one tensor copy of the input seen as (8, C_i,
+    // H_i*W_i/8, N) with box (8, 16*mn_k, mn_box/8, 1). Its T = mn_k "taps" are the
+    // 16-channel K steps (slab offset 256 bytes each); the MMAs read it with the B
+    // transpose bit set
+    int mnb, mn_box, mn_k;
     const uint16_t *src;   // NCHW input (CH, WX), window tensor (WW), NHWC input (CL)
     const uint16_t *fa;
     uint16_t *out;
@@ -456,6 +459,7 @@ __host__ __device__ inline int tap_dc(int j, int dil_w, int g_w) { return (j / g
 
 template <int MODE>
 __device__ __forceinline__ uint32_t tap_offset(const TapParams &p, int t) {
+    if (MODE == TAP_CH && p.mnb) return (uint32_t)t * 256u;  // K step t of an MN-major slab
     if (MODE == TAP_CH || MODE == TAP_CL) {
         const int r = t / p.W_f, j = t - r * p.W_f;
         const int dr = tap_dr(r, p.dil_h), dc = tap_dc(j, p.dil_w, p.g_w);
@@ -605,7 +609,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             int sb = 0, sa = 0;
             uint32_t phb = 0, pha = 0;
             // (an MN-major slab: K halves lbo = 128 bytes apart, position groups 256)
-            const uint64_t adesc0 = smem_desc(0, 128, 256), bdesc0 = smem_desc(0, p.lbo, p.mnb ? 256 : 128);
+            const uint64_t adesc0 = smem_desc(0, 128, 256),
+                           bdesc0 = smem_desc(0, p.lbo, p.mnb ? 256u * (uint32_t)p.mn_k : 128u);
             const uint32_t a_hi = (uint32_t)(adesc0 >> 32), b_hi = (uint32_t)(bdesc0 >> 32);
             const uint32_t a_lo_base = (uint32_t)adesc0 + (smem_u32(sA) >> 4);
             const uint32_t b_lo_base = (uint32_t)bdesc0 + (smem_u32(sB) >> 4);
@@ -640,7 +645,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     NW = which == 0 ? N0 : NTp - N0;
                     // slab offset of the issuer's first position, in 16-byte units (MN-major:
                     // 32 bytes per position)
-                    col0 = which == 0 ? 0u : (uint32_t)N0 * (p.mnb ? 2u : 1u);
+                    col0 = which == 0 ? 0u : (uint32_t)N0 * (p.mnb ? 2u * (uint32_t)p.mn_k : 1u);
                     idesc = make_idesc(p.bf16 != 0, BM, NW > 0 ? NW : 16) | (p.mnb ? 1u << 16 : 0u);
                     d_tmem = tmem + (which == 0 ? 0u : (uint32_t)N0);
                 }
@@ -882,7 +887,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             bool ok2 = true;
             int pend[kMaxSlabStages];  // per stage: parity of a copy not yet seen landed
             for (int s2 = 0; s2 < kMaxSlabStages; ++s2) pend[s2] = -1;
-            const uint32_t bytes = MODE == TAP_CH ? (uint32_t)p.mn_box * 32u
+            const uint32_t bytes = MODE == TAP_CH ? (uint32_t)p.mn_box * 32u * (uint32_t)p.mn_k
                                                   : 2u * (uint32_t)(p.s_h * p.s_w * p.slab_hh * p.pitch) * 16u;
             TapTile t2;
             for (int64_t id2 = blockIdx.x; ok2 && id2 < p.tiles_total; id2 += gridDim.x) {
@@ -893,7 +898,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     if (lane == 0 && MODE == TAP_CH) {
                         const uint32_t slab = smem_u32(sB + (size_t)sbt * p.stage_b);
                         mbar_arrive_expect_tx(full_b(sbt), bytes);
-                        tma_load_4d(slab, &p.tmap_x, 0, c2 * 16, (t2.ho0 * p.W_o) >> 3, t2.n, full_b(sbt));
+                        tma_load_4d(slab, &p.tmap_x, 0, c2 * 16 * p.mn_k, (t2.ho0 * p.W_o) >> 3, t2.n, full_b(sbt));
                     } else if (lane == 0) {
                         const uint32_t slab = smem_u32(sB + (size_t)sbt * p.stage_b);
                         mbar_arrive_expect_tx(full_b(sbt), bytes);
@@ -1601,10 +1606,16 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
     const int stack = (chan && s.C_o <= 64 && s.W_f > s.s_w && s.d_h == 1 && s.d_w == 1) ? 1 : 0;
     const int Gr = stack ? stacked_groups_per_row((int)s.W_f, (int)s.s_w) : 0;
     if (xpose && !stack) return pl;
+    // a 1x1 filter at stride 1 without padding on rows of whole 8-position groups: the
+    // input is its own window, copied MN-major into the slab by one tensor copy per
+    // chunk of 16*mn_k channels
+    const bool mnb = mode == TAP_CH && s.H_f == 1 && s.W_f == 1 && s.s_h == 1 && s.s_w == 1 && plain(s) &&
+                     s.W_o % 8 == 0;
+    const int64_t mn_k = mnb ? std::min<int64_t>(kMnK, (s.C_i + 15) / 16) : 1;
     if (chan) {
         pitch = (Wp + s.s_w - 1) / s.s_w;
-        T = stack ? s.H_f * Gr : s.H_f * s.W_f;
-        NCH = (s.C_i + 15) / 16;
+        T = mnb ? mn_k : stack ? s.H_f * Gr : s.H_f * s.W_f;
+        NCH = (s.C_i + 16 * mn_k - 1) / (16 * mn_k);
     } else {
         S = s.s_w * s.H_f;
         U = (S + 15) / 16;
@@ -1637,14 +1648,10 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
         // positions the MMAs read from the slab (transposed: whole M blocks)
         const int64_t NTp = xpose ? (Q * pitch + 1 + 127) / 128 * 128 : (Q * pitch + stack + 15) / 16 * 16;
         const int64_t RR = (Q - 1) * s.s_h + Hfe;  // slab rows under a tile of Q rows
-        // a 1x1 filter at stride 1 without padding on rows of whole position groups: the
-        // input is its own window, copied MN-major into the slab by one tensor copy
-        const bool mnb = mode == TAP_CH && s.H_f == 1 && s.W_f == 1 && s.s_h == 1 && s.s_w == 1 && plain(s) &&
-                         s.W_o % 8 == 0 && NTp / 8 <= 256;
         int64_t PB = 0, lbo, stage_b;
         if (mnb) {
-            lbo = 128;  // the two 8-channel core matrices of a position group
-            stage_b = NTp * 32;
+            lbo = 128;  // the two 8-channel core matrices of a 16-channel K step
+            stage_b = NTp * 32 * mn_k;
         } else if (chan) {
             const int64_t HH = (RR + s.s_h - 1) / s.s_h;
             // a multiple of 128 bytes, so that every polyphase block of a stage can be the
@@ -1759,6 +1766,7 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
                     p.raw_slot = (int)slot_e;
                     p.mnb = mnb ? 1 : 0;
                     p.mn_box = (int)NTp;
+                    p.mn_k = (int)mn_k;
                     p.raw_rows = (int)(pad ? Rb : RR);
                     p.raw_w = (int)(pad ? Wb : s.W_i);
                     p.raw_ch = p.raw_rows * p.raw_w;
@@ -2056,7 +2064,7 @@ static bool encode_mn_map(TapParams &p, const void *src) {
     if (!enc) return false;
     const cuuint64_t dims[4] = {8, (cuuint64_t)p.C_i, (cuuint64_t)(P / 8), (cuuint64_t)p.N_img};
     const cuuint64_t strides[3] = {(cuuint64_t)P * 2, 16, (cuuint64_t)p.C_i * P * 2};
-    const cuuint32_t box[4] = {8u, 16u, (cuuint32_t)(p.mn_box / 8), 1u};
+    const cuuint32_t box[4] = {8u, 16u * (cuuint32_t)p.mn_k, (cuuint32_t)(p.mn_box / 8), 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     const CUresult r = enc(&p.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(src), dims, strides,
                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -2069,15 +2077,17 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
     TapParams p = pl.p;
     uint32_t *status = static_cast<uint32_t *>(ws);
     uint16_t *fa = reinterpret_cast<uint16_t *>(static_cast<unsigned char *>(ws) + kStatusBytes);
-    const int n_chunks = pl.mtiles * p.NCH;
-    const int per_chunk = p.T * (int)(TAP_A_BYTES / 2);
+    // (an MN-major 1x1 slab's chunk of mn_k K steps is mn_k 16-channel chunks of one tap)
+    const int relay_nch = p.mnb ? p.NCH * p.mn_k : p.NCH, relay_t = p.mnb ? 1 : p.T;
+    const int n_chunks = pl.mtiles * relay_nch;
+    const int per_chunk = relay_t * (int)(TAP_A_BYTES / 2);
     const dim3 rgrid((unsigned)std::min(std::max(1, (per_chunk + 255) / 256), 64),
                      (unsigned)std::min(n_chunks, 65535));
     TapRelayout ra;
     ra.mode = pl.mode;
     ra.C_v = p.C_i; ra.H_fv = p.H_f; ra.W_fv = p.W_f; ra.s_wv = p.s_w;
     ra.view = pl.view; ra.C = (int)s.C_i; ra.H_f = (int)s.H_f; ra.W_f = (int)s.W_f;
-    ra.C_o = p.C_o; ra.T = p.T; ra.NCH = p.NCH; ra.U = p.U; ra.S = p.S;
+    ra.C_o = p.C_o; ra.T = relay_t; ra.NCH = relay_nch; ra.U = p.U; ra.S = p.S;
     ra.n_chunks = n_chunks; ra.stack = p.stack; ra.Gr = p.Gr;
     relayout_filter_tap<<<rgrid, 256, 0, st>>>(static_cast<const uint16_t *>(filt), fa, status, ra);
     cudaError_t e = cudaGetLastError();
