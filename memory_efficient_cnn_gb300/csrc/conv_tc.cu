@@ -365,11 +365,19 @@ struct TapParams {
     int slab_hh;           // CL with tma_slab: rows of a polyphase block
     // CH, 1x1 filter at stride 1 without padding (the input is its own window): a
     // chunk is 16*mn_k channels, its slab the tile's input positions x those channels
-    // held MN-major (8 positions x 8 channels per 128-byte core matrix, [position
-    // group][channel][position]), one tensor copy of the input seen as (8, C_i,
-    // H_i*W_i/8, N) with box (8, 16*mn_k, mn_box/8, 1). Its T = mn_k "taps" are the
-    // 16-channel K steps (slab offset 256 bytes each); the MMAs read it with the B
-    // transpose bit set
+    // held MN-major, one tensor copy per chunk; the MMAs read it with the B
+    // transpose bit set, and its T = mn_k "taps" are the 16-channel K steps.
+    //  mnb = 1: no swizzle (8 positions x 8 channels per 128-byte core matrix,
+    //    [position group][channel][position]): the input seen as (8, C_i, H_i*W_i/8,
+    //    N), box (8, 16*mn_k, mn_box/8, 1); K steps 256 bytes apart.
+    //  mnb = 2: 128-byte swizzle, where planes and tiles are whole 64-position
+    //    blocks: the input seen as (64, C_i, H_i*W_i/64, N), box (64, 16*mn_k,
+    //    mn_box/64, 1) with the copy's 128-byte swizzle, so that [block][channel]
+    //    rows of 64 positions (128 bytes) land with their 16-byte pieces permuted by
+    //    the row index mod 8 -- the MMA's 128-byte-swizzled MN-major layout (8
+    //    channels x 64 positions per 1024-byte atom; blocks lbo = 2048*mn_k bytes
+    //    apart, 8-channel groups 1024); K steps 2048 bytes apart. The copy then
+    //    moves 128-byte rows instead of 16-byte ones.
     int mnb, mn_box, mn_k;
     const uint16_t *src;   // NCHW input (CH, WX), window tensor (WW), NHWC input (CL)
     const uint16_t *fa;
@@ -441,16 +449,25 @@ __device__ __forceinline__ void tile_at(const TapParams &p, int64_t id, TapTile 
 
 // MMA split of a tile's NTp positions into two accumulators [0, N0) and
 // [N0, NTp) so that consecutive MMAs never wait on each other; N0 is a multiple
-// of 32 so that each accumulator's columns start on a 32-column TMEM load. The
+// of 32 so that each accumulator's columns start on a 32-column TMEM load (of
+// 64 with a 128-byte-swizzled MN-major slab: the second accumulator's operand
+// then starts on a swizzle atom). The
 // boundary is the same for every tile of a launch (that of the widest tile):
 // an accumulator is released as soon as it is drained, so the next tile's MMAs
 // into it must not reach columns of the other, possibly still draining, one.
 // A narrower tile may leave the second accumulator empty.
-__host__ __device__ __forceinline__ int split_n0(int NTp) {
-    return NTp >= 32 ? min(NTp, (NTp / 2 + 31) / 32 * 32) : NTp;
+__host__ __device__ __forceinline__ int split_n0(int NTp, int step = 32) {
+    return NTp >= step ? min(NTp, (NTp / 2 + step - 1) / step * step) : NTp;
+}
+// Accumulator columns of a tile of NT positions: whole 16-column MMA widths
+// (with stacking one column more), whole 64-position blocks of a swizzled
+// MN-major slab (a short last tile reads the zeros or rows past its own, which
+// the epilogue does not store).
+__device__ __forceinline__ int tile_ntp(const TapParams &p, int NT) {
+    return p.mnb == 2 ? (NT + 63) / 64 * 64 : (NT + p.stack + 15) / 16 * 16;
 }
 __device__ __forceinline__ int tile_n0(const TapParams &p, int NTp) {
-    return min(NTp, split_n0((p.Qmax * p.pitch + p.stack + 15) / 16 * 16));
+    return min(NTp, split_n0((p.Qmax * p.pitch + p.stack + 15) / 16 * 16, p.mnb == 2 ? 64 : 32));
 }
 
 // Slab row and column offsets of filter tap (r, j) (dilation; see TapParams).
@@ -459,7 +476,7 @@ __host__ __device__ inline int tap_dc(int j, int dil_w, int g_w) { return (j / g
 
 template <int MODE>
 __device__ __forceinline__ uint32_t tap_offset(const TapParams &p, int t) {
-    if (MODE == TAP_CH && p.mnb) return (uint32_t)t * 256u;  // K step t of an MN-major slab
+    if (MODE == TAP_CH && p.mnb) return (uint32_t)t * (p.mnb == 2 ? 2048u : 256u);  // K step t, MN-major slab
     if (MODE == TAP_CH || MODE == TAP_CL) {
         const int r = t / p.W_f, j = t - r * p.W_f;
         const int dr = tap_dr(r, p.dil_h), dc = tap_dc(j, p.dil_w, p.g_w);
@@ -608,9 +625,12 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             int k = 0;
             int sb = 0, sa = 0;
             uint32_t phb = 0, pha = 0;
-            // (an MN-major slab: K halves lbo = 128 bytes apart, position groups 256)
+            // (an MN-major slab: K halves lbo = 128 bytes apart, position groups 256*mn_k;
+            // swizzled: 64-position blocks lbo apart, 8-channel groups 1024 bytes,
+            // layout type 2 = 128-byte swizzle)
             const uint64_t adesc0 = smem_desc(0, 128, 256),
-                           bdesc0 = smem_desc(0, p.lbo, p.mnb ? 256u * (uint32_t)p.mn_k : 128u);
+                           bdesc0 = p.mnb == 2 ? (smem_desc(0, p.lbo, 1024u) | (2ull << 61))
+                                               : smem_desc(0, p.lbo, p.mnb ? 256u * (uint32_t)p.mn_k : 128u);
             const uint32_t a_hi = (uint32_t)(adesc0 >> 32), b_hi = (uint32_t)(bdesc0 >> 32);
             const uint32_t a_lo_base = (uint32_t)adesc0 + (smem_u32(sA) >> 4);
             const uint32_t b_lo_base = (uint32_t)bdesc0 + (smem_u32(sB) >> 4);
@@ -640,11 +660,11 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     d_tmem = tmem + (uint32_t)(buf * 256 + which * 128);
                 } else {
                     // stacked: one more column, read by the epilogue for the shifted rows
-                    const int NTp = (tl.Q * p.pitch + p.stack + 15) / 16 * 16;
+                    const int NTp = tile_ntp(p, tl.Q * p.pitch);
                     const int N0 = tile_n0(p, NTp);
                     NW = which == 0 ? N0 : NTp - N0;
                     // slab offset of the issuer's first position, in 16-byte units (MN-major:
-                    // 32 bytes per position)
+                    // 32*mn_k bytes per position, in 8- or 64-position blocks)
                     col0 = which == 0 ? 0u : (uint32_t)N0 * (p.mnb ? 2u * (uint32_t)p.mn_k : 1u);
                     idesc = make_idesc(p.bf16 != 0, BM, NW > 0 ? NW : 16) | (p.mnb ? 1u << 16 : 0u);
                     d_tmem = tmem + (which == 0 ? 0u : (uint32_t)N0);
@@ -898,7 +918,8 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     if (lane == 0 && MODE == TAP_CH) {
                         const uint32_t slab = smem_u32(sB + (size_t)sbt * p.stage_b);
                         mbar_arrive_expect_tx(full_b(sbt), bytes);
-                        tma_load_4d(slab, &p.tmap_x, 0, c2 * 16 * p.mn_k, (t2.ho0 * p.W_o) >> 3, t2.n, full_b(sbt));
+                        tma_load_4d(slab, &p.tmap_x, 0, c2 * 16 * p.mn_k, (t2.ho0 * p.W_o) >> (p.mnb == 2 ? 6 : 3),
+                                    t2.n, full_b(sbt));
                     } else if (lane == 0) {
                         const uint32_t slab = smem_u32(sB + (size_t)sbt * p.stage_b);
                         mbar_arrive_expect_tx(full_b(sbt), bytes);
@@ -1251,7 +1272,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
         for (int64_t id = blockIdx.x; id < p.tiles_total; id += gridDim.x) {
             tile_at(p, id, tl);
             const int NT = tl.Q * p.pitch;
-            const int NTp = (NT + p.stack + 15) / 16 * 16;  // the MMAs' columns
+            const int NTp = tile_ntp(p, NT);  // the MMAs' columns
             const int N0 = tile_n0(p, NTp);
             const int pitch = p.pitch, W_o = p.W_o;
             auto off_of = [&](int pp) -> int {
@@ -1649,8 +1670,13 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
         const int64_t NTp = xpose ? (Q * pitch + 1 + 127) / 128 * 128 : (Q * pitch + stack + 15) / 16 * 16;
         const int64_t RR = (Q - 1) * s.s_h + Hfe;  // slab rows under a tile of Q rows
         int64_t PB = 0, lbo, stage_b;
+        // the 128-byte-swizzled MN-major slab where the plane and the tile are whole
+        // 64-position blocks
+        const bool mn_sw = mnb && (s.H_i * s.W_i) % 64 == 0 && (Q * s.W_o) % 64 == 0;
         if (mnb) {
-            lbo = 128;  // the two 8-channel core matrices of a 16-channel K step
+            // the two 8-channel core matrices of a 16-channel K step; swizzled, the
+            // stride of the 64-position blocks
+            lbo = mn_sw ? 2048 * mn_k : 128;
             stage_b = NTp * 32 * mn_k;
         } else if (chan) {
             const int64_t HH = (RR + s.s_h - 1) / s.s_h;
@@ -1764,7 +1790,7 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
                     p.raw_elems = (int)raw_e;
                     p.ring = ring;
                     p.raw_slot = (int)slot_e;
-                    p.mnb = mnb ? 1 : 0;
+                    p.mnb = mnb ? (mn_sw ? 2 : 1) : 0;
                     p.mn_box = (int)NTp;
                     p.mn_k = (int)mn_k;
                     p.raw_rows = (int)(pad ? Rb : RR);
@@ -1972,7 +1998,7 @@ bool conv_tc_plan_info(const Shape &s, bool fused, int layout, int64_t sms, TcPl
     if (p.stack) {
         walk(0, (NT + 15) / 16 * 16);
     } else {
-        const int N0 = split_n0(NTp);
+        const int N0 = split_n0(NTp, p.mnb == 2 ? 64 : 32);
         walk(0, N0);
         walk(N0, NTp);
     }
@@ -2051,23 +2077,28 @@ static bool encode_slab_map(TapParams &p, const void *src) {
     return r == CUDA_SUCCESS;
 }
 
-// The tensor map of an MN-major 1x1 slab (mnb): the input as a 4-D tensor (8,
-// C_i, H_i*W_i/8, N) — eight consecutive positions, channels, position groups,
-// images — box (8, 16, mn_box/8, 1), zero fill outside (past the plane's last
-// group, channels past C_i). The planner chose mnb only where the plane is whole
-// groups; false when the encoder refuses it.
+// The tensor map of an MN-major 1x1 slab (mnb), zero fill outside (past the
+// plane's last position group, channels past C_i); false when the encoder
+// refuses it.
+//  mnb = 1: the input as a 4-D tensor (8, C_i, H_i*W_i/8, N) -- eight consecutive
+//    positions, channels, position groups, images -- box (8, 16*mn_k, mn_box/8, 1).
+//  mnb = 2: the same with 64-position blocks, box (64, 16*mn_k, mn_box/64, 1), and
+//    the copy's 128-byte swizzle (rows of 128 bytes). The planner chose it only
+//    where the plane and every tile are whole blocks.
 static bool encode_mn_map(TapParams &p, const void *src) {
     const int64_t P = (int64_t)p.H_i * p.W_i;
-    if (P % 8 != 0 || p.mn_box % 8 != 0 || p.mn_box / 8 > 256 || (reinterpret_cast<uintptr_t>(src) & 15) != 0)
+    const int64_t G = p.mnb == 2 ? 64 : 8;  // positions per row of the box
+    if (P % G != 0 || p.mn_box % G != 0 || p.mn_box / G > 256 || (reinterpret_cast<uintptr_t>(src) & 15) != 0)
         return false;
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
-    const cuuint64_t dims[4] = {8, (cuuint64_t)p.C_i, (cuuint64_t)(P / 8), (cuuint64_t)p.N_img};
-    const cuuint64_t strides[3] = {(cuuint64_t)P * 2, 16, (cuuint64_t)p.C_i * P * 2};
-    const cuuint32_t box[4] = {8u, 16u * (cuuint32_t)p.mn_k, (cuuint32_t)(p.mn_box / 8), 1u};
+    const cuuint64_t dims[4] = {(cuuint64_t)G, (cuuint64_t)p.C_i, (cuuint64_t)(P / G), (cuuint64_t)p.N_img};
+    const cuuint64_t strides[3] = {(cuuint64_t)P * 2, (cuuint64_t)G * 2, (cuuint64_t)p.C_i * P * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)G, 16u * (cuuint32_t)p.mn_k, (cuuint32_t)(p.mn_box / G), 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     const CUresult r = enc(&p.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(src), dims, strides,
-                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           p.mnb == 2 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

@@ -22,6 +22,9 @@ SMALL = [  # N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w
     # 1x1 filters at stride 1 on rows of whole 8-position groups: the input tile copied
     # MN-major into the slab (channels past C_i and positions past the plane read as zero)
     (2, 40, 12, 16, 72, 1, 1, 1, 1), (1, 32, 40, 24, 64, 1, 1, 1, 1), (1, 16, 5, 8, 128, 1, 1, 1, 1),
+    # ... in 64-position blocks with the copy's 128-byte swizzle (planes and tiles whole
+    # blocks): a tile of one block (no second accumulator), a ragged last tile, three chunks
+    (3, 24, 8, 32, 200, 1, 1, 1, 1), (2, 48, 16, 64, 130, 1, 1, 1, 1), (2, 96, 10, 32, 96, 1, 1, 1, 1),
 ]
 
 
@@ -56,6 +59,24 @@ def test_conv_tc_exact_on_sparse_integers(dt, bound, fused):
     out = _run(x, w, (1, 2), fused)
     want, _ = oracle.conv_direct(to_f64(x), to_f64(w), (1, 2))
     assert np.abs(want).max() <= bound
+    np.testing.assert_array_equal(to_f64(out), want)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["window", "fused"])
+@pytest.mark.parametrize("case", [(2, 40, 12, 16, 72), (2, 48, 16, 64, 130),
+                                  (64, 40, 16, 56, 64), (40, 32, 24, 56, 136)],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_conv_tc_1x1_exact_on_integers(case, fused):
+    """1x1 filters: the MN-major slab, without swizzle (16-position rows) and with the
+    128-byte swizzle (whole 64-position blocks). Sparse integer inputs make every
+    partial sum exact, so the result must equal the oracle exactly: a position or
+    channel read from the wrong place of the slab shows as a mismatch."""
+    N, C_i, H_i, W_i, C_o = case
+    layer = wl.Layer("mn", N, C_i, H_i, W_i, C_o, 1, 1, 1, 1, seed=12)
+    x, w = wl.make_int_inputs(layer, "bf16", seed=24, x_range=1, w_range=1, density=0.5)
+    out = _run(x, w, (1, 1), fused)
+    want, _ = oracle.conv_direct(to_f64(x), to_f64(w), (1, 1))
+    assert np.abs(want).max() <= 256
     np.testing.assert_array_equal(to_f64(out), want)
 
 
