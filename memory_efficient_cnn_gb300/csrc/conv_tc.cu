@@ -378,6 +378,13 @@ struct TapParams {
     //    channels x 64 positions per 1024-byte atom; blocks lbo = 2048*mn_k bytes
     //    apart, 8-channel groups 1024); K steps 2048 bytes apart. The copy then
     //    moves 128-byte rows instead of 16-byte ones.
+    // CL, the same filter with channels in whole 64s (mnb = 3): a chunk is 64
+    // channels (mn_k = 4 K steps) of the tile's mn_box positions, held K-major with
+    // the 128-byte swizzle: one tensor copy of the input seen as (C_i, W_i, H_i, N),
+    // box (64, W_i, rows per tile, 1), writes each position's 64 channels as one
+    // 128-byte row, 16-byte pieces permuted by the row index mod 8 (the MMA's
+    // 128-byte-swizzled K-major layout: 8-position groups 1024 bytes apart); K steps
+    // 32 bytes apart within the rows.
     int mnb, mn_box, mn_k;
     const uint16_t *src;   // NCHW input (CH, WX), window tensor (WW), NHWC input (CL)
     const uint16_t *fa;
@@ -477,6 +484,7 @@ __host__ __device__ inline int tap_dc(int j, int dil_w, int g_w) { return (j / g
 template <int MODE>
 __device__ __forceinline__ uint32_t tap_offset(const TapParams &p, int t) {
     if (MODE == TAP_CH && p.mnb) return (uint32_t)t * (p.mnb == 2 ? 2048u : 256u);  // K step t, MN-major slab
+    if (MODE == TAP_CL && p.mnb == 3) return (uint32_t)t * 32u;  // K step t, swizzled K-major 1x1 slab
     if (MODE == TAP_CH || MODE == TAP_CL) {
         const int r = t / p.W_f, j = t - r * p.W_f;
         const int dr = tap_dr(r, p.dil_h), dc = tap_dc(j, p.dil_w, p.g_w);
@@ -627,9 +635,10 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             uint32_t phb = 0, pha = 0;
             // (an MN-major slab: K halves lbo = 128 bytes apart, position groups 256*mn_k;
             // swizzled: 64-position blocks lbo apart, 8-channel groups 1024 bytes,
-            // layout type 2 = 128-byte swizzle)
+            // layout type 2 = 128-byte swizzle; the swizzled K-major 1x1 slab:
+            // 8-position groups 1024 bytes apart, the leading offset unused)
             const uint64_t adesc0 = smem_desc(0, 128, 256),
-                           bdesc0 = p.mnb == 2 ? (smem_desc(0, p.lbo, 1024u) | (2ull << 61))
+                           bdesc0 = p.mnb >= 2 ? (smem_desc(0, p.lbo, 1024u) | (2ull << 61))
                                                : smem_desc(0, p.lbo, p.mnb ? 256u * (uint32_t)p.mn_k : 128u);
             const uint32_t a_hi = (uint32_t)(adesc0 >> 32), b_hi = (uint32_t)(bdesc0 >> 32);
             const uint32_t a_lo_base = (uint32_t)adesc0 + (smem_u32(sA) >> 4);
@@ -664,9 +673,12 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                     const int N0 = tile_n0(p, NTp);
                     NW = which == 0 ? N0 : NTp - N0;
                     // slab offset of the issuer's first position, in 16-byte units (MN-major:
-                    // 32*mn_k bytes per position, in 8- or 64-position blocks)
-                    col0 = which == 0 ? 0u : (uint32_t)N0 * (p.mnb ? 2u * (uint32_t)p.mn_k : 1u);
-                    idesc = make_idesc(p.bf16 != 0, BM, NW > 0 ? NW : 16) | (p.mnb ? 1u << 16 : 0u);
+                    // 32*mn_k bytes per position, in 8- or 64-position blocks; the swizzled
+                    // K-major 1x1 slab: a 128-byte row per position)
+                    col0 = which == 0 ? 0u
+                                      : (uint32_t)N0 * (p.mnb == 3 ? 8u : p.mnb ? 2u * (uint32_t)p.mn_k : 1u);
+                    idesc = make_idesc(p.bf16 != 0, BM, NW > 0 ? NW : 16) |
+                            ((p.mnb == 1 || p.mnb == 2) ? 1u << 16 : 0u);
                     d_tmem = tmem + (which == 0 ? 0u : (uint32_t)N0);
                 }
                 for (int cc = 0; cc < p.NCH && ok; ++cc) {
@@ -900,7 +912,9 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             // (q, m) being input (row R0 + ph_r + q*s_h, column ph_c + m*s_w - p_w),
             // zero outside the input. An MN-major 1x1 slab (mnb) is one tensor copy of
             // the chunk's 16 channels at the tile's positions (zero past the plane's
-            // end or channel C_i). One thread issues them all on the stage's barrier;
+            // end or channel C_i), a channels-last one (mnb = 3) one copy of the chunk's
+            // 64 channels at the tile's rows (zero past the last input row). One thread
+            // issues them all on the stage's barrier;
             // the other producer warps have nothing to do.
             int sbt = 0;
             uint32_t pht = 0;
@@ -908,6 +922,7 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
             int pend[kMaxSlabStages];  // per stage: parity of a copy not yet seen landed
             for (int s2 = 0; s2 < kMaxSlabStages; ++s2) pend[s2] = -1;
             const uint32_t bytes = MODE == TAP_CH ? (uint32_t)p.mn_box * 32u * (uint32_t)p.mn_k
+                                   : p.mnb == 3   ? (uint32_t)p.mn_box * 128u
                                                   : 2u * (uint32_t)(p.s_h * p.s_w * p.slab_hh * p.pitch) * 16u;
             TapTile t2;
             for (int64_t id2 = blockIdx.x; ok2 && id2 < p.tiles_total; id2 += gridDim.x) {
@@ -920,6 +935,11 @@ __global__ void __launch_bounds__(TAP_THREADS, 1) conv_tc_tap_kernel(const __gri
                         mbar_arrive_expect_tx(full_b(sbt), bytes);
                         tma_load_4d(slab, &p.tmap_x, 0, c2 * 16 * p.mn_k, (t2.ho0 * p.W_o) >> (p.mnb == 2 ? 6 : 3),
                                     t2.n, full_b(sbt));
+                    } else if (lane == 0 && p.mnb == 3) {
+                        // channels-last 1x1: 64 channels of every position of the tile's rows
+                        const uint32_t slab = smem_u32(sB + (size_t)sbt * p.stage_b);
+                        mbar_arrive_expect_tx(full_b(sbt), bytes);
+                        tma_load_4d(slab, &p.tmap_x, c2 * 64, 0, t2.ho0, t2.n, full_b(sbt));
                     } else if (lane == 0) {
                         const uint32_t slab = smem_u32(sB + (size_t)sbt * p.stage_b);
                         mbar_arrive_expect_tx(full_b(sbt), bytes);
@@ -1632,10 +1652,16 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
     // chunk of 16*mn_k channels
     const bool mnb = mode == TAP_CH && s.H_f == 1 && s.W_f == 1 && s.s_h == 1 && s.s_w == 1 && plain(s) &&
                      s.W_o % 8 == 0;
-    const int64_t mn_k = mnb ? std::min<int64_t>(kMnK, (s.C_i + 15) / 16) : 1;
+    // the same filter channels-last, with channels in whole 64s: a chunk's slab is 64
+    // channels of the tile's rows, copied K-major (one 128-byte row per position, the
+    // copy's 128-byte swizzle) by one tensor copy per chunk
+    const bool kmb = mode == TAP_CL && s.H_f == 1 && s.W_f == 1 && s.s_h == 1 && s.s_w == 1 && plain(s) &&
+                     s.C_i % 64 == 0 && s.W_i % 8 == 0 && s.W_i <= 256;
+    const bool copy1 = mnb || kmb;  // a 1x1 slab by one tensor copy per chunk
+    const int64_t mn_k = mnb ? std::min<int64_t>(kMnK, (s.C_i + 15) / 16) : kmb ? 4 : 1;
     if (chan) {
         pitch = (Wp + s.s_w - 1) / s.s_w;
-        T = mnb ? mn_k : stack ? s.H_f * Gr : s.H_f * s.W_f;
+        T = copy1 ? mn_k : stack ? s.H_f * Gr : s.H_f * s.W_f;
         NCH = (s.C_i + 16 * mn_k - 1) / (16 * mn_k);
     } else {
         S = s.s_w * s.H_f;
@@ -1678,6 +1704,9 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
             // stride of the 64-position blocks
             lbo = mn_sw ? 2048 * mn_k : 128;
             stage_b = NTp * 32 * mn_k;
+        } else if (kmb) {
+            lbo = 16;  // (unused: a K step lies within the 128-byte rows)
+            stage_b = NTp * 128;
         } else if (chan) {
             const int64_t HH = (RR + s.s_h - 1) / s.s_h;
             // a multiple of 128 bytes, so that every polyphase block of a stage can be the
@@ -1741,13 +1770,13 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
             const int tg = (int)std::min<int64_t>(TG, T);
             if (TG > T && TG != 1) continue;
             if (pass == 0 && !xpose && tg < std::min<int64_t>(T, 8)) continue;
-            // an MN-major 1x1 slab is small and each stage is one tensor copy in flight:
-            // up to six stages, as many filter stages (one tap each)
-            const int bst_list[4] = {mnb ? 6 : 3, mnb ? 4 : 2, mnb ? 3 : 0, mnb ? 2 : 0};
+            // a 1x1 slab copied by tensor copies: each stage is one copy in flight; up
+            // to six stages, as many filter stages (a chunk's K steps each)
+            const int bst_list[4] = {copy1 ? 6 : 3, copy1 ? 4 : 2, copy1 ? 3 : 0, copy1 ? 2 : 0};
             for (int BST : bst_list) {
               if (BST == 0) continue;
               for (int AST : ast_list) {
-                if (AST == 0 || (mnb ? AST != BST : AST == 6)) continue;
+                if (AST == 0 || (copy1 ? AST != BST : AST == 6)) continue;
                 for (int pad : {1, 0}) {
                     if (pad && !(mode == TAP_CH && ring)) continue;
                     const int64_t slot_e = slot_elems(pad != 0);
@@ -1790,8 +1819,8 @@ TapPlan plan_tap_epi(const Shape &s, int mode, int64_t sms, int epi_blocks, bool
                     p.raw_elems = (int)raw_e;
                     p.ring = ring;
                     p.raw_slot = (int)slot_e;
-                    p.mnb = mnb ? (mn_sw ? 2 : 1) : 0;
-                    p.mn_box = (int)NTp;
+                    p.mnb = mnb ? (mn_sw ? 2 : 1) : kmb ? 3 : 0;
+                    p.mn_box = (int)(kmb ? Q * s.W_i : NTp);  // positions of a tile's copy
                     p.mn_k = (int)mn_k;
                     p.raw_rows = (int)(pad ? Rb : RR);
                     p.raw_w = (int)(pad ? Wb : s.W_i);
@@ -2103,6 +2132,26 @@ static bool encode_mn_map(TapParams &p, const void *src) {
     return r == CUDA_SUCCESS;
 }
 
+// The tensor map of a channels-last K-major 1x1 slab (mnb = 3): the input as
+// (C_i, W_i, H_i, N), box (64, W_i, Qmax, 1) -- 64 channels of every position of
+// a tile's rows -- with the copy's 128-byte swizzle; rows past H_i read as zero.
+// False when the shape or the encoder refuses it.
+static bool encode_kmb_map(TapParams &p, const void *src) {
+    if (p.C_i % 64 != 0 || p.W_i > 256 || p.Qmax > 256 || (reinterpret_cast<uintptr_t>(src) & 15) != 0)
+        return false;
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t W = (cuuint64_t)p.W_i, H = (cuuint64_t)p.H_i, C = (cuuint64_t)p.C_i;
+    const cuuint64_t dims[4] = {C, W, H, (cuuint64_t)p.N_img};
+    const cuuint64_t strides[3] = {C * 2, W * C * 2, H * W * C * 2};
+    const cuuint32_t box[4] = {64u, (cuuint32_t)p.W_i, (cuuint32_t)p.Qmax, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUresult r = enc(&p.tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void *>(src), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *filt, void *out,
                               void *ws, const Shape &s, int layout, bool bf16, cudaStream_t st) {
     TapParams p = pl.p;
@@ -2132,9 +2181,15 @@ static cudaError_t launch_tap(const TapPlan &pl, const void *src, const void *fi
         p.vec = (p.C_i % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
     if (pl.mode == TAP_CH && !p.vec) p.ring = 0;  // 16-byte copies need 16-byte rows
     p.tma_raw = (pl.mode == TAP_CH && p.ring && !p.mnb && encode_raw_map(p, src)) ? 1 : 0;
-    if (p.mnb && !encode_mn_map(p, src)) return cudaErrorInvalidValue;
+    if (pl.mode == TAP_CH && p.mnb && !encode_mn_map(p, src)) return cudaErrorInvalidValue;
     if (!p.tma_raw) p.raw_w = p.W_i;  // per-channel bulk copies: contiguous rows
-    p.tma_slab = (pl.mode == TAP_CL && p.vec && encode_slab_map(p, src)) ? 1 : 0;
+    if (pl.mode == TAP_CL && p.mnb == 3) {
+        // the plan's slab layout is the swizzled copy's: no other fill writes it
+        if (!p.vec || !encode_kmb_map(p, src)) return cudaErrorInvalidValue;
+        p.tma_slab = 1;
+    } else {
+        p.tma_slab = (pl.mode == TAP_CL && p.vec && encode_slab_map(p, src)) ? 1 : 0;
+    }
     p.div_pitch = make_fastdiv((uint32_t)p.pitch);
     p.div_cgs = make_fastdiv((uint32_t)std::max(1, p.W_i / 8));
     p.div_sh = make_fastdiv((uint32_t)p.s_h);

@@ -102,6 +102,11 @@ SMALL = [  # N, C_i, H_i, W_i, C_o, H_f, W_f, s_h, s_w
     (1, 3, 32, 32, 8, 3, 3, 1, 1), (2, 3, 47, 45, 96, 11, 11, 4, 4), (2, 5, 30, 33, 37, 3, 7, 1, 2),
     (2, 12, 19, 40, 20, 3, 4, 1, 1), (1, 100, 12, 13, 30, 3, 3, 1, 1), (1, 1, 50, 3, 1, 2, 3, 3, 1),
     (3, 17, 12, 14, 130, 1, 1, 1, 1),
+    # 1x1 filters with channels in whole 64s: 64-channel chunks copied K-major with the
+    # copy's 128-byte swizzle (tiles past the last row, positions past a box, no second
+    # accumulator, three chunks, 256-position rows)
+    (2, 64, 12, 16, 72, 1, 1, 1, 1), (3, 128, 9, 24, 200, 1, 1, 1, 1), (1, 192, 5, 40, 64, 1, 1, 1, 1),
+    (2, 64, 7, 8, 130, 1, 1, 1, 1), (1, 64, 3, 256, 96, 1, 1, 1, 1),
 ]
 
 
@@ -123,7 +128,9 @@ def test_conv_nhwc_small(case, dt, fused):
                                   (1, 40, 21, 29, 64, 7, 7, 2, 2), (2, 12, 19, 40, 20, 3, 4, 1, 1),
                                   # stacked tiles of two M blocks; many tiles per CTA
                                   (1, 24, 12, 150, 48, 5, 3, 1, 2), (2, 16, 9, 200, 64, 3, 4, 1, 1),
-                                  (160, 8, 9, 200, 16, 3, 4, 1, 1)],
+                                  (160, 8, 9, 200, 16, 3, 4, 1, 1),
+                                  # 1x1, 64-channel swizzled K-major chunks; several tiles per CTA
+                                  (2, 64, 12, 16, 72, 1, 1, 1, 1), (40, 64, 24, 56, 136, 1, 1, 1, 1)],
                          ids=lambda c: "x".join(map(str, c)))
 def test_conv_nhwc_exact_on_sparse_integers(case, fused):
     """Sparse +-1 inputs: every fp32 partial sum is an exact small integer and the
@@ -169,7 +176,7 @@ def test_conv_nhwc_status_ok_and_no_write_past_output():
 
 
 @pytest.mark.parametrize("layer,dt", [(wl.CV1, "f16"), (wl.CV1, "f32"), (wl.CV4, "f16"), (wl.CV5, "bf16"),
-                                      (wl.SWEEP[1], "bf16"), (wl.SWEEP[4], "bf16")],
+                                      (wl.SWEEP[0], "bf16"), (wl.SWEEP[1], "bf16"), (wl.SWEEP[4], "bf16")],
                          ids=lambda v: getattr(v, "name", v))
 def test_conv_nhwc_full_size_sampled(layer, dt):
     x, w = wl.make_inputs(layer, dt)
