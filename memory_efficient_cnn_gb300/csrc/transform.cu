@@ -521,6 +521,7 @@ struct TNParams {
     int C_i, H_i, W_i, H_f, s_h, H_o;
     int VPR;              // vectors per run (vector path: C_i*esz / 16)
     FastDiv div_vpr, div_wh, div_hf, div_ho;
+    FastDiv div_lp, div_c;  // staged path: window row length, channels
     int T, tiles;         // staged path: output rows per band, bands per image
     int64_t x_elems;      // staged path: elements of x
 };
@@ -644,9 +645,9 @@ __global__ void __launch_bounds__(256) transform_nhwc_staged(TNParams p) {
     // staged index of band element g (g = t*Lp + (w*H_f + r)*C + c)
     const int Lp = (int)p.Lp;
     auto staged = [&](int g) -> int {
-        const int t = g / Lp, o = g - t * Lp;
-        const int pos = o / C, c = o - pos * C;
-        const int w = pos / H_f, r = pos - w * H_f;
+        const int t = (int)fdiv((uint32_t)g, p.div_lp), o = g - t * Lp;
+        const int pos = (int)fdiv((uint32_t)o, p.div_c), c = o - pos * C;
+        const int w = (int)fdiv((uint32_t)pos, p.div_hf), r = pos - w * H_f;
         return (t * p.s_h + r) * RL + w * C + c + lead;
     };
     const int64_t f0 = ((int64_t)n * p.H_o + ho0) * Lp;
@@ -656,12 +657,13 @@ __global__ void __launch_bounds__(256) transform_nhwc_staged(TNParams p) {
     for (int64_t e = f0 + threadIdx.x; e < head; e += 256) win[e] = s_in[staged((int)(e - f0))];
     for (int64_t e = vend + threadIdx.x; e < f1; e += 256) win[e] = s_in[staged((int)(e - f0))];
     for (int64_t vv = head / V + threadIdx.x; vv < vend / V; vv += 256) {
+        // (the vector's first element, by multiply-shift divisions)
         const int g = (int)(vv * V - f0);
-        int t = g / Lp;
+        int t = (int)fdiv((uint32_t)g, p.div_lp);
         const int o = g - t * Lp;
-        const int pos = o / C;
+        const int pos = (int)fdiv((uint32_t)o, p.div_c);
         int c = o - pos * C;
-        int w = pos / H_f, r = pos - w * H_f;
+        int w = (int)fdiv((uint32_t)pos, p.div_hf), r = pos - w * H_f;
         int src = (t * p.s_h + r) * RL + w * C + c + lead;
         union {
             uint4 u;
@@ -864,6 +866,8 @@ cudaError_t launch_transform_nhwc(const void *x, void *win, const Shape &s, int 
     p.div_wh = make_fastdiv((uint32_t)(s.W_i * s.H_f));
     p.div_hf = make_fastdiv((uint32_t)s.H_f);
     p.div_ho = make_fastdiv((uint32_t)s.H_o);
+    p.div_lp = make_fastdiv((uint32_t)p.Lp);
+    p.div_c = make_fastdiv((uint32_t)s.C_i);
     if (p.vecs == 0) return cudaSuccess;
     if (staged) {
         const size_t smem = (size_t)(((T - 1) * s.s_h + s.H_f) * RLb + 16 + 15) / 16 * 16;
